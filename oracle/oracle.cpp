@@ -1,0 +1,183 @@
+// oracle.cpp — plain fp64 CPU primitives for the parallel transformer block oracle.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call this
+// library: only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg do.
+// It shares no code, header, table or helper with the CUDA path.
+//
+// The method (MegaScale: Scaling Large Language Model Training to More Than 10,000 GPUs,
+// reading notes, section 1.1 "Parallel Transformer Block", eq. (4)) is
+//     y = x + MLP(LN(x)) + Attention(LN(x)),
+// with the MLP of the Megatron-LM tensor-parallel notes (section 2.1: Y = GeLU(XA)B,
+// A:[h,4h], B:[4h,h]) and sliding-window attention (section 1.1 "Sliding Window
+// Attention", eqs. (5)-(6): each token attends to the most recent w tokens).
+//
+// Every routine here computes its textbook definition directly, in double precision,
+// with no rounding to bf16 anywhere. The block itself is composed step by step, in the
+// pages' order, by oracle/oracle.py.
+//
+// Threads: rows are split into contiguous ranges, one per std::thread. Splitting rows
+// changes no arithmetic: every output element is computed by one thread, summing its
+// terms in ascending index order.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+int resolve_threads(int requested) {
+  if (requested > 0) return requested;
+  unsigned hc = std::thread::hardware_concurrency();
+  return hc == 0 ? 1 : (int)hc;
+}
+
+// Calls body(begin, end) on `threads` contiguous slices of [0, n).
+template <class Body>
+void for_row_ranges(int64_t n, int threads, Body body) {
+  threads = resolve_threads(threads);
+  if (n <= 0) return;
+  if (threads > n) threads = (int)n;
+  if (threads == 1) {
+    body((int64_t)0, n);
+    return;
+  }
+  std::vector<std::thread> pool;
+  pool.reserve(threads);
+  for (int t = 0; t < threads; ++t) {
+    int64_t b = n * t / threads, e = n * (t + 1) / threads;
+    pool.emplace_back([=] { body(b, e); });
+  }
+  for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Number of worker threads a call with `requested` (<= 0: all hardware threads) uses.
+int oracle_threads(int requested) { return resolve_threads(requested); }
+
+// LayerNorm over the last dimension (the "LN" of eq. (4)):
+//   mu = mean_c x[r,c];  var = mean_c (x[r,c] - mu)^2   (biased, divide by H)
+//   out[r,c] = (x[r,c] - mu) / sqrt(var + eps) * gamma[c] + beta[c]
+void oracle_layernorm(int64_t rows, int64_t H, const double* x, const double* gamma,
+                      const double* beta, double eps, double* out, int threads) {
+  for_row_ranges(rows, threads, [=](int64_t r0, int64_t r1) {
+    for (int64_t r = r0; r < r1; ++r) {
+      const double* xr = x + r * H;
+      double sum = 0.0;
+      for (int64_t c = 0; c < H; ++c) sum += xr[c];
+      const double mu = sum / (double)H;
+      double sq = 0.0;
+      for (int64_t c = 0; c < H; ++c) sq += (xr[c] - mu) * (xr[c] - mu);
+      const double var = sq / (double)H;
+      const double inv = 1.0 / std::sqrt(var + eps);
+      double* o = out + r * H;
+      for (int64_t c = 0; c < H; ++c) o[c] = (xr[c] - mu) * inv * gamma[c] + beta[c];
+    }
+  });
+}
+
+// Linear layer in the pages' convention Y = X W (Megatron-LM notes section 2.1, with W
+// stored [in, out] row-major):
+//   C[i, j] = bias[j] + sum_{k=0}^{K-1} A[i, k] * W[k, j]      (bias may be NULL)
+// A is [M, K] with row stride lda, W is [K, N] with row stride ldw, C is [M, N] with
+// row stride ldc. Rows are visited 16 at a time and columns 512 at a time so that each
+// weight element fetched from memory serves 16 rows; within that, every C[i, j] still
+// adds its K products in ascending k, starting from the bias (or 0).
+void oracle_linear(int64_t M, int64_t K, int64_t N, const double* A, int64_t lda,
+                   const double* W, int64_t ldw, const double* bias, double* C, int64_t ldc,
+                   int threads) {
+  const int64_t RB = 16, CB = 512;
+  const int64_t n_groups = (M + RB - 1) / RB;
+  for_row_ranges(n_groups, threads, [=](int64_t g0, int64_t g1) {
+    for (int64_t g = g0; g < g1; ++g) {
+      const int64_t i0 = g * RB, i1 = std::min(M, i0 + RB);
+      for (int64_t j0 = 0; j0 < N; j0 += CB) {
+        const int64_t j1 = std::min(N, j0 + CB);
+        for (int64_t i = i0; i < i1; ++i)
+          for (int64_t j = j0; j < j1; ++j) C[i * ldc + j] = bias ? bias[j] : 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+          const double* wk = W + k * ldw;
+          for (int64_t i = i0; i < i1; ++i) {
+            const double a = A[i * lda + k];
+            double* ci = C + i * ldc;
+            for (int64_t j = j0; j < j1; ++j) ci[j] += a * wk[j];
+          }
+        }
+      }
+    }
+  });
+}
+
+// Exact GeLU (the activation of Y = GeLU(XA)B): gelu(z) = z * Phi(z) = 0.5 z (1 + erf(z/sqrt 2)).
+void oracle_gelu(int64_t n, const double* in, double* out, int threads) {
+  const double inv_sqrt2 = 0.70710678118654752440;
+  for_row_ranges(n, threads, [=](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i) out[i] = 0.5 * in[i] * (1.0 + std::erf(in[i] * inv_sqrt2));
+  });
+}
+
+// Sliding-window causal multi-head attention for ONE sequence (eqs. (5)-(6): each token
+// attends only to the most recent w tokens, itself included).
+//
+// Queries: nq rows at sequence positions q_pos[]; keys/values: nk rows at positions
+// k_pos[]. q, k, v and out are row-major with row length nh*dh; head j owns columns
+// [j*dh, (j+1)*dh). Key kk is visible to query qq iff 0 <= q_pos[qq] - k_pos[kk] < w.
+// For every query row and head:
+//   s_kk = (q . k_kk) / sqrt(dh) for visible keys, -inf otherwise
+//   p    = exp(s - max s) / sum exp(s - max s)                 (explicit softmax)
+//   out  = sum_kk p_kk v_kk
+// A query with no visible key (impossible when its own position is among k_pos) gets 0.
+void oracle_swa_attention(int64_t nq, const int64_t* q_pos, const double* q, int64_t nk,
+                          const int64_t* k_pos, const double* k, const double* v, int64_t nh,
+                          int64_t dh, int64_t w, double* out, int threads) {
+  const int64_t H = nh * dh;
+  const double scale = 1.0 / std::sqrt((double)dh);
+  const double neg_inf = -std::numeric_limits<double>::infinity();
+  for_row_ranges(nq, threads, [=](int64_t r0, int64_t r1) {
+    std::vector<double> s(nk > 0 ? nk : 1);
+    for (int64_t qi = r0; qi < r1; ++qi) {
+      for (int64_t head = 0; head < nh; ++head) {
+        const double* qr = q + qi * H + head * dh;
+        double smax = neg_inf;
+        for (int64_t kk = 0; kk < nk; ++kk) {
+          const int64_t dist = q_pos[qi] - k_pos[kk];
+          if (dist < 0 || dist >= w) {
+            s[kk] = neg_inf;
+            continue;
+          }
+          const double* kr = k + kk * H + head * dh;
+          double dot = 0.0;
+          for (int64_t d = 0; d < dh; ++d) dot += qr[d] * kr[d];
+          s[kk] = dot * scale;
+          smax = std::max(smax, s[kk]);
+        }
+        double* o = out + qi * H + head * dh;
+        for (int64_t d = 0; d < dh; ++d) o[d] = 0.0;
+        if (smax == neg_inf) continue;
+        double denom = 0.0;
+        for (int64_t kk = 0; kk < nk; ++kk) {
+          s[kk] = (s[kk] == neg_inf) ? 0.0 : std::exp(s[kk] - smax);
+          denom += s[kk];
+        }
+        for (int64_t kk = 0; kk < nk; ++kk) {
+          if (s[kk] == 0.0) continue;
+          const double p = s[kk] / denom;
+          const double* vr = v + kk * H + head * dh;
+          for (int64_t d = 0; d < dh; ++d) o[d] += p * vr[d];
+        }
+      }
+    }
+  });
+}
+
+// Elementwise sum of n-vectors: out = a + b + c (the three terms of eq. (4)).
+void oracle_add3(int64_t n, const double* a, const double* b, const double* c, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = a[i] + b[i] + c[i];
+}
+
+}  // extern "C"

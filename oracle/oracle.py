@@ -1,0 +1,262 @@
+"""fp64 CPU oracle for the parallel transformer block forward pass.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py``; never by the product package. It shares no code with the
+CUDA path (it does not import ``transformer_block_gb300``).
+
+What it computes (MegaScale reading notes, section 1.1, eq. (4)):
+
+    y = x + MLP(LN(x)) + Attention(LN(x))
+
+step by step, in the pages' order, with the ORIGINAL separate weights:
+
+1. ``xn = LN(x)`` -- LayerNorm with gamma/beta, one LN shared by both branches (eq. (4)).
+2. ``q = xn Wq``, ``k = xn Wk``, ``v = xn Wv`` (columns [Q | K | V] of Wqkv, the
+   ``[b, s, 3h]`` projection of the Megatron-LM notes, section 2.2) and ``h = xn W1``
+   (section 2.1, ``Y = GeLU(XA)B``), four separate matmuls, optional biases.
+3. Per sequence, head and query: explicit masked softmax over the most recent ``w``
+   tokens, self included (section 1.1, eqs. (5)-(6)), scale ``1/sqrt(dh)``.
+4. ``attn = concat_heads(o) Wo``, ``mlp = GeLU(h) W2``.
+5. ``y = x + mlp + attn``.
+
+All arithmetic is float64 in oracle.cpp (built here with g++); inputs are the exact
+bf16 values the GPU receives, passed as float32/float64 arrays.
+
+Row sampling (``rows=``): output row ``i`` of sequence ``b`` depends only on rows
+``max(0, i-w+1) .. i`` of the same sequence (the window), so the oracle can compute a
+chosen set of output rows exactly from that cone. ``stack_forward(prefix=P)`` uses
+causality the same way: the first ``P`` rows of every layer depend only on the first
+``P`` input rows.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile oracle.cpp into a shared library with g++ (no GPU, no CUDA)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", src, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(lib):
+    d, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.oracle_threads.argtypes = [i32]
+    lib.oracle_threads.restype = i32
+    lib.oracle_layernorm.argtypes = [i64, i64, d, d, d, ctypes.c_double, d, i32]
+    lib.oracle_linear.argtypes = [i64, i64, i64, d, i64, d, i64, d, d, i64, i32]
+    lib.oracle_gelu.argtypes = [i64, d, d, i32]
+    lib.oracle_swa_attention.argtypes = [i64, d, d, i64, d, d, d, i64, i64, i64, d, i32]
+    lib.oracle_add3.argtypes = [i64, d, d, d, d]
+    for f in ("oracle_layernorm", "oracle_linear", "oracle_gelu", "oracle_swa_attention",
+              "oracle_add3"):
+        getattr(lib, f).restype = None
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library; ``path`` loads another build."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+@dataclass(frozen=True)
+class Dims:
+    batch: int
+    seq: int
+    hidden: int
+    heads: int
+    head_dim: int
+    ffn: int
+    window: int
+    ln_eps: float = 1e-5
+
+
+# ----------------------------------------------------------------------------- primitives
+
+
+def threads_used(threads: int = 0, lib=None) -> int:
+    return (lib or load()).oracle_threads(threads)
+
+
+def layernorm(x, gamma, beta, eps, threads=0, lib=None) -> np.ndarray:
+    lib = lib or load()
+    x, g, b = _f64(x), _f64(gamma), _f64(beta)
+    rows, H = x.shape
+    out = np.empty_like(x)
+    lib.oracle_layernorm(rows, H, _ptr(x), _ptr(g), _ptr(b), float(eps), _ptr(out), threads)
+    return out
+
+
+def linear(a, w, bias=None, threads=0, lib=None) -> np.ndarray:
+    """``a [M, K] @ w [K, N] (+ bias [N])`` in float64."""
+    lib = lib or load()
+    a, w = _f64(a), _f64(w)
+    M, K = a.shape
+    K2, N = w.shape
+    assert K == K2, (a.shape, w.shape)
+    b = None if bias is None else _f64(bias)
+    out = np.empty((M, N), dtype=np.float64)
+    lib.oracle_linear(M, K, N, _ptr(a), K, _ptr(w), N, None if b is None else _ptr(b),
+                      _ptr(out), N, threads)
+    return out
+
+
+def gelu(z, threads=0, lib=None) -> np.ndarray:
+    lib = lib or load()
+    z = _f64(z)
+    out = np.empty_like(z)
+    lib.oracle_gelu(z.size, _ptr(z), _ptr(out), threads)
+    return out
+
+
+def swa_attention(q, q_pos, k, v, k_pos, heads, head_dim, window, threads=0, lib=None):
+    """Sliding-window causal attention of one sequence; positions index the sequence."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    qp = np.ascontiguousarray(q_pos, dtype=np.int64)
+    kp = np.ascontiguousarray(k_pos, dtype=np.int64)
+    out = np.empty_like(q)
+    lib.oracle_swa_attention(q.shape[0], _ptr(qp), _ptr(q), k.shape[0], _ptr(kp), _ptr(k),
+                             _ptr(v), heads, head_dim, window, _ptr(out), threads)
+    return out
+
+
+# ----------------------------------------------------------------------------- the block
+
+
+def _param(params, name):
+    t = params.get(name)
+    return None if t is None else _f64(t)
+
+
+def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads: int = 0,
+                  keep_stages: bool = False, lib=None):
+    """One parallel transformer block (eq. (4)) in float64.
+
+    ``x``: ``[B, S, H]``; ``params``: ``ln_gamma, ln_beta [H]``, ``wqkv [H, 3H]``,
+    ``w1 [H, F]``, ``wo [H, H]``, ``w2 [F, H]`` (all ``Y = X W``, ``[in, out]``) and
+    optional ``b_qkv [3H]``, ``b1 [F]``, ``b_o [H]``, ``b2 [H]``.
+
+    ``rows=None`` returns ``y [B, S, H]``. ``rows={b: positions}`` returns only those
+    output rows, ``[sum_b len(positions), H]``, ordered by ``b`` then position.
+    ``keep_stages=True`` also returns the intermediates of step 1-4 for the same rows.
+    """
+    lib = lib or load()
+    B, S, H = dims.batch, dims.seq, dims.hidden
+    nh, dh, F, w = dims.heads, dims.head_dim, dims.ffn, dims.window
+    assert nh * dh == H
+    x = np.asarray(x).reshape(B, S, H)
+
+    # Which query rows are wanted, and which rows their windows reach (the cone).
+    want, cone = {}, {}
+    for b in range(B):
+        if rows is None:
+            pos = np.arange(S, dtype=np.int64)
+            need = pos
+        else:
+            pos = np.unique(np.asarray(rows.get(b, []), dtype=np.int64))
+            if pos.size == 0:
+                continue
+            assert pos.min() >= 0 and pos.max() < S
+            mask = np.zeros(S, dtype=bool)
+            for i in pos:
+                mask[max(0, i - w + 1): i + 1] = True
+            need = np.nonzero(mask)[0].astype(np.int64)
+        want[b], cone[b] = pos, need
+
+    gamma, beta = _param(params, "ln_gamma"), _param(params, "ln_beta")
+    wqkv = params["wqkv"]
+    bqkv = _param(params, "b_qkv")
+    bq, bk, bv = (None, None, None) if bqkv is None else (bqkv[:H], bqkv[H:2 * H], bqkv[2 * H:])
+
+    cone_x = np.concatenate([x[b][cone[b]] for b in want]) if want else np.zeros((0, H))
+    # 1. one LayerNorm, shared by both branches
+    xn_cone = layernorm(cone_x, gamma, beta, dims.ln_eps, threads, lib)
+    # rows of the cone that are wanted queries
+    sel, off = [], 0
+    for b in want:
+        sel.append(off + np.searchsorted(cone[b], want[b]))
+        off += cone[b].size
+    sel = np.concatenate(sel) if sel else np.zeros(0, dtype=np.int64)
+    xn_q = xn_cone[sel]
+
+    # 2. four separate projections
+    q = linear(xn_q, wqkv[:, 0:H], bq, threads, lib)
+    k = linear(xn_cone, wqkv[:, H:2 * H], bk, threads, lib)
+    v = linear(xn_cone, wqkv[:, 2 * H:3 * H], bv, threads, lib)
+    h = linear(xn_q, params["w1"], _param(params, "b1"), threads, lib)
+
+    # 3. sliding-window attention, per sequence
+    attn = np.empty_like(q)
+    qoff, koff = 0, 0
+    for b in want:
+        nq, nk = want[b].size, cone[b].size
+        attn[qoff:qoff + nq] = swa_attention(q[qoff:qoff + nq], want[b], k[koff:koff + nk],
+                                             v[koff:koff + nk], cone[b], nh, dh, w, threads, lib)
+        qoff += nq
+        koff += nk
+
+    # 4. the two output projections
+    g = gelu(h, threads, lib)
+    mlp = linear(g, params["w2"], _param(params, "b2"), threads, lib)
+    att = linear(attn, params["wo"], _param(params, "b_o"), threads, lib)
+
+    # 5. residual sum of the three terms of eq. (4)
+    xq = _f64(np.concatenate([x[b][want[b]] for b in want]) if want else np.zeros((0, H)))
+    y = np.empty_like(xq)
+    lib.oracle_add3(y.size, _ptr(xq), _ptr(mlp), _ptr(att), _ptr(y))
+    if rows is None:
+        y = y.reshape(B, S, H)
+    if not keep_stages:
+        return y
+    stages = {"xn": xn_q, "q": q, "k": k[sel], "v": v[sel], "h": h, "gelu_h": g,
+              "attn": attn, "mlp": mlp, "att_proj": att}
+    return y, stages
+
+
+def stack_forward(dims: Dims, x, layers: list, prefix: int | None = None, threads: int = 0,
+                  lib=None):
+    """``len(layers)`` blocks applied in turn, ``x_{l+1} = block_l(x_l)`` (float64 between
+    layers). ``prefix=P`` computes only the first ``P`` rows of every sequence, which by
+    causality equal the first ``P`` rows of the full computation."""
+    lib = lib or load()
+    x = _f64(np.asarray(x).reshape(dims.batch, dims.seq, dims.hidden))
+    if prefix is not None:
+        x = np.ascontiguousarray(x[:, :prefix])
+        dims = Dims(dims.batch, prefix, dims.hidden, dims.heads, dims.head_dim, dims.ffn,
+                    dims.window, dims.ln_eps)
+    for p in layers:
+        x = block_forward(dims, x, p, threads=threads, lib=lib)
+    return x

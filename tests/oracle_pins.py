@@ -1,0 +1,331 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+Each ``pin_*`` takes a loaded oracle library and returns ``(ok, detail)``; the test
+suite asserts every pin holds for the real oracle and that each planted mistake (a
+mutated copy of oracle.cpp, see test_oracle_mutants.py) breaks at least one pin.
+
+What pins what:
+* closed forms: GeLU at standard-normal-table points, LayerNorm of a 2-vector,
+  two-key softmax (window 2) as a logistic weight, window 1 returning V exactly;
+* library routines in float64: ``numpy`` matmul, ``torch.nn.functional.layer_norm``,
+  ``F.gelu``, ``F.scaled_dot_product_attention`` (causal, and with an explicit band
+  mask), and a full block restated with them;
+* identities of the method: window >= seq is full causal attention; the concatenated
+  weight form ``x + [attn | GeLU(h)] [Wo ; W2]`` equals the two-branch sum;
+* invariants: LayerNorm statistics, value rows all equal give that value, head
+  permutation, translation of a window, per-row shift of x, batch independence.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from oracle import oracle as O
+
+# Standard normal CDF at a few points, from any printed normal table (textbook values).
+NORMAL_TABLE = {0.0: 0.5, 0.5: 0.6914624612740131, 1.0: 0.8413447460685429,
+                1.96: 0.9750021048517795, 2.0: 0.9772498680518208,
+                -1.0: 0.15865525393145707, -2.0: 0.022750131948179195}
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, tol):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    return err <= tol, f"max|diff|={err:.3e} (tol {tol:g})"
+
+
+# ----------------------------------------------------------------------------- GeLU
+
+
+def pin_gelu_table(lib):
+    z = np.array(list(NORMAL_TABLE.keys()))
+    want = z * np.array(list(NORMAL_TABLE.values()))
+    return _close(O.gelu(z, lib=lib), want, 1e-15)
+
+
+def pin_gelu_library(lib):
+    z = _rng(1).normal(0, 3, 1000)
+    want = F.gelu(torch.from_numpy(z), approximate="none").numpy()
+    return _close(O.gelu(z, lib=lib), want, 1e-14)
+
+
+# ----------------------------------------------------------------------------- LayerNorm
+
+
+def pin_layernorm_two_vector(lib):
+    # x = [1, 3]: mean 2, variance 1 -> normalised [-1, 1] / sqrt(1 + eps)
+    eps = 1e-5
+    x = np.array([[1.0, 3.0]])
+    g, b = np.array([2.0, 3.0]), np.array([0.5, -0.5])
+    s = 1.0 / math.sqrt(1.0 + eps)
+    want = np.array([[-2.0 * s + 0.5, 3.0 * s - 0.5]])
+    return _close(O.layernorm(x, g, b, eps, lib=lib), want, 1e-15)
+
+
+def pin_layernorm_library(lib):
+    r = _rng(2)
+    x = r.normal(0.3, 2.0, (37, 96))
+    g, b = r.normal(1, 0.1, 96), r.normal(0, 0.1, 96)
+    want = F.layer_norm(torch.from_numpy(x), (96,), torch.from_numpy(g), torch.from_numpy(b),
+                        1e-5).numpy()
+    return _close(O.layernorm(x, g, b, 1e-5, lib=lib), want, 1e-12)
+
+
+def pin_layernorm_stats(lib):
+    # Before the affine map each row has mean 0 and variance var / (var + eps).
+    r = _rng(3)
+    x = r.normal(1.0, 0.01, (5, 64))  # small variance so eps matters
+    eps = 1e-5
+    out = O.layernorm(x, np.ones(64), np.zeros(64), eps, lib=lib)
+    var = x.var(axis=1)
+    ok1, d1 = _close(out.mean(axis=1), 0.0, 1e-12)
+    ok2, d2 = _close(out.var(axis=1), var / (var + eps), 1e-12)
+    return ok1 and ok2, d1 + "; " + d2
+
+
+# ----------------------------------------------------------------------------- linear
+
+
+def pin_linear_library(lib):
+    r = _rng(4)
+    a, w, b = r.normal(size=(37, 19)), r.normal(size=(19, 1030)), r.normal(size=1030)
+    return _close(O.linear(a, w, b, lib=lib), a @ w + b, 1e-12)
+
+
+# ----------------------------------------------------------------------------- attention
+
+
+def _qkv(seed, S, nh, dh):
+    r = _rng(seed)
+    return (r.normal(size=(S, nh * dh)), r.normal(size=(S, nh * dh)), r.normal(size=(S, nh * dh)))
+
+
+def _attn(q, k, v, nh, dh, w, lib):
+    pos = np.arange(q.shape[0])
+    return O.swa_attention(q, pos, k, v, pos, nh, dh, w, lib=lib)
+
+
+def _sdpa(q, k, v, nh, dh, mask=None, causal=False):
+    S = q.shape[0]
+    t = lambda a: torch.from_numpy(a).reshape(S, nh, dh).transpose(0, 1)
+    o = F.scaled_dot_product_attention(t(q), t(k), t(v), attn_mask=mask, is_causal=causal)
+    return o.transpose(0, 1).reshape(S, nh * dh).numpy()
+
+
+def band_mask(S, w):
+    i = torch.arange(S).unsqueeze(1)
+    k = torch.arange(S).unsqueeze(0)
+    return (k <= i) & (i - k < w)
+
+
+def pin_attention_window1_is_v(lib):
+    q, k, v = _qkv(5, 9, 2, 4)
+    out = _attn(q, k, v, 2, 4, 1, lib)
+    return bool(np.array_equal(out, v)), "window 1 must return v exactly"
+
+
+def pin_attention_window2_closed_form(lib):
+    # Two visible keys (i-1, i): o_i = v_{i-1} + sigmoid(s_i - s_{i-1}) (v_i - v_{i-1}).
+    S, nh, dh = 7, 2, 4
+    q, k, v = _qkv(6, S, nh, dh)
+    out = _attn(q, k, v, nh, dh, 2, lib)
+    want = np.empty_like(v)
+    for h in range(nh):
+        c = slice(h * dh, (h + 1) * dh)
+        want[0, c] = v[0, c]
+        for i in range(1, S):
+            s_prev = q[i, c] @ k[i - 1, c] / math.sqrt(dh)
+            s_self = q[i, c] @ k[i, c] / math.sqrt(dh)
+            lam = 1.0 / (1.0 + math.exp(-(s_self - s_prev)))
+            want[i, c] = v[i - 1, c] + lam * (v[i, c] - v[i - 1, c])
+    return _close(out, want, 1e-13)
+
+
+def pin_attention_full_causal(lib):
+    # Identity: window >= seq is full causal attention.
+    S, nh, dh = 11, 3, 8
+    q, k, v = _qkv(7, S, nh, dh)
+    want = _sdpa(q, k, v, nh, dh, causal=True)
+    ok = True
+    detail = []
+    for w in (S, S + 17):
+        o, d = _close(_attn(q, k, v, nh, dh, w, lib), want, 1e-13)
+        ok &= o
+        detail.append(f"w={w}: {d}")
+    return ok, "; ".join(detail)
+
+
+def pin_attention_band_library(lib):
+    S, nh, dh = 23, 2, 8
+    q, k, v = _qkv(8, S, nh, dh)
+    ok, detail = True, []
+    for w in (1, 2, 3, 5, 22):
+        o, d = _close(_attn(q, k, v, nh, dh, w, lib), _sdpa(q, k, v, nh, dh, band_mask(S, w)),
+                      1e-13)
+        ok &= o
+        detail.append(f"w={w}: {d}")
+    return ok, "; ".join(detail)
+
+
+def pin_attention_rows_sum_to_one(lib):
+    # Softmax weights sum to 1: with every value row equal to c the output is c.
+    S, nh, dh = 13, 2, 4
+    q, k, _ = _qkv(9, S, nh, dh)
+    c = np.linspace(-1, 2, nh * dh)
+    v = np.tile(c, (S, 1))
+    return _close(_attn(q, k, v, nh, dh, 4, lib), v, 1e-14)
+
+
+def pin_attention_translation(lib):
+    # A row i >= w-1 depends only on rows i-w+1..i: recomputing on that slice alone,
+    # with shifted positions, gives the same row.
+    S, nh, dh, w = 20, 2, 4, 5
+    q, k, v = _qkv(10, S, nh, dh)
+    full = _attn(q, k, v, nh, dh, w, lib)
+    i = 15
+    part = _attn(q[i - w + 1:i + 1], k[i - w + 1:i + 1], v[i - w + 1:i + 1], nh, dh, w, lib)
+    return _close(part[-1], full[i], 1e-14)
+
+
+# ----------------------------------------------------------------------------- the block
+
+
+def tiny_params(H, nh, F_, seed, biases=True, std=0.3):
+    r = _rng(seed)
+    p = {"ln_gamma": 1 + 0.1 * r.normal(size=H), "ln_beta": 0.1 * r.normal(size=H),
+         "wqkv": std * r.normal(size=(H, 3 * H)), "w1": std * r.normal(size=(H, F_)),
+         "wo": std * r.normal(size=(H, H)), "w2": std * r.normal(size=(F_, H))}
+    if biases:
+        p.update(b_qkv=0.1 * r.normal(size=3 * H), b1=0.1 * r.normal(size=F_),
+                 b_o=0.1 * r.normal(size=H), b2=0.1 * r.normal(size=H))
+    return p
+
+
+def torch_block(dims, x, p):
+    """The block restated with torch float64 library routines (layer_norm, gelu, sdpa)."""
+    B, S, H, nh, dh = dims.batch, dims.seq, dims.hidden, dims.heads, dims.head_dim
+    T = lambda a: None if a is None else torch.from_numpy(np.asarray(a, dtype=np.float64))
+    X = T(x).reshape(B, S, H)
+    xn = F.layer_norm(X, (H,), T(p["ln_gamma"]), T(p["ln_beta"]), dims.ln_eps)
+    qkv = xn @ T(p["wqkv"])
+    if p.get("b_qkv") is not None:
+        qkv = qkv + T(p["b_qkv"])
+    q, k, v = (qkv[..., i * H:(i + 1) * H].reshape(B, S, nh, dh).transpose(1, 2) for i in range(3))
+    a = F.scaled_dot_product_attention(q, k, v, attn_mask=band_mask(S, dims.window))
+    a = a.transpose(1, 2).reshape(B, S, H) @ T(p["wo"])
+    h = xn @ T(p["w1"])
+    if p.get("b1") is not None:
+        h = h + T(p["b1"])
+    m = F.gelu(h, approximate="none") @ T(p["w2"])
+    if p.get("b_o") is not None:
+        a = a + T(p["b_o"])
+    if p.get("b2") is not None:
+        m = m + T(p["b2"])
+    return (X + m + a).numpy()
+
+
+def pin_block_library(lib):
+    ok, detail = True, []
+    for w in (1, 2, 3, 8, 13):
+        dims = O.Dims(2, 8, 8, 2, 4, 16, w)
+        p = tiny_params(8, 2, 16, seed=20 + w)
+        x = _rng(30 + w).normal(size=(2, 8, 8))
+        o, d = _close(O.block_forward(dims, x, p, lib=lib), torch_block(dims, x, p), 1e-12)
+        ok &= o
+        detail.append(f"w={w}: {d}")
+    return ok, "; ".join(detail)
+
+
+def pin_block_concat_identity(lib):
+    # y = x + [attn | GeLU(h)] [Wo ; W2] with [q|k|v|h] = xn [Wqkv | W1] (one GEMM each).
+    dims = O.Dims(2, 9, 16, 4, 4, 32, 3)
+    H = 16
+    p = tiny_params(H, 4, 32, seed=40)
+    x = _rng(41).normal(size=(2, 9, H))
+    y = O.block_forward(dims, x, p, lib=lib)
+    w1cat = np.concatenate([p["wqkv"], p["w1"]], axis=1)
+    w2cat = np.concatenate([p["wo"], p["w2"]], axis=0)
+    b1cat = np.concatenate([p["b_qkv"], p["b1"]])
+    X = x.reshape(-1, H)
+    mu = X.mean(1, keepdims=True)
+    xn = (X - mu) / np.sqrt(X.var(1, keepdims=True) + dims.ln_eps) * p["ln_gamma"] + p["ln_beta"]
+    z = xn @ w1cat + b1cat
+    attn = np.concatenate([_sdpa(z[b * 9:(b + 1) * 9, 0:H], z[b * 9:(b + 1) * 9, H:2 * H],
+                                 z[b * 9:(b + 1) * 9, 2 * H:3 * H], 4, 4, band_mask(9, 3))
+                           for b in range(2)])
+    act = np.concatenate([attn, F.gelu(torch.from_numpy(z[:, 3 * H:])).numpy()], axis=1)
+    y2 = X + act @ w2cat + (p["b_o"] + p["b2"])
+    return _close(y.reshape(-1, H), y2, 1e-10 * np.abs(y2).max())
+
+
+def pin_block_zero_affine(lib):
+    # gamma = beta = 0 and no biases: LN(x) = 0 -> every branch is 0 -> y = x exactly.
+    dims = O.Dims(2, 6, 8, 2, 4, 16, 3)
+    p = tiny_params(8, 2, 16, seed=50, biases=False)
+    p["ln_gamma"] = np.zeros(8)
+    p["ln_beta"] = np.zeros(8)
+    x = _rng(51).normal(size=(2, 6, 8))
+    return bool(np.array_equal(O.block_forward(dims, x, p, lib=lib), x)), "y must equal x"
+
+
+def pin_block_zero_output_weights(lib):
+    dims = O.Dims(1, 6, 8, 2, 4, 16, 4)
+    p = tiny_params(8, 2, 16, seed=52, biases=False)
+    p["wo"] = np.zeros((8, 8))
+    p["w2"] = np.zeros((16, 8))
+    x = _rng(53).normal(size=(1, 6, 8))
+    return bool(np.array_equal(O.block_forward(dims, x, p, lib=lib), x)), "y must equal x"
+
+
+def pin_block_invariants(lib):
+    dims = O.Dims(3, 10, 16, 4, 4, 32, 4)
+    p = tiny_params(16, 4, 32, seed=60)
+    x = _rng(61).normal(size=(3, 10, 16))
+    y = O.block_forward(dims, x, p, lib=lib)
+    out = []
+    # batch independence
+    one = O.Dims(1, 10, 16, 4, 4, 32, 4)
+    yb = np.stack([O.block_forward(one, x[b:b + 1], p, lib=lib)[0] for b in range(3)])
+    out.append(("batch", _close(yb, y, 1e-13)))
+    # per-row shift of x leaves y - x unchanged (LN removes the row mean)
+    c = _rng(62).normal(size=(3, 10, 1)) * 5
+    ys = O.block_forward(dims, x + c, p, lib=lib)
+    out.append(("shift", _close(ys - (x + c), y - x, 1e-10)))
+    # permuting heads consistently in Wq, Wk, Wv (columns) and Wo (rows)
+    perm = [2, 0, 3, 1]
+    idx = np.concatenate([np.arange(h * 4, h * 4 + 4) for h in perm])
+    pp = dict(p)
+    pp["wqkv"] = np.concatenate([p["wqkv"][:, i * 16:(i + 1) * 16][:, idx] for i in range(3)], 1)
+    pp["b_qkv"] = np.concatenate([p["b_qkv"][i * 16:(i + 1) * 16][idx] for i in range(3)])
+    pp["wo"] = p["wo"][idx, :]
+    out.append(("heads", _close(O.block_forward(dims, x, pp, lib=lib), y, 1e-12)))
+    ok = all(o for _, (o, _) in out)
+    return ok, "; ".join(f"{n}: {d}" for n, (_, d) in out)
+
+
+def pin_block_rows_mode(lib):
+    dims = O.Dims(2, 40, 16, 4, 4, 32, 7)
+    p = tiny_params(16, 4, 32, seed=70)
+    x = _rng(71).normal(size=(2, 40, 16))
+    full = O.block_forward(dims, x, p, lib=lib)
+    rows = {0: [0, 5, 39], 1: [6, 7, 20, 33]}
+    part = O.block_forward(dims, x, p, rows=rows, lib=lib)
+    want = np.concatenate([full[b][rows[b]] for b in (0, 1)])
+    return _close(part, want, 1e-13)
+
+
+ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_layernorm_library,
+            pin_layernorm_stats, pin_linear_library, pin_attention_window1_is_v,
+            pin_attention_window2_closed_form, pin_attention_full_causal,
+            pin_attention_band_library, pin_attention_rows_sum_to_one,
+            pin_attention_translation, pin_block_library, pin_block_concat_identity,
+            pin_block_zero_affine, pin_block_zero_output_weights, pin_block_invariants,
+            pin_block_rows_mode]
