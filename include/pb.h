@@ -1,0 +1,194 @@
+/*
+ * pb.h — C ABI of the GB300 (sm_103a) forward pass of the parallel transformer block
+ *
+ *     y = x + MLP(LN(x)) + Attention(LN(x))
+ *
+ * (MegaScale reading notes, section 1.1 "Parallel Transformer Block", eq. (4)), where
+ *   LN         = LayerNorm with gamma/beta, computed ONCE and shared by both branches;
+ *   MLP(z)     = GeLU(z W1) W2               (Megatron-LM notes, section 2.1, Y = GeLU(XA)B);
+ *   Attention  = multi-head attention on the [q | k | v] = z Wqkv projection (Megatron-LM
+ *                notes, section 2.2), each query attending to the most recent `window`
+ *                tokens of its own sequence, itself included (MegaScale reading notes,
+ *                section 1.1 "Sliding Window Attention", eqs. (5)-(6)), followed by Wo.
+ *
+ * The library fuses the two branches: one GEMM against [Wqkv | W1] (GeLU in its
+ * epilogue), one sliding-window flash attention kernel, and one GEMM of
+ * [attn | GeLU(h)] against [Wo ; W2] with the residual added in its epilogue.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are bf16 (IEEE bfloat16 bit patterns), row-major, on the CURRENT CUDA
+ *    device unless stated. Weights use the pages' Y = X W convention: [in, out].
+ *  - Token rows are ordered (batch, position): x and y are [batch*seq, hidden].
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). All work is
+ *    enqueued asynchronously on it; no call synchronises the host, except
+ *    pb_get_status, which reads a word the kernels write.
+ *  - The library allocates NO device memory. The caller owns every buffer: inputs,
+ *    outputs, the per-handle weight workspace and the per-call scratch.
+ *  - Every function returns pb_status; no C++ exception crosses the ABI. Argument
+ *    errors are detected before anything is enqueued. pb_last_error_message() returns
+ *    a thread-local description of the last failure on the calling thread.
+ *  - Device-side failures (a bounded wait inside a kernel that ran out) do not fault the
+ *    GPU: the kernel records PB_ERR_DEVICE_TIMEOUT in the handle's status word and
+ *    returns; pb_get_status reports it.
+ */
+#ifndef PB_H_
+#define PB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pb_status {
+  PB_OK = 0,
+  PB_ERR_INVALID_ARG = 1,     /* NULL/misaligned pointer, bad size, partial aliasing   */
+  PB_ERR_UNSUPPORTED = 2,     /* shape outside the supported set (see pb_dims)         */
+  PB_ERR_WORKSPACE = 3,       /* workspace or scratch smaller than required            */
+  PB_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (message has why)   */
+  PB_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait expired; results are invalid  */
+  PB_ERR_BAD_HANDLE = 6       /* NULL, destroyed or foreign handle, or wrong device    */
+} pb_status;
+
+/*
+ * Shape of one block. Supported (else PB_ERR_UNSUPPORTED):
+ *   batch, seq >= 1; window >= 1 (window >= seq is full causal attention);
+ *   head_dim in {64, 128}; hidden = heads * head_dim; hidden % 64 == 0; ffn % 64 == 0;
+ *   batch * seq < 2^31; ln_eps > 0.
+ */
+typedef struct pb_dims {
+  int32_t batch;
+  int32_t seq;
+  int32_t hidden;    /* H */
+  int32_t heads;     /* nh */
+  int32_t head_dim;  /* dh, H = nh * dh */
+  int32_t ffn;       /* F, width of the MLP (4H on the pages) */
+  int32_t window;    /* w: key k is visible to query i iff 0 <= i - k < w */
+  float ln_eps;      /* LayerNorm epsilon, inside the square root */
+} pb_dims;
+
+/*
+ * Parameters of one block (device pointers, bf16). They are read only by pb_create,
+ * which packs them into the workspace; they may be freed once the stream has passed
+ * pb_create's work.
+ *   ln_gamma, ln_beta : [H]
+ *   wqkv              : [H, 3H]; columns [Q | K | V], head j of each owns columns
+ *                       [j*dh, (j+1)*dh) of its H-wide block
+ *   w1                : [H, F]    (first MLP linear, "A" of Y = GeLU(XA)B)
+ *   wo                : [H, H]    (attention output projection)
+ *   w2                : [F, H]    (second MLP linear, "B")
+ *   b_qkv [3H], b1 [F], b_o [H], b2 [H] : optional biases, NULL = none.
+ */
+typedef struct pb_weights {
+  const void* ln_gamma;
+  const void* ln_beta;
+  const void* wqkv;
+  const void* w1;
+  const void* wo;
+  const void* w2;
+  const void* b_qkv;
+  const void* b1;
+  const void* b_o;
+  const void* b2;
+} pb_weights;
+
+/* Byte offsets of the intermediates inside the scratch buffer of a forward call, valid
+ * after the stream passes it (for inspection and tests):
+ *   xn  [T, H]          LN(x)
+ *   qk  [T, 2H]         [q | k] (head-major columns, no bias folded away)
+ *   vt  [batch, heads, dh, seq_pad] v transposed per head (seq_pad = seq rounded up to 8)
+ *   act [T, H + F]      [attention output (before Wo) | GeLU(h)]
+ * T = batch * seq. */
+typedef struct pb_scratch_layout {
+  size_t xn;
+  size_t qk;
+  size_t vt;
+  size_t act;
+  size_t io0; /* [T, H] staging / layer ping-pong buffer */
+  size_t io1; /* [T, H] */
+  size_t seq_pad;
+  size_t total;
+} pb_scratch_layout;
+
+typedef struct pb_handle pb_handle;
+
+/* Bytes of the per-handle weight workspace (packed [Wqkv | W1] and [Wo ; W2] in the
+ * K-major layout the tensor cores read, biases, LN parameters and the status word). */
+pb_status pb_weight_workspace_bytes(const pb_dims* dims, size_t* bytes);
+
+/* Bytes of the scratch one forward call needs (shared by all layers of a stack), and
+ * its layout. */
+pb_status pb_scratch_bytes(const pb_dims* dims, size_t* bytes);
+pb_status pb_get_scratch_layout(const pb_dims* dims, pb_scratch_layout* layout);
+
+/* Creates a handle for one block on the current device. `workspace` (device, 256-byte
+ * aligned, >= pb_weight_workspace_bytes) is owned by the caller and must outlive the
+ * handle. Enqueues the weight packing on `stream`. */
+pb_status pb_create(const pb_dims* dims, const pb_weights* weights, void* workspace,
+                    size_t workspace_bytes, void* stream, pb_handle** out);
+
+/* One block: y = x + MLP(LN(x)) + Attention(LN(x)). x, y: [batch*seq, hidden] bf16,
+ * 16-byte aligned; y may equal x (in place), partial overlap is PB_ERR_INVALID_ARG.
+ * `scratch` (device, 256-byte aligned, >= pb_scratch_bytes) must not be used by another
+ * call that may run concurrently. */
+pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t scratch_bytes,
+                     void* stream);
+
+/* A stack of residual blocks (MegaScale reading notes, section 1.1: L layers give a
+ * receptive field of L*w), x_{l+1} = block_l(x_l). All handles must have the same
+ * dims. Intermediate activations live in the scratch's io0/io1 buffers. */
+pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const void* x, void* y,
+                           void* scratch, size_t scratch_bytes, void* stream);
+
+/* As pb_forward_stack, with x and y in HOST memory (pinned memory gives asynchronous
+ * copies): copies x to the device, runs the stack, copies y back, all on `stream`.
+ * The caller synchronises the stream before reading y. */
+pb_status pb_forward_stack_host(pb_handle* const* layers, int32_t n_layers, const void* x_host,
+                                void* y_host, void* scratch, size_t scratch_bytes, void* stream);
+
+/* Reads the handle's device status word (blocks until the word can be read on the
+ * handle's device) and returns PB_OK or the first device-side error recorded since
+ * the last pb_clear_status. */
+pb_status pb_get_status(pb_handle* h);
+pb_status pb_clear_status(pb_handle* h, void* stream);
+
+/* Sets the limit, in nanoseconds, of every bounded wait inside this handle's kernels
+ * (default 2e9). A wait that reaches it records PB_ERR_DEVICE_TIMEOUT and the kernel
+ * returns. */
+pb_status pb_set_wait_limit_ns(pb_handle* h, uint64_t limit_ns);
+
+/* Destroys the handle (host memory only; the caller frees the workspace). */
+pb_status pb_destroy(pb_handle* h);
+
+const char* pb_status_string(pb_status s);
+const char* pb_last_error_message(void);
+
+/* ------------------------------------------------------------------------------------
+ * Single steps of the block, exported for testing and reuse. Same conventions.
+ * ---------------------------------------------------------------------------------- */
+
+/* LayerNorm (the LN of eq. (4)): out[r,:] = (x[r,:] - mean) / sqrt(var + eps) * gamma
+ * + beta, biased variance, fp32 statistics. x, out: [rows, H] bf16; gamma, beta: [H]
+ * bf16. H % 8 == 0, H <= 16384. */
+pb_status pb_layernorm(int64_t rows, int32_t H, const void* x, const void* gamma,
+                       const void* beta, float eps, void* out, void* stream);
+
+/* C[M, N] = A[M, K] * B[N, K]^T on the tensor cores (bf16 inputs, fp32 accumulation,
+ * bf16 output rounded to nearest even): the contraction of every linear layer of the
+ * block with the weight stored K-major. A, B, C 16-byte aligned; K % 64 == 0,
+ * N % 32 == 0. `status` (device int, may be NULL) receives PB_ERR_DEVICE_TIMEOUT if a
+ * bounded wait runs out. */
+pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const void* B, void* C,
+                       int* status, void* stream);
+
+/* Sliding-window causal attention alone (section 1.1, eqs. (5)-(6)) from the scratch
+ * layout's qk and vt buffers into columns [0, H) of `act` ([T, act_ld] bf16). */
+pb_status pb_swa_attention(const pb_dims* dims, const void* qk, const void* vt, void* act,
+                           int64_t act_ld, int* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PB_H_ */

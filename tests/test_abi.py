@@ -1,0 +1,116 @@
+"""The C-ABI library loads, exports every function include/pb.h declares, and rejects bad
+arguments on the host before touching a GPU (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from transformer_block_gb300 import build, pb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pb.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:pb_status|const char\s*\*)\s*(pb_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pb.lib()
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for required in ("pb_create", "pb_forward", "pb_destroy", "pb_forward_stack_host"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and the binding wraps exactly the declared functions
+    assert set(pb.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code, name in pb.STATUS_NAMES.items():
+        assert lib.pb_status_string(code).decode() == name
+
+
+def dims(**kw):
+    base = dict(batch=1, seq=128, hidden=256, heads=4, head_dim=64, ffn=1024, window=32)
+    base.update(kw)
+    return pb.make_dims(**base)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(hidden=250), pb.STATUS_NAMES and 1),          # heads * head_dim != hidden
+    (dict(head_dim=32, heads=8), 2),                     # unsupported head_dim
+    (dict(ffn=1000), 2),                                 # ffn % 64
+    (dict(window=0), 1),
+    (dict(seq=0), 1),
+    (dict(ln_eps=0.0), 1),
+    (dict(batch=65536, seq=65536), 2),                   # 2^32 tokens
+])
+def test_bad_dims_rejected(lib, bad, code):
+    n = ctypes.c_size_t()
+    d = dims(**bad)
+    assert lib.pb_weight_workspace_bytes(ctypes.byref(d), ctypes.byref(n)) == code
+    assert lib.pb_last_error_message().decode()
+
+
+def test_workspace_and_scratch_sizes(lib):
+    d = dims()
+    H, F, T = 256, 1024, 128
+    ws = pb.weight_workspace_bytes(d)
+    assert ws >= 2 * ((3 * H + F) * H + H * (H + F))
+    L = pb.scratch_layout(d)
+    assert L.seq_pad == 128
+    assert L.total == pb.scratch_bytes(d)
+    for a, b in [("xn", "qk"), ("qk", "vt"), ("vt", "act"), ("act", "io0"), ("io0", "io1")]:
+        assert getattr(L, a) < getattr(L, b) and getattr(L, b) % 1024 == 0
+    assert L.act - L.vt >= 2 * 1 * H * 128
+    assert L.total - L.io1 >= 2 * T * H
+    # ragged sequences pad the transposed V to a multiple of 8 tokens
+    assert pb.scratch_layout(dims(seq=130)).seq_pad == 136
+
+
+def test_create_rejects_missing_weights_before_cuda(lib):
+    d = dims()
+    w = pb.pb_weights()
+    h = ctypes.c_void_p()
+    assert lib.pb_create(ctypes.byref(d), ctypes.byref(w), ctypes.c_void_p(1 << 20), 1 << 30,
+                         None, ctypes.byref(h)) == 1
+    assert "NULL" in lib.pb_last_error_message().decode()
+    assert not h.value
+
+
+def test_create_rejects_small_workspace(lib):
+    d = dims()
+    ptrs = [ctypes.c_void_p(0x100000 + 0x10000 * i) for i in range(6)] + [None] * 4
+    w = pb.pb_weights(*ptrs)
+    h = ctypes.c_void_p()
+    assert lib.pb_create(ctypes.byref(d), ctypes.byref(w), ctypes.c_void_p(0x4000000), 16, None,
+                         ctypes.byref(h)) == 3
+    assert lib.pb_create(ctypes.byref(d), ctypes.byref(w), ctypes.c_void_p(0x4000001), 1 << 40,
+                         None, ctypes.byref(h)) == 1  # misaligned workspace
+
+
+def test_null_handles(lib):
+    assert lib.pb_forward(None, None, None, None, 0, None) == 6
+    assert lib.pb_destroy(None) == 6
+    assert lib.pb_get_status(None) == 6
+    arr = (ctypes.c_void_p * 1)(None)
+    assert lib.pb_forward_stack(arr, 1, None, None, None, 0, None) == 6
+    assert lib.pb_forward_stack(arr, 0, None, None, None, 0, None) == 1
+
+
+def test_step_entry_points_validate(lib):
+    assert lib.pb_gemm_bf16(128, 100, 64, None, None, None, None, None) == 2  # N % 32
+    assert lib.pb_gemm_bf16(128, 128, 64, None, None, None, None, None) == 1  # NULL
+    assert lib.pb_layernorm(4, 12, None, None, None, 1e-5, None, None) == 2   # H % 8
+    assert lib.pb_layernorm(4, 16, None, None, None, 1e-5, None, None) == 1   # NULL

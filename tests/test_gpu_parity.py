@@ -1,0 +1,225 @@
+"""GPU parity: the C-ABI path against the fp64 oracle on the same seeded bf16 inputs.
+
+Small cases span several tiles and ragged tails and are compared element by element
+on every output (and every intermediate the scratch exposes). Full-size workloads are
+compared on sampled output rows the oracle computes exactly from their window cones.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from tests.parity import assert_parity, host, host_params, oracle_dims
+from transformer_block_gb300 import WORKLOADS, inputs, pb
+from transformer_block_gb300.configs import Workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    pb.lib()
+
+
+def wl_small(name, B, S, H, nh, dh, F, w, layers=1, std=0.02):
+    return Workload(name, B, S, H, nh, dh, F, w, layers, std)
+
+
+# --------------------------------------------------------------------------- single steps
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 128), (200, 288, 192),
+                                   (1, 32, 64), (300, 1056, 512), (1000, 768, 2048)])
+def test_gemm_matches_oracle(M, N, K):
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N * 3 + K)
+    a = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    c = pb.gemm(a, b, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = O.linear(host(a), host(b).T)
+    assert_parity(host(c), ref, f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("rows,H", [(37, 256), (5, 2048), (3, 12288), (64, 16384)])
+def test_layernorm_matches_oracle(rows, H):
+    g = torch.Generator(device="cuda").manual_seed(rows + H)
+    x = (torch.randn(rows, H, generator=g, device="cuda") * 2 + 0.5).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(H, generator=g, device="cuda")).to(torch.bfloat16)
+    beta = (0.1 * torch.randn(H, generator=g, device="cuda")).to(torch.bfloat16)
+    out = pb.layernorm(x, gamma, beta, 1e-5)
+    torch.cuda.synchronize()
+    ref = O.layernorm(host(x), host(gamma), host(beta), 1e-5)
+    assert_parity(host(out), ref, f"layernorm {rows}x{H}")
+
+
+# --------------------------------------------------------------------------- whole block
+
+SMALL = [
+    WORKLOADS["tiny"],
+    wl_small("b2-s130-h256-dh128", 2, 130, 256, 2, 128, 512, 64),
+    wl_small("b3-s33-h128-dh64-w5", 3, 33, 128, 2, 64, 256, 5),
+    wl_small("b1-s300-h384-w300", 1, 300, 384, 3, 128, 768, 300),
+    wl_small("b2-s257-h256-w129", 2, 257, 256, 4, 64, 1024, 129),
+    wl_small("b1-s1", 1, 1, 256, 2, 128, 512, 4),
+    wl_small("b1-s200-w1", 1, 200, 256, 2, 128, 512, 1),
+    wl_small("b2-s384-h512-w1000", 2, 384, 512, 4, 128, 2048, 1000),
+]
+
+
+def run_block(wl, biases=False, seed=0):
+    x, params = inputs.make_layer(wl, 0, seed=seed, device="cuda", biases=biases)
+    dims = pb.make_dims(wl)
+    block = pb.ParallelBlock(dims, params)
+    scratch = pb.new_scratch(dims)
+    y = block(x, scratch=scratch)
+    torch.cuda.synchronize()
+    assert block.status() == pb.PB_OK
+    return x, params, dims, block, scratch, y
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_block_matches_oracle(wl):
+    x, params, dims, block, scratch, y = run_block(wl)
+    od = oracle_dims(wl)
+    ref, st = O.block_forward(od, host(x).reshape(wl.batch, wl.seq, wl.hidden),
+                              host_params(params), keep_stages=True)
+    H, T = wl.hidden, wl.tokens
+    assert_parity(host(y), ref.reshape(T, H), f"{wl.name} y")
+    assert_parity(host(y) - host(x), ref.reshape(T, H) - host(x), f"{wl.name} y-x",
+                  max_tol=5e-2, mean_tol=2e-2)
+    # intermediates
+    assert_parity(host(pb.scratch_view(scratch, dims, "xn")), st["xn"], f"{wl.name} xn")
+    qk = host(pb.scratch_view(scratch, dims, "qk"))
+    assert_parity(qk[:, :H], st["q"], f"{wl.name} q")
+    assert_parity(qk[:, H:], st["k"], f"{wl.name} k")
+    vt = host(pb.scratch_view(scratch, dims, "vt"))[..., :wl.seq]  # [B, nh, dh, S]
+    v = vt.transpose(0, 3, 1, 2).reshape(T, H)
+    assert_parity(v, st["v"], f"{wl.name} v")
+    act = host(pb.scratch_view(scratch, dims, "act"))
+    assert_parity(act[:, :H], st["attn"], f"{wl.name} attention")
+    assert_parity(act[:, H:], st["gelu_h"], f"{wl.name} GeLU(h)")
+
+
+def test_block_with_biases():
+    wl = wl_small("bias-b2-s150-h256", 2, 150, 256, 2, 128, 512, 40)
+    x, params, dims, block, scratch, y = run_block(wl, biases=True)
+    ref = O.block_forward(oracle_dims(wl), host(x).reshape(2, 150, 256), host_params(params))
+    assert_parity(host(y), ref.reshape(-1, 256), "biases y")
+
+
+def test_zero_affine_gives_identity_bit_exact():
+    wl = wl_small("zero-affine", 2, 160, 256, 2, 128, 512, 50)
+    x, params = inputs.make_layer(wl, 0, device="cuda")
+    params["ln_gamma"].zero_()
+    params["ln_beta"].zero_()
+    y = pb.ParallelBlock(pb.make_dims(wl), params)(x)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x)
+
+
+def test_window_one_returns_v_exactly():
+    wl = wl_small("w1", 2, 140, 256, 2, 128, 512, 1)
+    x, params, dims, block, scratch, y = run_block(wl)
+    vt = pb.scratch_view(scratch, dims, "vt")[..., :wl.seq]
+    v = vt.permute(0, 3, 1, 2).reshape(wl.tokens, wl.hidden)
+    attn = pb.scratch_view(scratch, dims, "act")[:, :wl.hidden]
+    assert torch.equal(attn, v)
+
+
+def test_in_place_matches_out_of_place():
+    wl = wl_small("inplace", 1, 256, 256, 2, 128, 512, 64)
+    x, params, dims, block, scratch, y = run_block(wl)
+    x2 = x.clone()
+    block(x2, y=x2, scratch=scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(x2, y)
+
+
+def test_deterministic():
+    wl = wl_small("det", 2, 200, 256, 2, 128, 512, 70)
+    x, params, dims, block, scratch, y = run_block(wl)
+    y2 = block(x, scratch=scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+
+
+def test_stack_matches_oracle_and_host_path():
+    wl = wl_small("stack3", 2, 192, 256, 2, 128, 512, 48, layers=3)
+    x, layers = inputs.make_stack(wl, device="cuda")
+    dims = pb.make_dims(wl)
+    blocks = [pb.ParallelBlock(dims, p) for p in layers]
+    scratch = pb.new_scratch(dims)
+    y = pb.forward_stack(blocks, x, scratch=scratch)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    pb.forward_stack_host(blocks, xh, yh, scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y.cpu())
+    # chaining single-layer calls gives the same bits
+    z = x
+    for b in blocks:
+        z = b(z, scratch=scratch)
+    torch.cuda.synchronize()
+    assert torch.equal(z, y)
+    ref = O.stack_forward(oracle_dims(wl), host(x), [host_params(p) for p in layers])
+    assert_parity(host(y), ref.reshape(-1, wl.hidden), "stack3 y")
+
+
+# --------------------------------------------------------------------------- full sizes
+
+def sample_rows(wl, clusters):
+    rows = {}
+    for b in range(wl.batch):
+        pos = set()
+        for start, n in clusters:
+            s = start if start >= 0 else wl.seq + start
+            pos.update(range(max(0, s), min(wl.seq, s + n)))
+        rows[b] = sorted(pos)
+    return rows
+
+
+@pytest.mark.parametrize("name,clusters", [
+    ("block-h2048", [(0, 4), (509, 6), (1500, 3), (-5, 5)]),
+    ("gpt3-175b-layer", [(0, 3), (1023, 3), (-6, 6)]),
+    ("long-swa-32k", [(0, 3), (4093, 5), (-5, 5)]),
+])
+def test_full_size_sampled_rows(name, clusters):
+    wl = WORKLOADS[name]
+    x, params, dims, block, scratch, y = run_block(wl)
+    rows = sample_rows(wl, clusters)
+    hp = host_params(params)
+    del params
+    ref = O.block_forward(oracle_dims(wl), host(x).reshape(wl.batch, wl.seq, wl.hidden), hp,
+                          rows=rows)
+    yh = host(y).reshape(wl.batch, wl.seq, wl.hidden)
+    g = np.concatenate([yh[b][rows[b]] for b in sorted(rows)])
+    assert_parity(g, ref, f"{name} sampled y ({len(g)} rows)")
+    xh = host(x).reshape(wl.batch, wl.seq, wl.hidden)
+    xs = np.concatenate([xh[b][rows[b]] for b in sorted(rows)])
+    assert_parity(g - xs, ref - xs, f"{name} sampled y-x", max_tol=5e-2, mean_tol=2e-2)
+
+
+def test_full_size_stack_prefix_rows():
+    # By causality the first P rows of every layer depend only on the first P inputs, so
+    # the oracle runs the 8 layers on a P-token prefix.
+    wl = WORKLOADS["stack8-h5120"]
+    P = 96
+    x, layers = inputs.make_stack(wl, device="cuda")
+    dims = pb.make_dims(wl)
+    blocks = [pb.ParallelBlock(dims, p) for p in layers]
+    y = pb.forward_stack(blocks, x)
+    torch.cuda.synchronize()
+    for b in blocks:
+        assert b.status() == pb.PB_OK
+    od = oracle_dims(wl)
+    od = O.Dims(od.batch, P, od.hidden, od.heads, od.head_dim, od.ffn, od.window, od.ln_eps)
+    z = host(x).reshape(wl.batch, wl.seq, wl.hidden)[:, :P].astype(np.float64)
+    for p in layers:
+        z = O.block_forward(od, z, host_params(p))
+    g = host(y).reshape(wl.batch, wl.seq, wl.hidden)[:, :P]
+    assert_parity(g, z, f"stack8 prefix {P} rows")

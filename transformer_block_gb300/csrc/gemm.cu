@@ -1,0 +1,298 @@
+// gemm.cu — persistent warp-specialised tcgen05 GEMM, D = A * B^T, with the epilogues of
+// the parallel block's two linear steps fused in:
+//   * [q | k | v | h] = LN(x) [Wqkv | W1], GeLU(h) applied in the epilogue (the fused
+//     QKV projection of the MegaScale reading notes, section 1.3, widened to the MLP's
+//     first linear because both read the same LN output in eq. (4));
+//   * y = x + [attn | GeLU(h)] [Wo ; W2] (+ bias), the residual sum of eq. (4) applied
+//     in the epilogue of the one GEMM that computes both branch outputs.
+//
+// CTA tile 128 x 256, K step 64 (one 128-byte swizzle row of bf16), 4-stage TMA ring.
+// Warp 0: TMA producer. Warp 1: TMEM allocation and the single MMA-issuing thread.
+// Warps 2-5: epilogue, one TMEM lane quadrant each (warp w reads lanes 32*(w%4)..+31).
+// The fp32 accumulator lives in tensor memory, double-buffered (2 x 256 columns), so
+// the epilogue of one tile overlaps the main loop of the next. Tiles are handed out
+// round-robin, M-block fastest, so CTAs running at the same time share B tiles in L2.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace pb {
+namespace {
+
+constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16;
+
+__device__ __forceinline__ float gelu_erf(float z) {
+  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    d[q] = u;
+  }
+}
+
+// Epilogue of 32 consecutive columns [col0, col0 + 32) of one output row.
+template <int KIND>
+__device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col0,
+                                           const uint32_t (&r)[32]) {
+  if (row >= ep.M) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  if (KIND != kEpiStore && ep.bias != nullptr) {
+    const float4* b4 = reinterpret_cast<const float4*>(ep.bias + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 b = __ldg(b4 + q);
+      v[4 * q + 0] += b.x;
+      v[4 * q + 1] += b.y;
+      v[4 * q + 2] += b.z;
+      v[4 * q + 3] += b.w;
+    }
+  }
+  if (KIND == kEpiStore) {
+    store_row32(ep.c + int64_t(row) * ep.ldc + col0, v);
+  } else if (KIND == kEpiBlockIn) {
+    const int H = ep.H;
+    if (col0 < 2 * H) {  // q | k
+      store_row32(ep.qk + int64_t(row) * (2 * H) + col0, v);
+    } else if (col0 < 3 * H) {  // v, stored transposed per (sequence, head)
+      const int c = col0 - 2 * H;
+      const int head = c / ep.dh, d0 = c - head * ep.dh;
+      const int b = row / ep.S, s = row - b * ep.S;
+      __nv_bfloat16* dst =
+          ep.vt + (int64_t(b * ep.nh + head) * ep.dh + d0) * ep.seq_pad + s;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[int64_t(i) * ep.seq_pad] = __float2bfloat16_rn(v[i]);
+    } else {  // h -> GeLU(h), next to the attention output in the second GEMM's A operand
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+      store_row32(ep.act + int64_t(row) * (H + ep.F) + H + (col0 - 3 * H), v);
+    }
+  } else {  // kEpiResidual
+    const uint4* x4 = reinterpret_cast<const uint4*>(ep.resid + int64_t(row) * ep.N + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u = x4[q];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+        float2 f = __bfloat1622float2(p);
+        v[8 * q + 2 * e] += f.x;
+        v[8 * q + 2 * e + 1] += f.y;
+      }
+    }
+    store_row32(ep.y + int64_t(row) * ep.N + col0, v);
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                int K, const EpiParams ep, int* status, uint64_t limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(STAGES) * STAGE_BYTES);
+  const uint32_t full0 = smem_u32(bars);                 // [STAGES] TMA landed
+  const uint32_t empty0 = smem_u32(bars + STAGES);       // [STAGES] MMAs done reading
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);   // [2] accumulator ready
+  const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);  // [2] accumulator drained
+  const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (cta_should_skip(status)) return;
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, status, limit_ns};
+
+  const int num_m = (ep.M + BM - 1) / BM;
+  const int num_n = (ep.N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = K / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      uint32_t last_par[STAGES];
+      uint32_t used = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, wc, 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + size_t(stage) * STAGE_BYTES);
+          mbar_arrive_expect_tx(full0 + 8 * stage, STAGE_BYTES);
+          tma_load_2d(sa, &tmA, full0 + 8 * stage, kb * BK, m0);
+          tma_load_2d(sa + A_BYTES, &tmB, full0 + 8 * stage, kb * BK, n0);
+          last_par[stage] = phase;
+          used |= 1u << stage;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Every copy this thread started must land before the CTA exits.
+      for (int s = 0; s < STAGES; ++s)
+        if (used & (1u << s)) mbar_wait_drain(full0 + 8 * s, last_par[s], limit_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1, wc, 2)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, wc, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + size_t(stage) * STAGE_BYTES);
+          const uint64_t da = sdesc_kmajor_sw128(sa);
+          const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_ss(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) acc_par ^= 1;
+      }
+      // Every MMA this thread issued must finish before tensor memory is released.
+      mma_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0, limit_ns);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue warps
+    const uint32_t quad = warp & 3;
+    int acc = 0;
+    uint32_t acc_par = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      if (!mbar_wait_warp(tfull0 + 8 * acc, acc_par, wc, 4)) break;
+      tc_fence_after();
+      const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+      const int row = m0 + int(quad * 32 + lane);
+      const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= ep.N) break;
+        uint32_t r[32];
+        tmem_ld32(taddr + uint32_t(c * 32), r);
+        tmem_ld_wait(r);
+        epilogue32<KIND>(ep, row, col0, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_par ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
+                        const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
+                        cudaStream_t stream) {
+  static cudaError_t attr = cudaFuncSetAttribute(
+      gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
+  if (attr != cudaSuccess) return attr;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  EpiParams e = ep;
+  e.M = M;
+  e.N = N;
+  gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, K, e, status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB, int M,
+                        int N, int K, const EpiParams& ep, int num_sms, int* status,
+                        uint64_t limit_ns, cudaStream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  switch (kind) {
+    case kEpiStore:
+      return launch_kind<kEpiStore>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, stream);
+    case kEpiBlockIn:
+      return launch_kind<kEpiBlockIn>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, stream);
+    case kEpiResidual:
+      return launch_kind<kEpiResidual>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,
+                                       stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pb

@@ -1,0 +1,75 @@
+// kernels.h — launch interface between the C ABI (pb_api.cu) and the sm_103a kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pb {
+
+// ---------------------------------------------------------------- LayerNorm (ln.cu)
+constexpr int kLnMaxH = 16384;
+cudaError_t launch_layernorm(int64_t rows, int H, const __nv_bfloat16* x,
+                             const __nv_bfloat16* gamma, const __nv_bfloat16* beta, float eps,
+                             __nv_bfloat16* out, cudaStream_t stream);
+
+// ---------------------------------------------------------------- GEMM (gemm.cu)
+// D[M, N] = A[M, K] * B[N, K]^T with tcgen05; A and B come in through TMA tensor maps
+// (bf16, 128-byte swizzle, boxes of 64 x kGemmBM rows for A and 64 x kGemmBN rows for B).
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 64;
+
+enum EpiKind : int {
+  kEpiStore = 0,     // C = bf16(D)
+  kEpiBlockIn = 1,   // D = xn [Wqkv | W1]: route q|k, v (transposed per head), GeLU(h)
+  kEpiResidual = 2,  // y = bf16(D + bias + x)
+};
+
+struct EpiParams {
+  int M, N;
+  // kEpiStore
+  __nv_bfloat16* c;
+  int64_t ldc;
+  // kEpiBlockIn
+  int H, F, S, nh, dh;
+  int64_t seq_pad;
+  __nv_bfloat16* qk;   // [T, 2H]
+  __nv_bfloat16* vt;   // [B*nh*dh, seq_pad]
+  __nv_bfloat16* act;  // [T, H + F]; GeLU(h) goes to columns [H, H + F)
+  // kEpiBlockIn / kEpiResidual: fp32 bias of the N output columns, or null
+  const float* bias;
+  // kEpiResidual
+  const __nv_bfloat16* resid;  // [M, N]
+  __nv_bfloat16* y;            // [M, N]
+};
+
+size_t gemm_smem_bytes();
+cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB, int M,
+                        int N, int K, const EpiParams& ep, int num_sms, int* status,
+                        uint64_t limit_ns, cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention (swa.cu)
+struct SwaParams {
+  int B, S, H, nh, dh, window;
+  int num_q_tiles;
+  float scale_log2;    // log2(e) / sqrt(dh)
+  __nv_bfloat16* out;  // attention output, row (b*S + i), columns [head*dh, (head+1)*dh)
+  int64_t out_ld;
+};
+constexpr int kSwaBQ = 128;
+constexpr int kSwaBKV = 128;
+cudaError_t launch_swa(const CUtensorMap& tmQK, const CUtensorMap& tmVT, const SwaParams& p,
+                       int* status, uint64_t limit_ns, cudaStream_t stream);
+
+// ---------------------------------------------------------------- packing (pack.cu)
+// out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols.
+cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
+                             __nv_bfloat16* out, int64_t ld_out, cudaStream_t stream);
+// bias1[3H + F] = [b_qkv | b1] (0 where absent); bias2[H] = b_o + b2.
+cudaError_t launch_bias_prep(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
+                             const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
+                             float* bias1, float* bias2, cudaStream_t stream);
+
+}  // namespace pb

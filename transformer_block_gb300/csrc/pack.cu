@@ -1,0 +1,72 @@
+// pack.cu — one-time packing of the block's weights (run by pb_create, not per forward).
+//
+// The pages store a linear layer as W [in, out] with Y = X W (Megatron-LM notes, section
+// 2.1). The tensor-core GEMM reads its B operand K-major, [out, in], so each weight is
+// transposed once into the two concatenated operands:
+//   W1cat [3H + F, H] = [Wqkv | W1]^T        W2cat [H, H + F] = [Wo ; W2]^T
+// and the optional biases are gathered into fp32 vectors of the GEMMs' output columns.
+#include "kernels.h"
+
+namespace pb {
+namespace {
+
+constexpr int TILE = 32;
+
+// out[c * ld_out + r] = in[r * ld_in + c], through a padded 32 x 32 shared-memory tile so
+// both the reads and the writes are coalesced.
+__global__ void transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t rows, int64_t cols,
+                                 int64_t ld_in, __nv_bfloat16* __restrict__ out, int64_t ld_out) {
+  __shared__ __nv_bfloat16 tile[TILE][TILE + 2];
+  const int64_t r0 = int64_t(blockIdx.y) * TILE, c0 = int64_t(blockIdx.x) * TILE;
+  for (int i = threadIdx.y; i < TILE; i += blockDim.y) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = in[r * ld_in + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < TILE; i += blockDim.y) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[c * ld_out + r] = tile[threadIdx.x][i];
+  }
+}
+
+__global__ void bias_prep_kernel(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
+                                 const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
+                                 float* bias1, float* bias2) {
+  const int n1 = 3 * H + F;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n1; i += gridDim.x * blockDim.x) {
+    float v = 0.f;
+    if (i < 3 * H) {
+      if (b_qkv) v = __bfloat162float(b_qkv[i]);
+    } else if (b1) {
+      v = __bfloat162float(b1[i - 3 * H]);
+    }
+    bias1[i] = v;
+    if (i < H) {
+      float w = 0.f;
+      if (b_o) w += __bfloat162float(b_o[i]);
+      if (b2) w += __bfloat162float(b2[i]);
+      bias2[i] = w;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
+                             __nv_bfloat16* out, int64_t ld_out, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int64_t gx = (cols + TILE - 1) / TILE, gy = (rows + TILE - 1) / TILE;
+  if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidValue;
+  transpose_kernel<<<dim3(unsigned(gx), unsigned(gy)), dim3(TILE, 8), 0, stream>>>(
+      in, rows, cols, ld_in, out, ld_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_prep(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
+                             const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
+                             float* bias1, float* bias2, cudaStream_t stream) {
+  bias_prep_kernel<<<256, 256, 0, stream>>>(b_qkv, b1, b_o, b2, H, F, bias1, bias2);
+  return cudaGetLastError();
+}
+
+}  // namespace pb

@@ -1,0 +1,253 @@
+"""Python binding of the C ABI in ``include/pb.h`` (argument marshalling only).
+
+Every step of the forward pass runs in ``libpb.so``'s kernels; PyTorch only supplies
+device memory and the current CUDA stream. There is no fallback: if the library has not
+been built, or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+from .configs import Workload
+
+PB_OK = 0
+STATUS_NAMES = {0: "PB_OK", 1: "PB_ERR_INVALID_ARG", 2: "PB_ERR_UNSUPPORTED",
+                3: "PB_ERR_WORKSPACE", 4: "PB_ERR_CUDA", 5: "PB_ERR_DEVICE_TIMEOUT",
+                6: "PB_ERR_BAD_HANDLE"}
+
+
+class PbError(RuntimeError):
+    def __init__(self, func: str, status: int, message: str):
+        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class pb_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seq", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("ln_eps", ctypes.c_float)]
+
+
+WEIGHT_FIELDS = ["ln_gamma", "ln_beta", "wqkv", "w1", "wo", "w2", "b_qkv", "b1", "b_o", "b2"]
+
+
+class pb_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class pb_scratch_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("xn", "qk", "vt", "act", "io0", "io1", "seq_pad", "total")]
+
+
+# name -> (restype, argtypes); every function of include/pb.h
+_P, _S, _I32, _I64, _U64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64, \
+    ctypes.c_uint64
+_DP = ctypes.POINTER(pb_dims)
+SIGNATURES = {
+    "pb_weight_workspace_bytes": (ctypes.c_int, [_DP, ctypes.POINTER(_S)]),
+    "pb_scratch_bytes": (ctypes.c_int, [_DP, ctypes.POINTER(_S)]),
+    "pb_get_scratch_layout": (ctypes.c_int, [_DP, ctypes.POINTER(pb_scratch_layout)]),
+    "pb_create": (ctypes.c_int, [_DP, ctypes.POINTER(pb_weights), _P, _S, _P,
+                                 ctypes.POINTER(_P)]),
+    "pb_forward": (ctypes.c_int, [_P, _P, _P, _P, _S, _P]),
+    "pb_forward_stack": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
+    "pb_forward_stack_host": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
+    "pb_get_status": (ctypes.c_int, [_P]),
+    "pb_clear_status": (ctypes.c_int, [_P, _P]),
+    "pb_set_wait_limit_ns": (ctypes.c_int, [_P, _U64]),
+    "pb_destroy": (ctypes.c_int, [_P]),
+    "pb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pb_last_error_message": (ctypes.c_char_p, []),
+    "pb_layernorm": (ctypes.c_int, [_I64, _I32, _P, _P, _P, ctypes.c_float, _P, _P]),
+    "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "pb_swa_attention": (ctypes.c_int, [_DP, _P, _P, _P, _I64, _P, _P]),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded ``libpb.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with transformer_block_gb300.build."
+                               "build(); the forward pass has no other implementation")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(func: str, status: int):
+    if status != PB_OK:
+        msg = lib().pb_last_error_message()
+        raise PbError(func, status, msg.decode() if msg else "")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_dims(wl: Workload | None = None, **kw) -> pb_dims:
+    src = dict(wl.__dict__) if wl is not None else {}
+    src.update(kw)
+    return pb_dims(src["batch"], src["seq"], src["hidden"], src["heads"], src["head_dim"],
+                   src["ffn"], src["window"], float(src.get("ln_eps", 1e-5)))
+
+
+def weight_workspace_bytes(dims: pb_dims) -> int:
+    n = ctypes.c_size_t()
+    _check("pb_weight_workspace_bytes", lib().pb_weight_workspace_bytes(ctypes.byref(dims),
+                                                                        ctypes.byref(n)))
+    return n.value
+
+
+def scratch_bytes(dims: pb_dims) -> int:
+    n = ctypes.c_size_t()
+    _check("pb_scratch_bytes", lib().pb_scratch_bytes(ctypes.byref(dims), ctypes.byref(n)))
+    return n.value
+
+
+def scratch_layout(dims: pb_dims) -> pb_scratch_layout:
+    L = pb_scratch_layout()
+    _check("pb_get_scratch_layout", lib().pb_get_scratch_layout(ctypes.byref(dims),
+                                                                ctypes.byref(L)))
+    return L
+
+
+def new_scratch(dims: pb_dims, device="cuda") -> torch.Tensor:
+    return torch.empty(scratch_bytes(dims), dtype=torch.uint8, device=device)
+
+
+def scratch_view(scratch: torch.Tensor, dims: pb_dims, name: str) -> torch.Tensor:
+    """A bf16 view of one intermediate in the scratch (``xn, qk, vt, act, io0, io1``)."""
+    L = scratch_layout(dims)
+    T, H, F = dims.batch * dims.seq, dims.hidden, dims.ffn
+    shapes = {"xn": (T, H), "qk": (T, 2 * H), "act": (T, H + F), "io0": (T, H), "io1": (T, H),
+              "vt": (dims.batch, dims.heads, dims.head_dim, L.seq_pad)}
+    shape = shapes[name]
+    n = 1
+    for s in shape:
+        n *= s
+    off = getattr(L, name)
+    return scratch[off:off + 2 * n].view(torch.bfloat16).view(*shape)
+
+
+class ParallelBlock:
+    """One parallel transformer block: a ``pb_handle`` plus the workspace it owns."""
+
+    def __init__(self, dims: pb_dims, params: dict, stream=None):
+        self.dims = dims
+        self._lib = lib()
+        dev = params["wqkv"].device
+        self.workspace = torch.empty(weight_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+        w = pb_weights(*[_ptr(params.get(n)) for n in WEIGHT_FIELDS])
+        h = ctypes.c_void_p()
+        _check("pb_create", self._lib.pb_create(ctypes.byref(dims), ctypes.byref(w),
+                                                _ptr(self.workspace), self.workspace.numel(),
+                                                _stream(stream), ctypes.byref(h)))
+        self.handle = h
+
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None,
+                scratch: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if y is None:
+            y = torch.empty_like(x)
+        if scratch is None:
+            scratch = new_scratch(self.dims, x.device)
+        _check("pb_forward", self._lib.pb_forward(self.handle, _ptr(x), _ptr(y), _ptr(scratch),
+                                                  scratch.numel(), _stream(stream)))
+        return y
+
+    __call__ = forward
+
+    def status(self) -> int:
+        return self._lib.pb_get_status(self.handle)
+
+    def clear_status(self, stream=None):
+        _check("pb_clear_status", self._lib.pb_clear_status(self.handle, _stream(stream)))
+
+    def set_wait_limit_ns(self, ns: int):
+        _check("pb_set_wait_limit_ns", self._lib.pb_set_wait_limit_ns(self.handle, int(ns)))
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            _check("pb_destroy", self._lib.pb_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _handles(blocks):
+    arr = (ctypes.c_void_p * len(blocks))(*[b.handle.value for b in blocks])
+    return arr
+
+
+def forward_stack(blocks, x, y=None, scratch=None, stream=None):
+    if y is None:
+        y = torch.empty_like(x)
+    if scratch is None:
+        scratch = new_scratch(blocks[0].dims, x.device)
+    _check("pb_forward_stack", lib().pb_forward_stack(_handles(blocks), len(blocks), _ptr(x),
+                                                      _ptr(y), _ptr(scratch), scratch.numel(),
+                                                      _stream(stream)))
+    return y
+
+
+def forward_stack_host(blocks, x_host, y_host, scratch, stream=None):
+    """Host (pinned) x -> device -> stack -> host y, enqueued on ``stream``."""
+    _check("pb_forward_stack_host",
+           lib().pb_forward_stack_host(_handles(blocks), len(blocks), _ptr(x_host), _ptr(y_host),
+                                       _ptr(scratch), scratch.numel(), _stream(stream)))
+    return y_host
+
+
+def layernorm(x, gamma, beta, eps=1e-5, out=None, stream=None):
+    if out is None:
+        out = torch.empty_like(x)
+    _check("pb_layernorm", lib().pb_layernorm(x.shape[0], x.shape[1], _ptr(x), _ptr(gamma),
+                                              _ptr(beta), float(eps), _ptr(out),
+                                              _stream(stream)))
+    return out
+
+
+def gemm(a, b, out=None, status=None, stream=None):
+    """``a [M, K] @ b[N, K]^T`` -> bf16 ``[M, N]`` on the tensor cores."""
+    M, K = a.shape
+    N = b.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _check("pb_gemm_bf16", lib().pb_gemm_bf16(M, N, K, _ptr(a), _ptr(b), _ptr(out),
+                                              _ptr(status), _stream(stream)))
+    return out
+
+
+def swa_attention(dims: pb_dims, qk, vt, act, status=None, stream=None):
+    _check("pb_swa_attention", lib().pb_swa_attention(ctypes.byref(dims), _ptr(qk), _ptr(vt),
+                                                      _ptr(act), act.shape[1], _ptr(status),
+                                                      _stream(stream)))
+    return act
