@@ -1,0 +1,376 @@
+"""Throughput of the parallel transformer block forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one forward pass of the whole block stack of the workload (LayerNorm, first
+GEMM with GeLU, sliding-window attention, second GEMM with the residual, per layer)
+through the C ABI, on inputs already resident in HBM. ``value`` is model TFLOP/s:
+2 FLOPs per weight per token plus 4*H per windowed (query, key) pair (the MFU
+convention of the Megatron-LM performance notes), summed over all ranks. ``e2e`` is the
+same metric through ``pb_forward_stack_host``: pinned host x in, host y out, copies
+inside the timed region. One JSON line is printed by rank 0.
+
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of the same
+workload (the first tokens of the sequence; causality makes that prefix an exact
+sub-problem), on this host's cores.
+
+Multi-GPU (``torchrun --nproc-per-node N bench.py --gpus N``): the forward pass needs
+no exchange between replicas, so every rank runs its own replica of the workload
+(weak scaling); ranks only meet at the barriers around the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "parallel-block fwd TFLOP/s and MFU vs GB300 dense BF16 peak (1 GPU)"
+UNIT = "TFLOP/s"
+# GB300 dense bf16 tensor-core peak, nominal (no sparsity), for MFU.
+SPEC_BF16_TFLOPS = 2250.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS = ["layernorm", "gemm_block_in", "swa_attention", "gemm_residual"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=192,
+                    help="tokens of the oracle's CPU-baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "transformer_block_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the first GEMM from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_source") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+class OracleSample:
+    """The fp64 oracle on the first `rows` tokens of sequence 0, every layer, full weights
+    (by causality an exact sub-problem of the workload). Inputs are drawn once; run()
+    times one pass."""
+
+    def __init__(self, wl, rows: int, threads: int = 0):
+        import numpy as np
+        import torch
+
+        from oracle import oracle as O
+        from transformer_block_gb300 import flops, inputs
+
+        self.O, self.threads = O, threads
+        P = min(rows, wl.seq)
+        sub = wl.with_(batch=1, seq=P)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        x, p0 = inputs.make_layer(sub, 0, seed=0, device=dev)
+        self.params = [{k: v.float().cpu().numpy() for k, v in p0.items()}]
+        del p0
+        for l in range(1, wl.layers):
+            p = inputs.make_layer(sub, l, seed=0, device=dev)[1]
+            self.params.append({k: v.float().cpu().numpy() for k, v in p.items()})
+            del p
+        self.x = x.float().cpu().numpy().reshape(1, P, wl.hidden).astype(np.float64)
+        self.dims = O.Dims(1, P, wl.hidden, wl.heads, wl.head_dim, wl.ffn, wl.window, wl.ln_eps)
+        self.rows = P
+        self.work = wl.layers * (flops.gemm_flops(sub)
+                                 + 4 * wl.hidden * flops.windowed_pairs(P, wl.window))
+        self.cores = O.threads_used(threads)
+
+    def run(self) -> float:
+        z = self.x
+        t0 = time.perf_counter()
+        for p in self.params:
+            z = self.O.block_forward(self.dims, z, p, threads=self.threads)
+        return time.perf_counter() - t0
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rows = min(wl.seq, 8)
+    sample = OracleSample(wl, rows)
+    cores = sample.cores
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = sample.run()
+        if i >= args.warmup:
+            times.append(dt)
+    value = sample.work * len(times) / sum(times) / 1e12
+    sample = (f"oracle fp64 on the first {rows} tokens of sequence 0, all {wl.layers} layer(s), "
+              f"full weights, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl, args):
+    return {"workload": wl.name, "batch": wl.batch, "seq": wl.seq, "hidden": wl.hidden,
+            "heads": wl.heads, "head_dim": wl.head_dim, "ffn": wl.ffn, "window": wl.window,
+            "layers": wl.layers, "weight_std": wl.weight_std,
+            "parallelism": f"replicas x{args.gpus} (no collective on the data path)",
+            "l2": "inputs larger than L2 (weights alone exceed the 129 MB L2)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse()
+    from transformer_block_gb300 import BENCH_WORKLOAD, WORKLOADS
+
+    wl = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import torch.distributed as dist
+
+    from transformer_block_gb300 import flops, inputs, pb
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # Inputs (seeded, synthetic, on the device) and one handle per layer.
+    x, layers = inputs.make_stack(wl, seed=rank, device="cuda")
+    dims = pb.make_dims(wl)
+    blocks = [pb.ParallelBlock(dims, p) for p in layers]
+    del layers
+    torch.cuda.empty_cache()
+    scratch = pb.new_scratch(dims)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pb.forward_stack(blocks, x, y, scratch)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for b in blocks:
+        if b.status() != pb.PB_OK:
+            raise RuntimeError("device status word reports an error after warm-up")
+        b.trace_enable(args.steps)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    per_kernel = [0.0] * 4
+    for b in blocks:
+        k_ms, n = b.trace_read()
+        assert n == args.steps
+        per_kernel = [a + c for a, c in zip(per_kernel, k_ms)]
+        b.trace_enable(0)
+    for b in blocks:
+        if b.status() != pb.PB_OK:
+            raise RuntimeError("device status word reports an error in the timed region")
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    model = flops.model_flops(wl)
+    value = world * model * args.steps / (ms / 1e3) / 1e12
+
+    # ---- end to end through the host-buffer entry point (pinned x in, y out)
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        n_e2e = max(3, min(args.steps, 20))
+        pb.forward_stack_host(blocks, xh, yh, scratch)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n_e2e):
+            pb.forward_stack_host(blocks, xh, yh, scratch)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = t0.elapsed_time(t1)
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        nbytes = x.numel() * x.element_size()
+        e2e = {"value": world * model * n_e2e / (e_ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+               "steps": n_e2e, "ms_per_step": e_ms / n_e2e,
+               "api": "pb_forward_stack_host"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (the first GEMM), timed live above
+    peaks, peak_src = load_peaks()
+    launches = args.steps * wl.layers
+    g1_ms = per_kernel[1] / launches
+    g1_flops = 2 * wl.tokens * wl.hidden * (3 * wl.hidden + wl.ffn)
+    achieved = g1_flops / (g1_ms / 1e3) / 1e12
+    traffic = profiled_traffic(wl.name)
+    roofline = {"kernel": "gemm_block_in (LN(x) [Wqkv | W1], GeLU epilogue)", "bound": "tensor",
+                "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "algorithmic_flops_per_launch": g1_flops, "ms_per_launch": g1_ms}
+    step_ms = ms / args.steps
+    kernels = {}
+    for name, k_ms in zip(KERNELS, per_kernel):
+        kernels[name] = {"ms_per_step": k_ms / args.steps,
+                         "share": k_ms / max(sum(per_kernel), 1e-9)}
+    att = flops.attention_flops(wl)
+    kernels["swa_attention"]["tflops"] = att / (per_kernel[2] / launches / 1e3) / 1e12
+    g2_flops = 2 * wl.tokens * wl.hidden * (wl.hidden + wl.ffn)
+    kernels["gemm_residual"]["tflops"] = g2_flops / (per_kernel[3] / launches / 1e3) / 1e12
+    kernels["gemm_block_in"]["tflops"] = achieved
+    ln_bytes = 4 * wl.tokens * wl.hidden + 4 * wl.hidden
+    kernels["layernorm"]["gbs"] = ln_bytes / (per_kernel[0] / launches / 1e3) / 1e9
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        smp = OracleSample(wl, args.cpu_rows)
+        work, dt, cores = smp.work, smp.run(), smp.cores
+        cpu = {"value": work / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"fp64 oracle on the first {min(args.cpu_rows, wl.seq)} tokens of "
+                         f"sequence 0 (exact causal prefix), all {wl.layers} layer(s), full "
+                         f"weights; {work / 1e12:.3f} TFLOP in {dt:.1f} s"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0, std) weights)",
+            "config": config_of(wl, args),
+            "mfu": {"vs_spec_dense_bf16": value / world / SPEC_BF16_TFLOPS,
+                    "spec_tflops": SPEC_BF16_TFLOPS,
+                    "vs_measured_bf16": value / world / peaks["bf16_tflops"],
+                    "measured_tflops": peaks["bf16_tflops"]},
+            "model_flops_per_step": model * world,
+            "kernels": kernels,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * wl.layers * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -48,7 +48,9 @@ typedef enum pb_status {
   PB_ERR_WORKSPACE = 3,       /* workspace or scratch smaller than required            */
   PB_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (message has why)   */
   PB_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait expired; results are invalid  */
-  PB_ERR_BAD_HANDLE = 6       /* NULL, destroyed or foreign handle, or wrong device    */
+  PB_ERR_BAD_HANDLE = 6,      /* NULL, destroyed or foreign handle, or wrong device    */
+  PB_ERR_RANGE = 7            /* PB_OPERANDS_FP16 only: a weight or an activation that */
+                              /* feeds a GEMM exceeded the fp16 range (|v| > 65504)    */
 } pb_status;
 
 /*
@@ -95,21 +97,40 @@ typedef struct pb_weights {
 
 /* Byte offsets of the intermediates inside the scratch buffer of a forward call, valid
  * after the stream passes it (for inspection and tests):
- *   xn  [T, H]          LN(x)
- *   qk  [T, 2H]         [q | k] (head-major columns, no bias folded away)
- *   vt  [batch, heads, dh, seq_pad] v transposed per head (seq_pad = seq rounded up to 8)
- *   act [T, H + F]      [attention output (before Wo) | GeLU(h)]
+ *   xn   [T, H]          LN(x)                      (bf16, fp16 with PB_OPERANDS_FP16)
+ *   qk   [T, 2H]         [q | k], head-major columns (bf16)
+ *   vt   [batch, heads, dh, seq_pad] v transposed per head, seq_pad = seq rounded up to 8
+ *   act  [T, H + F]      [attention output (before Wo) | GeLU(h)]  (bf16 / fp16)
+ *   io   [T, H]          bf16 staging of the host-buffer entry point
+ *   res0, res1 [T, H]    fp32 residual stream between the layers of a stack
  * T = batch * seq. */
 typedef struct pb_scratch_layout {
   size_t xn;
   size_t qk;
   size_t vt;
   size_t act;
-  size_t io0; /* [T, H] staging / layer ping-pong buffer */
-  size_t io1; /* [T, H] */
+  size_t io;
+  size_t res0;
+  size_t res1;
   size_t seq_pad;
   size_t total;
 } pb_scratch_layout;
+
+/* Precision of the two GEMMs' operands. The pages' mixed-precision recipe computes in
+ * bf16 with fp32 accumulation (Megatron-LM notes, section 5.4-5.5; performance notes,
+ * "BF16 / FP16 / FP8"), which is the default. PB_OPERANDS_FP16 stores LN(x), the packed
+ * weights, the attention output and GeLU(h) as fp16 instead: the same 16 bits and the
+ * same tensor-core rate, 3 more mantissa bits, and a range limit of 65504 that the
+ * kernels check (PB_ERR_RANGE). Attention (q, k, v, P) stays bf16 in both modes. */
+typedef enum pb_operand_precision {
+  PB_OPERANDS_BF16 = 0,
+  PB_OPERANDS_FP16 = 1
+} pb_operand_precision;
+
+typedef struct pb_options {
+  int32_t operand_precision; /* pb_operand_precision */
+  uint64_t wait_limit_ns;    /* limit of every bounded wait in the kernels; 0 = 2e9 */
+} pb_options;
 
 typedef struct pb_handle pb_handle;
 
@@ -128,6 +149,10 @@ pb_status pb_get_scratch_layout(const pb_dims* dims, pb_scratch_layout* layout);
 pb_status pb_create(const pb_dims* dims, const pb_weights* weights, void* workspace,
                     size_t workspace_bytes, void* stream, pb_handle** out);
 
+/* pb_create with options (NULL = defaults: bf16 operands, 2 s wait limit). */
+pb_status pb_create_ex(const pb_dims* dims, const pb_weights* weights, const pb_options* options,
+                       void* workspace, size_t workspace_bytes, void* stream, pb_handle** out);
+
 /* One block: y = x + MLP(LN(x)) + Attention(LN(x)). x, y: [batch*seq, hidden] bf16,
  * 16-byte aligned; y may equal x (in place), partial overlap is PB_ERR_INVALID_ARG.
  * `scratch` (device, 256-byte aligned, >= pb_scratch_bytes) must not be used by another
@@ -137,7 +162,9 @@ pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t
 
 /* A stack of residual blocks (MegaScale reading notes, section 1.1: L layers give a
  * receptive field of L*w), x_{l+1} = block_l(x_l). All handles must have the same
- * dims. Intermediate activations live in the scratch's io0/io1 buffers. */
+ * dims. Between layers the residual stream stays in fp32 (scratch res0/res1; the pages
+ * keep residual accumulation in BF16/FP32, performance notes, "BF16 / FP16 / FP8"): only
+ * x and the final y are bf16. */
 pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const void* x, void* y,
                            void* scratch, size_t scratch_bytes, void* stream);
 
@@ -157,6 +184,15 @@ pb_status pb_clear_status(pb_handle* h, void* stream);
  * (default 2e9). A wait that reaches it records PB_ERR_DEVICE_TIMEOUT and the kernel
  * returns. */
 pb_status pb_set_wait_limit_ns(pb_handle* h, uint64_t limit_ns);
+
+/* Per-kernel timing of this handle's forward calls. pb_trace_enable(h, n) makes the
+ * next n forward calls record CUDA events (host-side event objects, no device memory)
+ * around each of the block's four kernels on the call's stream; n = 0 turns tracing off.
+ * pb_trace_read waits for the recorded events and returns in ms[4] the summed
+ * milliseconds of [LayerNorm, first GEMM, attention, second GEMM] over the traced calls,
+ * and their number in *calls. */
+pb_status pb_trace_enable(pb_handle* h, int32_t n_calls);
+pb_status pb_trace_read(pb_handle* h, float* ms, int32_t* calls);
 
 /* Destroys the handle (host memory only; the caller frees the workspace). */
 pb_status pb_destroy(pb_handle* h);
@@ -186,6 +222,12 @@ pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const voi
  * layout's qk and vt buffers into columns [0, H) of `act` ([T, act_ld] bf16). */
 pb_status pb_swa_attention(const pb_dims* dims, const void* qk, const void* vt, void* act,
                            int64_t act_ld, int* status, void* stream);
+
+/* Failure-detection self-test: one thread waits, with the kernels' bounded-wait
+ * routine, on an mbarrier that nothing arrives at. After `limit_ns` it records
+ * PB_ERR_DEVICE_TIMEOUT in *status (a device int) and the kernel returns; no copy, MMA
+ * or tensor memory is involved, so the context stays usable. */
+pb_status pb_wait_probe(uint64_t limit_ns, int* status, void* stream);
 
 #ifdef __cplusplus
 }

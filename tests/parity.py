@@ -33,6 +33,14 @@ def assert_parity(g, r, what: str, max_tol=MAX_REL_TOL, mean_tol=MEAN_REL_TOL):
     assert mx <= max_tol and mn <= mean_tol, f"{what}: max_rel={mx:.3e} mean_rel={mn:.3e}"
 
 
+def report(g, r, what: str):
+    """Prints the metrics without asserting. Used for the branch sum y - x: its error is
+    dominated by the bf16 rounding of y itself (|y| ~ 1 while |y - x| ~ 0.05), so it has
+    no tolerance of its own; each branch is checked through the intermediates instead."""
+    mx, mn = metrics(g, r)
+    print(f"{what}: max_rel={mx:.3e} mean_rel={mn:.3e} (reported)")
+
+
 def host(t: torch.Tensor) -> np.ndarray:
     """Exact float32 copy of a bf16 tensor (every bf16 value is a float32)."""
     return t.detach().float().cpu().numpy()

@@ -71,10 +71,13 @@ def test_workspace_and_scratch_sizes(lib):
     L = pb.scratch_layout(d)
     assert L.seq_pad == 128
     assert L.total == pb.scratch_bytes(d)
-    for a, b in [("xn", "qk"), ("qk", "vt"), ("vt", "act"), ("act", "io0"), ("io0", "io1")]:
+    order = ["xn", "qk", "vt", "act", "io", "res0", "res1"]
+    for a, b in zip(order, order[1:]):
         assert getattr(L, a) < getattr(L, b) and getattr(L, b) % 1024 == 0
     assert L.act - L.vt >= 2 * 1 * H * 128
-    assert L.total - L.io1 >= 2 * T * H
+    assert L.res0 - L.io >= 2 * T * H
+    assert L.res1 - L.res0 >= 4 * T * H          # fp32 residual stream
+    assert L.total - L.res1 >= 4 * T * H
     # ragged sequences pad the transposed V to a multiple of 8 tokens
     assert pb.scratch_layout(dims(seq=130)).seq_pad == 136
 
@@ -98,6 +101,17 @@ def test_create_rejects_small_workspace(lib):
                          ctypes.byref(h)) == 3
     assert lib.pb_create(ctypes.byref(d), ctypes.byref(w), ctypes.c_void_p(0x4000001), 1 << 40,
                          None, ctypes.byref(h)) == 1  # misaligned workspace
+
+
+def test_create_rejects_bad_options(lib):
+    d = dims()
+    ptrs = [ctypes.c_void_p(0x100000 + 0x10000 * i) for i in range(6)] + [None] * 4
+    w = pb.pb_weights(*ptrs)
+    h = ctypes.c_void_p()
+    opt = pb.pb_options(5, 0)
+    assert lib.pb_create_ex(ctypes.byref(d), ctypes.byref(w), ctypes.byref(opt),
+                            ctypes.c_void_p(0x4000000), 1 << 40, None, ctypes.byref(h)) == 1
+    assert "operand_precision" in lib.pb_last_error_message().decode()
 
 
 def test_null_handles(lib):

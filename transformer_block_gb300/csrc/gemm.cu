@@ -32,17 +32,31 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32]) {
+template <bool F16>
+__device__ __forceinline__ void store_row32(void* dst, const float (&v)[32]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 u;
-    u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-    u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-    u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-    u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    if (F16) {
+      u.x = pack_f16x2(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack_f16x2(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack_f16x2(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack_f16x2(v[8 * q + 6], v[8 * q + 7]);
+    } else {
+      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    }
     d[q] = u;
   }
+}
+
+__device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 // Epilogue of 32 consecutive columns [col0, col0 + 32) of one output row.
@@ -65,11 +79,11 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
     }
   }
   if (KIND == kEpiStore) {
-    store_row32(ep.c + int64_t(row) * ep.ldc + col0, v);
+    store_row32<false>(ep.c + int64_t(row) * ep.ldc + col0, v);
   } else if (KIND == kEpiBlockIn) {
     const int H = ep.H;
     if (col0 < 2 * H) {  // q | k
-      store_row32(ep.qk + int64_t(row) * (2 * H) + col0, v);
+      store_row32<false>(ep.qk + int64_t(row) * (2 * H) + col0, v);
     } else if (col0 < 3 * H) {  // v, stored transposed per (sequence, head)
       const int c = col0 - 2 * H;
       const int head = c / ep.dh, d0 = c - head * ep.dh;
@@ -81,27 +95,53 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
     } else {  // h -> GeLU(h), next to the attention output in the second GEMM's A operand
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-      store_row32(ep.act + int64_t(row) * (H + ep.F) + H + (col0 - 3 * H), v);
-    }
-  } else {  // kEpiResidual
-    const uint4* x4 = reinterpret_cast<const uint4*>(ep.resid + int64_t(row) * ep.N + col0);
+      const int64_t off = int64_t(row) * (H + ep.F) + H + (col0 - 3 * H);
+      if (ep.act_f16) {
+        bool bad = false;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 u = x4[q];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-        float2 f = __bfloat1622float2(p);
-        v[8 * q + 2 * e] += f.x;
-        v[8 * q + 2 * e + 1] += f.y;
+        for (int i = 0; i < 32; ++i) bad |= !(fabsf(v[i]) <= kF16Max);
+        if (bad) report_range(ep.status);
+        store_row32<true>(static_cast<__half*>(ep.act) + off, v);
+      } else {
+        store_row32<false>(static_cast<__nv_bfloat16*>(ep.act) + off, v);
       }
     }
-    store_row32(ep.y + int64_t(row) * ep.N + col0, v);
+  } else {  // kEpiResidual: y = D + bias + x
+    const int64_t off = int64_t(row) * ep.N + col0;
+    if (ep.resid_f32) {
+      const float4* x4 = reinterpret_cast<const float4*>(static_cast<const float*>(ep.resid) + off);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 f = x4[q];
+        v[4 * q + 0] += f.x;
+        v[4 * q + 1] += f.y;
+        v[4 * q + 2] += f.z;
+        v[4 * q + 3] += f.w;
+      }
+    } else {
+      const uint4* x4 =
+          reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ep.resid) + off);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u = x4[q];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+          float2 f = __bfloat1622float2(p);
+          v[8 * q + 2 * e] += f.x;
+          v[8 * q + 2 * e + 1] += f.y;
+        }
+      }
+    }
+    if (ep.y_f32)
+      store_row32_f32(static_cast<float*>(ep.y) + off, v);
+    else
+      store_row32<false>(static_cast<__nv_bfloat16*>(ep.y) + off, v);
   }
 }
 
-template <int KIND>
+template <int KIND, bool F16>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int K, const EpiParams ep, int* status, uint64_t limit_ns) {
@@ -145,6 +185,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
+  // Teardown waits for the CTA's own copies and MMAs get at least a second, whatever the
+  // wait limit, so shared and tensor memory are never released under them.
+  const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
 
   const int num_m = (ep.M + BM - 1) / BM;
   const int num_n = (ep.N + BN - 1) / BN;
@@ -180,12 +223,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // Every copy this thread started must land before the CTA exits.
       for (int s = 0; s < STAGES; ++s)
-        if (used & (1u << s)) mbar_wait_drain(full0 + 8 * s, last_par[s], limit_ns);
+        if (used & (1u << s)) mbar_wait_drain(full0 + 8 * s, last_par[s], drain_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      const uint32_t idesc = idesc_f32acc(BM, BN, F16);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -206,7 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ss(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+            mma_f16kind_ss(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
           mma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
@@ -220,7 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // Every MMA this thread issued must finish before tensor memory is released.
       mma_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0, limit_ns);
+      mbar_wait_drain(drain_bar, 0, drain_ns);
     }
     __syncwarp();
   } else {
@@ -259,19 +302,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int KIND>
+template <int KIND, bool F16>
 cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
                         cudaStream_t stream) {
   static cudaError_t attr = cudaFuncSetAttribute(
-      gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
+      gemm_kernel<KIND, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
   if (attr != cudaSuccess) return attr;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   EpiParams e = ep;
   e.M = M;
   e.N = N;
-  gemm_kernel<KIND><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, K, e, status, limit_ns);
+  gemm_kernel<KIND, F16><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, K, e, status,
+                                                                limit_ns);
   return cudaGetLastError();
 }
 
@@ -279,19 +323,43 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
 
 size_t gemm_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB, int M,
-                        int N, int K, const EpiParams& ep, int num_sms, int* status,
+namespace {
+// The bounded wait of the kernels above, on a barrier that never completes.
+__global__ void wait_probe_kernel(uint64_t limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  const WaitCtl wc{&abort_flag, status, limit_ns};
+  mbar_wait(smem_u32(&bar), 0, wc, 99);
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(uint64_t limit_ns, int* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(EpiKind kind, bool ab_f16, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        int M, int N, int K, const EpiParams& ep, int num_sms, int* status,
                         uint64_t limit_ns, cudaStream_t stream) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+#define PB_GEMM_CASE(KIND_)                                                                 \
+  return ab_f16 ? launch_kind<KIND_, true>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, \
+                                           stream)                                           \
+                : launch_kind<KIND_, false>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, \
+                                            stream)
   switch (kind) {
     case kEpiStore:
-      return launch_kind<kEpiStore>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, stream);
+      PB_GEMM_CASE(kEpiStore);
     case kEpiBlockIn:
-      return launch_kind<kEpiBlockIn>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, stream);
+      PB_GEMM_CASE(kEpiBlockIn);
     case kEpiResidual:
-      return launch_kind<kEpiResidual>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,
-                                       stream);
+      PB_GEMM_CASE(kEpiResidual);
   }
+#undef PB_GEMM_CASE
   return cudaErrorInvalidValue;
 }
 

@@ -10,9 +10,12 @@ namespace pb {
 
 // ---------------------------------------------------------------- LayerNorm (ln.cu)
 constexpr int kLnMaxH = 16384;
-cudaError_t launch_layernorm(int64_t rows, int H, const __nv_bfloat16* x,
+constexpr int kStatusRange = 7;  // == PB_ERR_RANGE
+// x: [rows, H] bf16 (x_f32 false) or fp32; out: bf16 (out_f16 false) or fp16. With fp16
+// output a value beyond the fp16 range records kStatusRange in *status (may be null).
+cudaError_t launch_layernorm(int64_t rows, int H, const void* x, bool x_f32,
                              const __nv_bfloat16* gamma, const __nv_bfloat16* beta, float eps,
-                             __nv_bfloat16* out, cudaStream_t stream);
+                             void* out, bool out_f16, int* status, cudaStream_t stream);
 
 // ---------------------------------------------------------------- GEMM (gemm.cu)
 // D[M, N] = A[M, K] * B[N, K]^T with tcgen05; A and B come in through TMA tensor maps
@@ -29,6 +32,7 @@ enum EpiKind : int {
 
 struct EpiParams {
   int M, N;
+  int* status;  // device status word (fp16 range errors), may be null
   // kEpiStore
   __nv_bfloat16* c;
   int64_t ldc;
@@ -37,17 +41,21 @@ struct EpiParams {
   int64_t seq_pad;
   __nv_bfloat16* qk;   // [T, 2H]
   __nv_bfloat16* vt;   // [B*nh*dh, seq_pad]
-  __nv_bfloat16* act;  // [T, H + F]; GeLU(h) goes to columns [H, H + F)
+  void* act;           // [T, H + F]; GeLU(h) goes to columns [H, H + F)
+  bool act_f16;        // act holds fp16 (else bf16)
   // kEpiBlockIn / kEpiResidual: fp32 bias of the N output columns, or null
   const float* bias;
   // kEpiResidual
-  const __nv_bfloat16* resid;  // [M, N]
-  __nv_bfloat16* y;            // [M, N]
+  const void* resid;  // [M, N], fp32 if resid_f32 else bf16
+  void* y;            // [M, N], fp32 if y_f32 else bf16
+  bool resid_f32;
+  bool y_f32;
 };
 
 size_t gemm_smem_bytes();
-cudaError_t launch_gemm(EpiKind kind, const CUtensorMap& tmA, const CUtensorMap& tmB, int M,
-                        int N, int K, const EpiParams& ep, int num_sms, int* status,
+// ab_f16: A and B are fp16 (else bf16).
+cudaError_t launch_gemm(EpiKind kind, bool ab_f16, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        int M, int N, int K, const EpiParams& ep, int num_sms, int* status,
                         uint64_t limit_ns, cudaStream_t stream);
 
 // ---------------------------------------------------------------- attention (swa.cu)
@@ -55,8 +63,9 @@ struct SwaParams {
   int B, S, H, nh, dh, window;
   int num_q_tiles;
   float scale_log2;    // log2(e) / sqrt(dh)
-  __nv_bfloat16* out;  // attention output, row (b*S + i), columns [head*dh, (head+1)*dh)
+  void* out;  // attention output, row (b*S + i), columns [head*dh, (head+1)*dh)
   int64_t out_ld;
+  bool out_f16;  // write fp16 (else bf16)
 };
 constexpr int kSwaBQ = 128;
 constexpr int kSwaBKV = 128;
@@ -64,12 +73,17 @@ cudaError_t launch_swa(const CUtensorMap& tmQK, const CUtensorMap& tmVT, const S
                        int* status, uint64_t limit_ns, cudaStream_t stream);
 
 // ---------------------------------------------------------------- packing (pack.cu)
-// out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols.
+// out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols; with out_f16 the bf16
+// value is converted to fp16 (kStatusRange in *status if it is beyond the fp16 range).
 cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
-                             __nv_bfloat16* out, int64_t ld_out, cudaStream_t stream);
+                             void* out, int64_t ld_out, bool out_f16, int* status,
+                             cudaStream_t stream);
 // bias1[3H + F] = [b_qkv | b1] (0 where absent); bias2[H] = b_o + b2.
 cudaError_t launch_bias_prep(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
                              const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
                              float* bias1, float* bias2, cudaStream_t stream);
+
+// ---------------------------------------------------------------- self-test (gemm.cu)
+cudaError_t launch_wait_probe(uint64_t limit_ns, int* status, cudaStream_t stream);
 
 }  // namespace pb

@@ -1,18 +1,22 @@
 // ln.cu — LayerNorm of the token rows (the single LN shared by both branches of the
 // parallel block, MegaScale reading notes, section 1.1, eq. (4)).
 //
-// One 128-thread CTA per row. Each thread keeps its share of the row in registers as
-// 128-bit vectors (8 bf16), so x is read from HBM once; the mean and then the centred
-// variance are reduced across the CTA in fp32 (warp shuffles, then 4 partial sums in
-// shared memory); the normalised, affine-mapped row is written back as bf16 (round to
-// nearest even). HBM-bound: 2 bytes read + 2 bytes written per element.
+// One 256-thread CTA per row. Each thread keeps its share of the row in registers as
+// vectors of 8 elements (one 128-bit load of bf16, or two of fp32 for the fp32 residual
+// stream of a stack), so x is read from HBM once; the mean and then the centred
+// variance are reduced across the CTA in fp32 (warp shuffles, then 8 partial sums in
+// shared memory); the normalised, affine-mapped row is written back as bf16 or fp16
+// (round to nearest even). HBM-bound: one read and one write of the row.
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 
 namespace pb {
 namespace {
 
-constexpr int THREADS = 128;
-constexpr int MAXV = kLnMaxH / (8 * THREADS);  // 16 vectors per thread
+constexpr int THREADS = 256;
+constexpr int MAXV = kLnMaxH / (8 * THREADS);  // 8 vectors of 8 elements per thread
+constexpr float kF16Max = 65504.f;
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -20,12 +24,15 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  const float s = red[0] + red[1] + red[2] + red[3];
+  float s = 0.f;
+#pragma unroll
+  for (int w = 0; w < THREADS / 32; ++w) s += red[w];
   __syncthreads();
   return s;
 }
 
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+__device__ __forceinline__ void load8(const __nv_bfloat16* row, int idx, float (&f)[8]) {
+  const uint4 u = reinterpret_cast<const uint4*>(row)[idx];
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -35,31 +42,43 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   }
 }
 
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
+__device__ __forceinline__ void load8(const float* row, int idx, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(row)[2 * idx];
+  const float4 b = reinterpret_cast<const float4*>(row)[2 * idx + 1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-__global__ void __launch_bounds__(THREADS) layernorm_kernel(const uint4* __restrict__ x,
-                                                            const uint4* __restrict__ gamma,
-                                                            const uint4* __restrict__ beta,
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if (F16) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <typename TIn, bool F16>
+__global__ void __launch_bounds__(THREADS) layernorm_kernel(const TIn* __restrict__ x,
+                                                            const __nv_bfloat16* __restrict__ gamma,
+                                                            const __nv_bfloat16* __restrict__ beta,
                                                             uint4* __restrict__ out, int H,
-                                                            float eps) {
-  __shared__ float red[4];
+                                                            float eps, int* status) {
+  __shared__ float red[THREADS / 32];
   const int nv = H / 8;
   const int64_t row = blockIdx.x;
-  const uint4* xr = x + row * nv;
-  uint4 v[MAXV];
+  const TIn* xr = x + row * H;
+  float v[MAXV][8];
   float sum = 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int idx = threadIdx.x + i * THREADS;
     if (idx < nv) {
-      v[i] = xr[idx];
-      float f[8];
-      unpack8(v[i], f);
+      load8(xr, idx, v[i]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sum += f[e];
+      for (int e = 0; e < 8; ++e) sum += v[i][e];
     }
   }
   const float mean = block_sum(sum, red) / float(H);
@@ -68,44 +87,59 @@ __global__ void __launch_bounds__(THREADS) layernorm_kernel(const uint4* __restr
   for (int i = 0; i < MAXV; ++i) {
     const int idx = threadIdx.x + i * THREADS;
     if (idx < nv) {
-      float f[8];
-      unpack8(v[i], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sq += (f[e] - mean) * (f[e] - mean);
+      for (int e = 0; e < 8; ++e) sq += (v[i][e] - mean) * (v[i][e] - mean);
     }
   }
   const float var = block_sum(sq, red) / float(H);
   const float rstd = rsqrtf(var + eps);
   uint4* orow = out + row * nv;
+  bool out_of_range = false;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int idx = threadIdx.x + i * THREADS;
     if (idx < nv) {
-      float f[8], g[8], b[8];
-      unpack8(v[i], f);
-      unpack8(__ldg(gamma + idx), g);
-      unpack8(__ldg(beta + idx), b);
-      uint4 o;
-      o.x = pack2((f[0] - mean) * rstd * g[0] + b[0], (f[1] - mean) * rstd * g[1] + b[1]);
-      o.y = pack2((f[2] - mean) * rstd * g[2] + b[2], (f[3] - mean) * rstd * g[3] + b[3]);
-      o.z = pack2((f[4] - mean) * rstd * g[4] + b[4], (f[5] - mean) * rstd * g[5] + b[5]);
-      o.w = pack2((f[6] - mean) * rstd * g[6] + b[6], (f[7] - mean) * rstd * g[7] + b[7]);
-      orow[idx] = o;
+      float g[8], b[8], o[8];
+      load8(gamma, idx, g);
+      load8(beta, idx, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        o[e] = (v[i][e] - mean) * rstd * g[e] + b[e];
+        if (F16) out_of_range |= !(fabsf(o[e]) <= kF16Max);
+      }
+      uint4 u;
+      u.x = pack2<F16>(o[0], o[1]);
+      u.y = pack2<F16>(o[2], o[3]);
+      u.z = pack2<F16>(o[4], o[5]);
+      u.w = pack2<F16>(o[6], o[7]);
+      orow[idx] = u;
     }
   }
+  if (F16 && out_of_range && status != nullptr) atomicCAS(status, 0, kStatusRange);
+}
+
+template <typename TIn, bool F16>
+cudaError_t launch_t(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
+                     const __nv_bfloat16* beta, float eps, void* out, int* status,
+                     cudaStream_t stream) {
+  layernorm_kernel<TIn, F16><<<unsigned(rows), THREADS, 0, stream>>>(
+      static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), H, eps, status);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_layernorm(int64_t rows, int H, const __nv_bfloat16* x,
+cudaError_t launch_layernorm(int64_t rows, int H, const void* x, bool x_f32,
                              const __nv_bfloat16* gamma, const __nv_bfloat16* beta, float eps,
-                             __nv_bfloat16* out, cudaStream_t stream) {
+                             void* out, bool out_f16, int* status, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   if (H <= 0 || H % 8 != 0 || H > kLnMaxH || rows > 0x7fffffff) return cudaErrorInvalidValue;
-  layernorm_kernel<<<unsigned(rows), THREADS, 0, stream>>>(
-      reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(gamma),
-      reinterpret_cast<const uint4*>(beta), reinterpret_cast<uint4*>(out), H, eps);
-  return cudaGetLastError();
+  if (x_f32)
+    return out_f16 ? launch_t<float, true>(rows, H, x, gamma, beta, eps, out, status, stream)
+                   : launch_t<float, false>(rows, H, x, gamma, beta, eps, out, status, stream);
+  return out_f16
+             ? launch_t<__nv_bfloat16, true>(rows, H, x, gamma, beta, eps, out, status, stream)
+             : launch_t<__nv_bfloat16, false>(rows, H, x, gamma, beta, eps, out, status, stream);
 }
 
 }  // namespace pb

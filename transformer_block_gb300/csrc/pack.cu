@@ -5,6 +5,10 @@
 // transposed once into the two concatenated operands:
 //   W1cat [3H + F, H] = [Wqkv | W1]^T        W2cat [H, H + F] = [Wo ; W2]^T
 // and the optional biases are gathered into fp32 vectors of the GEMMs' output columns.
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace pb {
@@ -13,20 +17,33 @@ namespace {
 constexpr int TILE = 32;
 
 // out[c * ld_out + r] = in[r * ld_in + c], through a padded 32 x 32 shared-memory tile so
-// both the reads and the writes are coalesced.
+// both the reads and the writes are coalesced; TOut is bf16 (a copy) or fp16 (a
+// conversion, exact inside the fp16 range; values beyond it are reported).
+template <typename TOut>
 __global__ void transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t rows, int64_t cols,
-                                 int64_t ld_in, __nv_bfloat16* __restrict__ out, int64_t ld_out) {
-  __shared__ __nv_bfloat16 tile[TILE][TILE + 2];
+                                 int64_t ld_in, TOut* __restrict__ out, int64_t ld_out,
+                                 int* status) {
+  __shared__ float tile[TILE][TILE + 1];
   const int64_t r0 = int64_t(blockIdx.y) * TILE, c0 = int64_t(blockIdx.x) * TILE;
   for (int i = threadIdx.y; i < TILE; i += blockDim.y) {
     const int64_t r = r0 + i, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) tile[i][threadIdx.x] = in[r * ld_in + c];
+    if (r < rows && c < cols) tile[i][threadIdx.x] = __bfloat162float(in[r * ld_in + c]);
   }
   __syncthreads();
+  bool bad = false;
   for (int i = threadIdx.y; i < TILE; i += blockDim.y) {
     const int64_t c = c0 + i, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) out[c * ld_out + r] = tile[threadIdx.x][i];
+    if (r < rows && c < cols) {
+      const float v = tile[threadIdx.x][i];
+      if (sizeof(TOut) == 2 && std::is_same<TOut, __half>::value) {
+        bad |= !(fabsf(v) <= 65504.f);
+        out[c * ld_out + r] = TOut(__float2half_rn(v));
+      } else {
+        out[c * ld_out + r] = TOut(__float2bfloat16_rn(v));
+      }
+    }
   }
+  if (bad && status != nullptr) atomicCAS(status, 0, kStatusRange);
 }
 
 __global__ void bias_prep_kernel(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
@@ -53,12 +70,19 @@ __global__ void bias_prep_kernel(const __nv_bfloat16* b_qkv, const __nv_bfloat16
 }  // namespace
 
 cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
-                             __nv_bfloat16* out, int64_t ld_out, cudaStream_t stream) {
+                             void* out, int64_t ld_out, bool out_f16, int* status,
+                             cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const int64_t gx = (cols + TILE - 1) / TILE, gy = (rows + TILE - 1) / TILE;
   if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidValue;
-  transpose_kernel<<<dim3(unsigned(gx), unsigned(gy)), dim3(TILE, 8), 0, stream>>>(
-      in, rows, cols, ld_in, out, ld_out);
+  const dim3 grid{unsigned(gx), unsigned(gy), 1u}, block{unsigned(TILE), 8u, 1u};
+  if (out_f16)
+    transpose_kernel<__half><<<grid, block, 0, stream>>>(in, rows, cols, ld_in,
+                                                          static_cast<__half*>(out), ld_out,
+                                                          status);
+  else
+    transpose_kernel<__nv_bfloat16><<<grid, block, 0, stream>>>(
+        in, rows, cols, ld_in, static_cast<__nv_bfloat16*>(out), ld_out, status);
   return cudaGetLastError();
 }
 

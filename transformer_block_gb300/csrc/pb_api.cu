@@ -13,6 +13,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "../../include/pb.h"
 #include "kernels.h"
@@ -27,8 +28,9 @@ struct pb_handle {
   uint64_t limit_ns;
   uint8_t* ws;
   int* status;             // device status word
-  __nv_bfloat16* w1cat;    // [3H + F, H]
-  __nv_bfloat16* w2cat;    // [H, H + F]
+  bool f16;                // PB_OPERANDS_FP16
+  void* w1cat;             // [3H + F, H], bf16 or fp16
+  void* w2cat;             // [H, H + F], bf16 or fp16
   float* bias1;            // [3H + F]
   float* bias2;            // [H]
   __nv_bfloat16* gamma;    // [H]
@@ -36,6 +38,9 @@ struct pb_handle {
   bool has_bias;
   CUtensorMap tm_w1cat;
   CUtensorMap tm_w2cat;
+  std::vector<cudaEvent_t> trace;  // 5 events per traced call
+  int trace_max;
+  int trace_calls;
 };
 
 namespace {
@@ -133,10 +138,12 @@ pb_scratch_layout scratch_layout(const pb_dims& d) {
   off = align_up(off + size_t(d.batch) * H * L.seq_pad * 2, 1024);
   L.act = off;
   off = align_up(off + T * (H + F) * 2, 1024);
-  L.io0 = off;
+  L.io = off;
   off = align_up(off + T * H * 2, 1024);
-  L.io1 = off;
-  off = align_up(off + T * H * 2, 1024);
+  L.res0 = off;
+  off = align_up(off + T * H * 4, 1024);
+  L.res1 = off;
+  off = align_up(off + T * H * 4, 1024);
   L.total = off;
   return L;
 }
@@ -166,9 +173,10 @@ pb_status get_encoder(EncodeTiledFn* out) {
   return PB_OK;
 }
 
-// bf16 tensor of `rank` dims (dims[0] innermost), 128-byte swizzle, zero fill outside.
+// 16-bit tensor (bf16, or fp16 when f16) of `rank` dims (dims[0] innermost), 128-byte
+// swizzle, zero fill outside.
 pb_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                   const uint64_t* strides_bytes, const uint32_t* box) {
+                   const uint64_t* strides_bytes, const uint32_t* box, bool f16 = false) {
   EncodeTiledFn enc;
   pb_status s = get_encoder(&enc);
   if (s != PB_OK) return s;
@@ -179,20 +187,21 @@ pb_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d
     bx[i] = box[i];
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base),
+  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   cuuint32_t(rank), const_cast<void*>(base),
                    gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   return PB_OK;
 }
 
-// Row-major [rows, cols] bf16 matrix read in boxes of 64 columns x box_rows rows.
+// Row-major [rows, cols] 16-bit matrix read in boxes of 64 columns x box_rows rows.
 pb_status make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                      uint64_t ld, uint32_t box_rows) {
+                      uint64_t ld, uint32_t box_rows, bool f16 = false) {
   const uint64_t dims[2] = {cols, rows};
   const uint64_t strides[1] = {ld * 2};
   const uint32_t box[2] = {64, box_rows};
-  return make_map(m, base, 2, dims, strides, box);
+  return make_map(m, base, 2, dims, strides, box, f16);
 }
 
 pb_status check_handle(pb_handle* h) {
@@ -211,25 +220,35 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// One block from x to y, intermediates in `scratch`.
-pb_status run_block(pb_handle* h, const __nv_bfloat16* x, __nv_bfloat16* y, uint8_t* scratch,
-                    cudaStream_t st) {
+// One block from x to y (each bf16, or fp32 inside a stack's residual stream),
+// intermediates in `scratch`.
+pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32,
+                    uint8_t* scratch, cudaStream_t st) {
   const pb_dims& d = h->d;
   const pb_scratch_layout L = scratch_layout(d);
   const int H = d.hidden, F = d.ffn, T = d.batch * d.seq;
-  auto* xn = reinterpret_cast<__nv_bfloat16*>(scratch + L.xn);
+  void* xn = scratch + L.xn;
   auto* qk = reinterpret_cast<__nv_bfloat16*>(scratch + L.qk);
   auto* vt = reinterpret_cast<__nv_bfloat16*>(scratch + L.vt);
-  auto* act = reinterpret_cast<__nv_bfloat16*>(scratch + L.act);
+  void* act = scratch + L.act;
+
+  cudaEvent_t* ev = nullptr;
+  if (h->trace_calls < h->trace_max) ev = &h->trace[size_t(h->trace_calls++) * 5];
+  auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], st) : cudaSuccess; };
+  PB_CUDA(mark(0), "cudaEventRecord");
 
   // 1. the shared LayerNorm
-  PB_CUDA(pb::launch_layernorm(T, H, x, h->gamma, h->beta, d.ln_eps, xn, st), "layernorm launch");
+  PB_CUDA(pb::launch_layernorm(T, H, x, x_f32, h->gamma, h->beta, d.ln_eps, xn, h->f16,
+                               h->status, st),
+          "layernorm launch");
+  PB_CUDA(mark(1), "cudaEventRecord");
 
   // 2. [q | k | v | h] = xn [Wqkv | W1], GeLU(h) in the epilogue
   CUtensorMap tm_xn, tm_act, tm_qk, tm_vt;
-  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, pb::kGemmBM);
+  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, pb::kGemmBM, h->f16);
   if (s != PB_OK) return s;
   EpiParams e1{};
+  e1.status = h->status;
   e1.H = H;
   e1.F = F;
   e1.S = d.seq;
@@ -239,10 +258,12 @@ pb_status run_block(pb_handle* h, const __nv_bfloat16* x, __nv_bfloat16* y, uint
   e1.qk = qk;
   e1.vt = vt;
   e1.act = act;
+  e1.act_f16 = h->f16;
   e1.bias = h->has_bias ? h->bias1 : nullptr;
-  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, tm_xn, h->tm_w1cat, T, 3 * H + F, H, e1, h->num_sms,
-                          h->status, h->limit_ns, st),
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, h->tm_w1cat, T, 3 * H + F, H, e1,
+                          h->num_sms, h->status, h->limit_ns, st),
           "first GEMM launch");
+  PB_CUDA(mark(2), "cudaEventRecord");
 
   // 3. sliding-window attention -> act[:, 0:H]
   {
@@ -269,19 +290,32 @@ pb_status run_block(pb_handle* h, const __nv_bfloat16* x, __nv_bfloat16* y, uint
   sp.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d.head_dim)));
   sp.out = act;
   sp.out_ld = H + F;
+  sp.out_f16 = h->f16;
   PB_CUDA(pb::launch_swa(tm_qk, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
+  PB_CUDA(mark(3), "cudaEventRecord");
 
   // 4. y = x + [attn | GeLU(h)] [Wo ; W2] (+ b_o + b2)
-  s = make_map_2d(&tm_act, act, T, H + F, H + F, pb::kGemmBM);
+  s = make_map_2d(&tm_act, act, T, H + F, H + F, pb::kGemmBM, h->f16);
   if (s != PB_OK) return s;
   EpiParams e2{};
+  e2.status = h->status;
   e2.bias = h->has_bias ? h->bias2 : nullptr;
   e2.resid = x;
+  e2.resid_f32 = x_f32;
   e2.y = y;
-  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, tm_act, h->tm_w2cat, T, H, H + F, e2, h->num_sms,
-                          h->status, h->limit_ns, st),
+  e2.y_f32 = y_f32;
+  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->f16, tm_act, h->tm_w2cat, T, H, H + F, e2,
+                          h->num_sms, h->status, h->limit_ns, st),
           "second GEMM launch");
+  PB_CUDA(mark(4), "cudaEventRecord");
   return PB_OK;
+}
+
+void trace_free(pb_handle* h) {
+  for (cudaEvent_t e : h->trace) cudaEventDestroy(e);
+  h->trace.clear();
+  h->trace_max = 0;
+  h->trace_calls = 0;
 }
 
 pb_status check_stack(pb_handle* const* layers, int32_t n_layers, const void* scratch,
@@ -301,19 +335,21 @@ pb_status check_stack(pb_handle* const* layers, int32_t n_layers, const void* sc
   return PB_OK;
 }
 
-pb_status run_stack(pb_handle* const* layers, int32_t n, const __nv_bfloat16* x,
-                    __nv_bfloat16* y, uint8_t* scratch, cudaStream_t st) {
+// Layer 0 reads bf16 x, the last layer writes bf16 y; in between the residual stream
+// alternates between the fp32 buffers res0 and res1.
+pb_status run_stack(pb_handle* const* layers, int32_t n, const void* x, void* y,
+                    uint8_t* scratch, cudaStream_t st) {
   const pb_scratch_layout L = scratch_layout(layers[0]->d);
-  __nv_bfloat16* io[2] = {reinterpret_cast<__nv_bfloat16*>(scratch + L.io0),
-                          reinterpret_cast<__nv_bfloat16*>(scratch + L.io1)};
-  const __nv_bfloat16* in = x;
-  int next = (in == io[0]) ? 1 : 0;
+  void* res[2] = {scratch + L.res0, scratch + L.res1};
+  const void* in = x;
+  bool in_f32 = false;
   for (int32_t l = 0; l < n; ++l) {
-    __nv_bfloat16* out = (l == n - 1) ? y : io[next];
-    pb_status s = run_block(layers[l], in, out, scratch, st);
+    const bool last = (l == n - 1);
+    void* out = last ? y : res[l % 2];
+    pb_status s = run_block(layers[l], in, in_f32, out, !last, scratch, st);
     if (s != PB_OK) return s;
     in = out;
-    next ^= 1;
+    in_f32 = !last;
   }
   return PB_OK;
 }
@@ -331,6 +367,7 @@ const char* pb_status_string(pb_status s) {
     case PB_ERR_CUDA: return "PB_ERR_CUDA";
     case PB_ERR_DEVICE_TIMEOUT: return "PB_ERR_DEVICE_TIMEOUT";
     case PB_ERR_BAD_HANDLE: return "PB_ERR_BAD_HANDLE";
+    case PB_ERR_RANGE: return "PB_ERR_RANGE";
   }
   return "unknown pb_status";
 }
@@ -363,6 +400,11 @@ pb_status pb_get_scratch_layout(const pb_dims* dims, pb_scratch_layout* layout) 
 
 pb_status pb_create(const pb_dims* dims, const pb_weights* w, void* workspace,
                     size_t workspace_bytes, void* stream, pb_handle** out) {
+  return pb_create_ex(dims, w, nullptr, workspace, workspace_bytes, stream, out);
+}
+
+pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_options* options,
+                       void* workspace, size_t workspace_bytes, void* stream, pb_handle** out) {
   pb_status s = check_dims(dims);
   if (s != PB_OK) return s;
   if (out == nullptr) return fail(PB_ERR_INVALID_ARG, "out is NULL");
@@ -375,10 +417,15 @@ pb_status pb_create(const pb_dims* dims, const pb_weights* w, void* workspace,
     if (!aligned(req[i], 16))
       return fail(PB_ERR_INVALID_ARG, "weights.%s is not 16-byte aligned", names[i]);
   }
-  const void* opt[4] = {w->b_qkv, w->b1, w->b_o, w->b2};
+  const void* biases[4] = {w->b_qkv, w->b1, w->b_o, w->b2};
   for (int i = 0; i < 4; ++i)
-    if (opt[i] != nullptr && !aligned(opt[i], 2))
+    if (biases[i] != nullptr && !aligned(biases[i], 2))
       return fail(PB_ERR_INVALID_ARG, "a bias pointer is misaligned");
+  pb_options opt{PB_OPERANDS_BF16, 0};
+  if (options != nullptr) opt = *options;
+  if (opt.operand_precision != PB_OPERANDS_BF16 && opt.operand_precision != PB_OPERANDS_FP16)
+    return fail(PB_ERR_INVALID_ARG, "operand_precision %d is not a pb_operand_precision",
+                opt.operand_precision);
   const WsLayout L = ws_layout(*dims);
   if (workspace == nullptr || !aligned(workspace, 256))
     return fail(PB_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
@@ -395,11 +442,12 @@ pb_status pb_create(const pb_dims* dims, const pb_weights* w, void* workspace,
   h->d = *dims;
   h->device = dev;
   h->num_sms = sms;
-  h->limit_ns = kDefaultLimitNs;
+  h->limit_ns = opt.wait_limit_ns ? opt.wait_limit_ns : kDefaultLimitNs;
+  h->f16 = opt.operand_precision == PB_OPERANDS_FP16;
   h->ws = static_cast<uint8_t*>(workspace);
   h->status = reinterpret_cast<int*>(h->ws + L.status);
-  h->w1cat = reinterpret_cast<__nv_bfloat16*>(h->ws + L.w1cat);
-  h->w2cat = reinterpret_cast<__nv_bfloat16*>(h->ws + L.w2cat);
+  h->w1cat = h->ws + L.w1cat;
+  h->w2cat = h->ws + L.w2cat;
   h->bias1 = reinterpret_cast<float*>(h->ws + L.bias1);
   h->bias2 = reinterpret_cast<float*>(h->ws + L.bias2);
   h->gamma = reinterpret_cast<__nv_bfloat16*>(h->ws + L.gamma);
@@ -421,11 +469,18 @@ pb_status pb_create(const pb_dims* dims, const pb_weights* w, void* workspace,
   } while (0)
   PB_CUDA_H(cudaMemsetAsync(h->status, 0, 256, st), "cudaMemsetAsync(status)");
   // W1cat rows [0, 3H) = Wqkv^T, rows [3H, 3H + F) = W1^T
-  PB_CUDA_H(pb::launch_transpose(bf(w->wqkv), H, 3 * H, 3 * H, h->w1cat, H, st), "pack Wqkv");
-  PB_CUDA_H(pb::launch_transpose(bf(w->w1), H, F, F, h->w1cat + 3 * H * H, H, st), "pack W1");
+  uint8_t* w1c = static_cast<uint8_t*>(h->w1cat);
+  uint8_t* w2c = static_cast<uint8_t*>(h->w2cat);
+  PB_CUDA_H(pb::launch_transpose(bf(w->wqkv), H, 3 * H, 3 * H, w1c, H, h->f16, h->status, st),
+            "pack Wqkv");
+  PB_CUDA_H(pb::launch_transpose(bf(w->w1), H, F, F, w1c + 3 * H * H * 2, H, h->f16, h->status,
+                                 st),
+            "pack W1");
   // W2cat columns [0, H) = Wo^T, columns [H, H + F) = W2^T
-  PB_CUDA_H(pb::launch_transpose(bf(w->wo), H, H, H, h->w2cat, H + F, st), "pack Wo");
-  PB_CUDA_H(pb::launch_transpose(bf(w->w2), F, H, H, h->w2cat + H, H + F, st), "pack W2");
+  PB_CUDA_H(pb::launch_transpose(bf(w->wo), H, H, H, w2c, H + F, h->f16, h->status, st),
+            "pack Wo");
+  PB_CUDA_H(pb::launch_transpose(bf(w->w2), F, H, H, w2c + H * 2, H + F, h->f16, h->status, st),
+            "pack W2");
   PB_CUDA_H(pb::launch_bias_prep(bf(w->b_qkv), bf(w->b1), bf(w->b_o), bf(w->b2), int(H), int(F),
                                  h->bias1, h->bias2, st),
             "bias prep");
@@ -434,8 +489,8 @@ pb_status pb_create(const pb_dims* dims, const pb_weights* w, void* workspace,
   PB_CUDA_H(cudaMemcpyAsync(h->beta, w->ln_beta, H * 2, cudaMemcpyDeviceToDevice, st),
             "copy beta");
 #undef PB_CUDA_H
-  s = make_map_2d(&h->tm_w1cat, h->w1cat, 3 * H + F, H, H, pb::kGemmBN);
-  if (s == PB_OK) s = make_map_2d(&h->tm_w2cat, h->w2cat, H, H + F, H + F, pb::kGemmBN);
+  s = make_map_2d(&h->tm_w1cat, h->w1cat, 3 * H + F, H, H, pb::kGemmBN, h->f16);
+  if (s == PB_OK) s = make_map_2d(&h->tm_w2cat, h->w2cat, H, H + F, H + F, pb::kGemmBN, h->f16);
   if (s != PB_OK) return cleanup(s);
   *out = h;
   return PB_OK;
@@ -453,8 +508,8 @@ pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t
   const pb_scratch_layout L = scratch_layout(h->d);
   if (overlap(x, n, scratch, L.total) || overlap(y, n, scratch, L.total))
     return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
-  return run_block(h, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y),
-                   static_cast<uint8_t*>(scratch), static_cast<cudaStream_t>(stream));
+  return run_block(h, x, false, y, false, static_cast<uint8_t*>(scratch),
+                   static_cast<cudaStream_t>(stream));
 }
 
 pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const void* x, void* y,
@@ -470,8 +525,7 @@ pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const voi
   const pb_scratch_layout L = scratch_layout(d);
   if (overlap(x, n, scratch, L.total) || overlap(y, n, scratch, L.total))
     return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
-  return run_stack(layers, n_layers, static_cast<const __nv_bfloat16*>(x),
-                   static_cast<__nv_bfloat16*>(y), static_cast<uint8_t*>(scratch),
+  return run_stack(layers, n_layers, x, y, static_cast<uint8_t*>(scratch),
                    static_cast<cudaStream_t>(stream));
 }
 
@@ -485,16 +539,14 @@ pb_status pb_forward_stack_host(pb_handle* const* layers, int32_t n_layers, cons
   const size_t n = size_t(d.batch) * d.seq * d.hidden * 2;
   const pb_scratch_layout L = scratch_layout(d);
   uint8_t* sc = static_cast<uint8_t*>(scratch);
-  auto* io0 = reinterpret_cast<__nv_bfloat16*>(sc + L.io0);
-  auto* io1 = reinterpret_cast<__nv_bfloat16*>(sc + L.io1);
+  void* io = sc + L.io;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  PB_CUDA(cudaMemcpyAsync(io0, x_host, n, cudaMemcpyHostToDevice, st), "copy x to the device");
-  // The last layer writes into whichever io buffer did not hold its input.
-  __nv_bfloat16* out = (n_layers % 2 == 1) ? io1 : io0;
-  if (n_layers == 1) out = io1;
-  s = run_stack(layers, n_layers, io0, out, sc, st);
+  PB_CUDA(cudaMemcpyAsync(io, x_host, n, cudaMemcpyHostToDevice, st), "copy x to the device");
+  // io holds x for layer 0 and receives y from the last layer (in place when there is one
+  // layer; later layers no longer read x).
+  s = run_stack(layers, n_layers, io, io, sc, st);
   if (s != PB_OK) return s;
-  PB_CUDA(cudaMemcpyAsync(y_host, out, n, cudaMemcpyDeviceToHost, st), "copy y to the host");
+  PB_CUDA(cudaMemcpyAsync(y_host, io, n, cudaMemcpyDeviceToHost, st), "copy y to the host");
   return PB_OK;
 }
 
@@ -523,9 +575,48 @@ pb_status pb_set_wait_limit_ns(pb_handle* h, uint64_t limit_ns) {
   return PB_OK;
 }
 
+pb_status pb_trace_enable(pb_handle* h, int32_t n_calls) {
+  pb_status s = check_handle(h);
+  if (s != PB_OK) return s;
+  if (n_calls < 0 || n_calls > (1 << 20)) return fail(PB_ERR_INVALID_ARG, "n_calls out of range");
+  trace_free(h);
+  h->trace.resize(size_t(n_calls) * 5, nullptr);
+  for (auto& e : h->trace) {
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) {
+      e = nullptr;
+      for (auto& f : h->trace)
+        if (f) cudaEventDestroy(f);
+      h->trace.clear();
+      return cuda_fail(err, "cudaEventCreate");
+    }
+  }
+  h->trace_max = n_calls;
+  return PB_OK;
+}
+
+pb_status pb_trace_read(pb_handle* h, float* ms, int32_t* calls) {
+  pb_status s = check_handle(h);
+  if (s != PB_OK) return s;
+  if (ms == nullptr || calls == nullptr) return fail(PB_ERR_INVALID_ARG, "ms or calls is NULL");
+  for (int k = 0; k < 4; ++k) ms[k] = 0.f;
+  for (int c = 0; c < h->trace_calls; ++c) {
+    cudaEvent_t* ev = &h->trace[size_t(c) * 5];
+    PB_CUDA(cudaEventSynchronize(ev[4]), "cudaEventSynchronize");
+    for (int k = 0; k < 4; ++k) {
+      float t = 0.f;
+      PB_CUDA(cudaEventElapsedTime(&t, ev[k], ev[k + 1]), "cudaEventElapsedTime");
+      ms[k] += t;
+    }
+  }
+  *calls = h->trace_calls;
+  return PB_OK;
+}
+
 pb_status pb_destroy(pb_handle* h) {
   if (h == nullptr) return fail(PB_ERR_BAD_HANDLE, "handle is NULL");
   if (h->magic != kMagic) return fail(PB_ERR_BAD_HANDLE, "handle is destroyed or invalid");
+  trace_free(h);
   h->magic = kDead;
   delete h;
   return PB_OK;
@@ -542,10 +633,8 @@ pb_status pb_layernorm(int64_t rows, int32_t H, const void* x, const void* gamma
   for (const void* p : ps)
     if (p == nullptr || !aligned(p, 16))
       return fail(PB_ERR_INVALID_ARG, "pointers must be 16-byte aligned device pointers");
-  PB_CUDA(pb::launch_layernorm(rows, H, static_cast<const __nv_bfloat16*>(x),
-                               static_cast<const __nv_bfloat16*>(gamma),
-                               static_cast<const __nv_bfloat16*>(beta), eps,
-                               static_cast<__nv_bfloat16*>(out),
+  PB_CUDA(pb::launch_layernorm(rows, H, x, false, static_cast<const __nv_bfloat16*>(gamma),
+                               static_cast<const __nv_bfloat16*>(beta), eps, out, false, nullptr,
                                static_cast<cudaStream_t>(stream)),
           "layernorm launch");
   return PB_OK;
@@ -570,7 +659,7 @@ pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const voi
   EpiParams ep{};
   ep.c = static_cast<__nv_bfloat16*>(C);
   ep.ldc = N;
-  PB_CUDA(pb::launch_gemm(pb::kEpiStore, ta, tb, M, N, K, ep, sms, status, kDefaultLimitNs,
+  PB_CUDA(pb::launch_gemm(pb::kEpiStore, false, ta, tb, M, N, K, ep, sms, status, kDefaultLimitNs,
                           static_cast<cudaStream_t>(stream)),
           "gemm launch");
   return PB_OK;
@@ -608,11 +697,22 @@ pb_status pb_swa_attention(const pb_dims* dims, const void* qk, const void* vt, 
   sp.window = d.window;
   sp.num_q_tiles = (d.seq + pb::kSwaBQ - 1) / pb::kSwaBQ;
   sp.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d.head_dim)));
-  sp.out = static_cast<__nv_bfloat16*>(act);
+  sp.out = act;
   sp.out_ld = act_ld;
+  sp.out_f16 = false;
   PB_CUDA(pb::launch_swa(tm_qk, tm_vt, sp, status, kDefaultLimitNs,
                          static_cast<cudaStream_t>(stream)),
           "attention launch");
+  return PB_OK;
+}
+
+pb_status pb_wait_probe(uint64_t limit_ns, int* status, void* stream) {
+  if (status == nullptr || !aligned(status, 4))
+    return fail(PB_ERR_INVALID_ARG, "status must be a 4-byte aligned device pointer");
+  if (limit_ns == 0 || limit_ns > 10000000000ull)
+    return fail(PB_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10]");
+  PB_CUDA(pb::launch_wait_probe(limit_ns, status, static_cast<cudaStream_t>(stream)),
+          "wait probe launch");
   return PB_OK;
 }
 

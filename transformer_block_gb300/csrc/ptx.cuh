@@ -4,11 +4,13 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace pb {
 
 constexpr int kStatusTimeout = 5;  // == PB_ERR_DEVICE_TIMEOUT
+constexpr uint64_t kDrainFloorNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -181,7 +183,7 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one instruction of K = 16 (bf16), fp32 accumulate.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+__device__ __forceinline__ void mma_f16kind_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -198,13 +200,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 D, M x N.
+// Instruction descriptor of kind::f16: A and B both bf16 (or both fp16 when f16), both
+// K-major, fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool f16 = false) {
+  return (1u << 4)                                   // D format: f32
+         | ((f16 ? 0u : 1u) << 7)                    // A format: f16 = 0, bf16 = 1
+         | ((f16 ? 0u : 1u) << 10)                   // B format
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4)                               // D format: f32
-         | (1u << 7)                             // A format: bf16
-         | (1u << 10)                            // B format: bf16
-         | (static_cast<uint32_t>(N >> 3) << 17) // N / 8
-         | (static_cast<uint32_t>(M >> 4) << 24);// M / 16
+  return idesc_f32acc(M, N, false);
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA with 128-byte
@@ -270,6 +276,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+constexpr float kF16Max = 65504.f;
+constexpr int kStatusRangeCode = 7;  // == PB_ERR_RANGE
+
+// Records an fp16 range error in the status word (first error wins).
+__device__ __forceinline__ void report_range(int* status) {
+  if (status != nullptr) atomicCAS(status, 0, kStatusRangeCode);
 }
 
 }  // namespace pb

@@ -111,6 +111,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
+  // Teardown waits for the CTA's own copies and MMAs get at least a second, whatever the
+  // wait limit, so shared and tensor memory are never released under them.
+  const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
   const uint32_t sQ = smem_u32(smem + L::Q_OFF);
   const uint32_t sKV = smem_u32(smem + L::KV_OFF);
   const uint32_t sP = smem_u32(smem + L::P_OFF);
@@ -143,9 +146,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         last_par[st] = par;
         used |= 1u << st;
       }
-      mbar_wait_drain(q_full, 0, limit_ns);
+      mbar_wait_drain(q_full, 0, drain_ns);
       for (int s = 0; s < 2; ++s)
-        if (used & (1u << s)) mbar_wait_drain(kv_full0 + 8 * s, last_par[s], limit_ns);
+        if (used & (1u << s)) mbar_wait_drain(kv_full0 + 8 * s, last_par[s], drain_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kk = 0; kk < BKV / 16; ++kk) {
           const uint64_t da = sdesc_kmajor_sw128(sP + (kk >> 2) * BOX) + 2 * (kk & 3);
           const uint64_t db = sdesc_kmajor_sw128(vbase + (kk >> 2) * L::VHALF) + 2 * (kk & 3);
-          mma_bf16_ss(t_o, da, db, id_o, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_f16kind_ss(t_o, da, db, id_o, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(kv_empty0 + 8 * (i & 1));
         mma_commit(o_ready);
@@ -187,14 +190,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t da = sdesc_kmajor_sw128(sQ + (kk >> 2) * BOX) + 2 * (kk & 3);
           const uint64_t db = sdesc_kmajor_sw128(kbase + (kk >> 2) * BOX) + 2 * (kk & 3);
-          mma_bf16_ss(t_s, da, db, id_s, kk > 0 ? 1u : 0u);
+          mma_f16kind_ss(t_s, da, db, id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(s_full0 + 8 * st);
         if (j > 0 && !issue_pv(j - 1)) ok = false;
       }
       if (ok) issue_pv(nkv - 1);
       mma_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0, limit_ns);
+      mbar_wait_drain(drain_bar, 0, drain_ns);
     }
     __syncwarp();
   } else {
@@ -293,29 +296,43 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && mbar_wait_warp(o_ready, (nkv - 1) & 1, wc, 18)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      __nv_bfloat16* dst = p.out + (int64_t(b) * p.S + i) * p.out_ld + head * DH;
+      const int64_t off = (int64_t(b) * p.S + i) * p.out_ld + head * DH;
+      bool bad = false;
 #pragma unroll
       for (int ch = 0; ch < DH / 32; ++ch) {
         uint32_t u[32];
         tmem_ld32(tmem_base + lane_addr + 256u + uint32_t(ch * 32), u);
         tmem_ld_wait(u);
         if (i < p.S) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(u[e]) * inv_l;
+          uint4* d4 = p.out_f16
+                          ? reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + off + ch * 32)
+                          : reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off +
+                                                     ch * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
+            const float* f = o + 8 * q;
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(u[8 * q + 0]) * inv_l,
-                              __uint_as_float(u[8 * q + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(u[8 * q + 2]) * inv_l,
-                              __uint_as_float(u[8 * q + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(u[8 * q + 4]) * inv_l,
-                              __uint_as_float(u[8 * q + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(u[8 * q + 6]) * inv_l,
-                              __uint_as_float(u[8 * q + 7]) * inv_l);
+            if (p.out_f16) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) bad |= !(fabsf(f[e]) <= kF16Max);
+              v.x = pack_f16x2(f[0], f[1]);
+              v.y = pack_f16x2(f[2], f[3]);
+              v.z = pack_f16x2(f[4], f[5]);
+              v.w = pack_f16x2(f[6], f[7]);
+            } else {
+              v.x = pack_bf16x2(f[0], f[1]);
+              v.y = pack_bf16x2(f[2], f[3]);
+              v.z = pack_bf16x2(f[4], f[5]);
+              v.w = pack_bf16x2(f[6], f[7]);
+            }
             d4[q] = v;
           }
         }
       }
+      if (bad) report_range(status);
     }
   }
 

@@ -16,9 +16,12 @@ from . import build as _build
 from .configs import Workload
 
 PB_OK = 0
+PB_ERR_DEVICE_TIMEOUT = 5
+PB_ERR_RANGE = 7
 STATUS_NAMES = {0: "PB_OK", 1: "PB_ERR_INVALID_ARG", 2: "PB_ERR_UNSUPPORTED",
                 3: "PB_ERR_WORKSPACE", 4: "PB_ERR_CUDA", 5: "PB_ERR_DEVICE_TIMEOUT",
-                6: "PB_ERR_BAD_HANDLE"}
+                6: "PB_ERR_BAD_HANDLE", 7: "PB_ERR_RANGE"}
+PB_OPERANDS_BF16, PB_OPERANDS_FP16 = 0, 1
 
 
 class PbError(RuntimeError):
@@ -42,7 +45,11 @@ class pb_weights(ctypes.Structure):
 
 class pb_scratch_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("xn", "qk", "vt", "act", "io0", "io1", "seq_pad", "total")]
+                ("xn", "qk", "vt", "act", "io", "res0", "res1", "seq_pad", "total")]
+
+
+class pb_options(ctypes.Structure):
+    _fields_ = [("operand_precision", ctypes.c_int32), ("wait_limit_ns", ctypes.c_uint64)]
 
 
 # name -> (restype, argtypes); every function of include/pb.h
@@ -55,18 +62,23 @@ SIGNATURES = {
     "pb_get_scratch_layout": (ctypes.c_int, [_DP, ctypes.POINTER(pb_scratch_layout)]),
     "pb_create": (ctypes.c_int, [_DP, ctypes.POINTER(pb_weights), _P, _S, _P,
                                  ctypes.POINTER(_P)]),
+    "pb_create_ex": (ctypes.c_int, [_DP, ctypes.POINTER(pb_weights),
+                                    ctypes.POINTER(pb_options), _P, _S, _P, ctypes.POINTER(_P)]),
     "pb_forward": (ctypes.c_int, [_P, _P, _P, _P, _S, _P]),
     "pb_forward_stack": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
     "pb_forward_stack_host": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
     "pb_get_status": (ctypes.c_int, [_P]),
     "pb_clear_status": (ctypes.c_int, [_P, _P]),
     "pb_set_wait_limit_ns": (ctypes.c_int, [_P, _U64]),
+    "pb_trace_enable": (ctypes.c_int, [_P, _I32]),
+    "pb_trace_read": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I32)]),
     "pb_destroy": (ctypes.c_int, [_P]),
     "pb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pb_last_error_message": (ctypes.c_char_p, []),
     "pb_layernorm": (ctypes.c_int, [_I64, _I32, _P, _P, _P, ctypes.c_float, _P, _P]),
     "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "pb_swa_attention": (ctypes.c_int, [_DP, _P, _P, _P, _I64, _P, _P]),
+    "pb_wait_probe": (ctypes.c_int, [_U64, _P, _P]),
 }
 
 _lib = None
@@ -140,33 +152,44 @@ def new_scratch(dims: pb_dims, device="cuda") -> torch.Tensor:
     return torch.empty(scratch_bytes(dims), dtype=torch.uint8, device=device)
 
 
-def scratch_view(scratch: torch.Tensor, dims: pb_dims, name: str) -> torch.Tensor:
-    """A bf16 view of one intermediate in the scratch (``xn, qk, vt, act, io0, io1``)."""
+def scratch_view(scratch: torch.Tensor, dims: pb_dims, name: str,
+                 dtype=torch.bfloat16) -> torch.Tensor:
+    """A view of one intermediate in the scratch (``xn, qk, vt, act, io, res0, res1``);
+    ``dtype`` is the element type it holds (fp16 for ``xn``/``act`` with fp16 operands,
+    fp32 for ``res0``/``res1``)."""
     L = scratch_layout(dims)
     T, H, F = dims.batch * dims.seq, dims.hidden, dims.ffn
-    shapes = {"xn": (T, H), "qk": (T, 2 * H), "act": (T, H + F), "io0": (T, H), "io1": (T, H),
+    shapes = {"xn": (T, H), "qk": (T, 2 * H), "act": (T, H + F), "io": (T, H),
+              "res0": (T, H), "res1": (T, H),
               "vt": (dims.batch, dims.heads, dims.head_dim, L.seq_pad)}
+    if name in ("res0", "res1"):
+        dtype = torch.float32
     shape = shapes[name]
     n = 1
     for s in shape:
         n *= s
     off = getattr(L, name)
-    return scratch[off:off + 2 * n].view(torch.bfloat16).view(*shape)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    return scratch[off:off + nbytes].view(dtype).view(*shape)
 
 
 class ParallelBlock:
     """One parallel transformer block: a ``pb_handle`` plus the workspace it owns."""
 
-    def __init__(self, dims: pb_dims, params: dict, stream=None):
+    def __init__(self, dims: pb_dims, params: dict, stream=None,
+                 operand_precision: int = PB_OPERANDS_BF16, wait_limit_ns: int = 0):
         self.dims = dims
+        self.operand_precision = operand_precision
         self._lib = lib()
         dev = params["wqkv"].device
         self.workspace = torch.empty(weight_workspace_bytes(dims), dtype=torch.uint8, device=dev)
         w = pb_weights(*[_ptr(params.get(n)) for n in WEIGHT_FIELDS])
+        opt = pb_options(operand_precision, wait_limit_ns)
         h = ctypes.c_void_p()
-        _check("pb_create", self._lib.pb_create(ctypes.byref(dims), ctypes.byref(w),
-                                                _ptr(self.workspace), self.workspace.numel(),
-                                                _stream(stream), ctypes.byref(h)))
+        _check("pb_create_ex", self._lib.pb_create_ex(ctypes.byref(dims), ctypes.byref(w),
+                                                      ctypes.byref(opt), _ptr(self.workspace),
+                                                      self.workspace.numel(), _stream(stream),
+                                                      ctypes.byref(h)))
         self.handle = h
 
     def forward(self, x: torch.Tensor, y: torch.Tensor | None = None,
@@ -189,6 +212,16 @@ class ParallelBlock:
 
     def set_wait_limit_ns(self, ns: int):
         _check("pb_set_wait_limit_ns", self._lib.pb_set_wait_limit_ns(self.handle, int(ns)))
+
+    def trace_enable(self, n_calls: int):
+        _check("pb_trace_enable", self._lib.pb_trace_enable(self.handle, int(n_calls)))
+
+    def trace_read(self):
+        """Summed ms of [LayerNorm, first GEMM, attention, second GEMM] and the call count."""
+        ms = (ctypes.c_float * 4)()
+        n = ctypes.c_int32()
+        _check("pb_trace_read", self._lib.pb_trace_read(self.handle, ms, ctypes.byref(n)))
+        return list(ms), n.value
 
     def close(self):
         if getattr(self, "handle", None) is not None and self.handle.value:
@@ -251,3 +284,8 @@ def swa_attention(dims: pb_dims, qk, vt, act, status=None, stream=None):
                                                       _ptr(act), act.shape[1], _ptr(status),
                                                       _stream(stream)))
     return act
+
+
+def wait_probe(limit_ns: int, status: torch.Tensor, stream=None):
+    """Runs the bounded-wait self-test kernel; ``status`` is a 1-element int32 CUDA tensor."""
+    _check("pb_wait_probe", lib().pb_wait_probe(int(limit_ns), _ptr(status), _stream(stream)))
