@@ -1,31 +1,41 @@
-// gemm.cu — persistent warp-specialised tcgen05 GEMM, D = A * B^T, with the epilogues of
-// the parallel block's two linear steps fused in:
+// gemm.cu — persistent warp-specialised tcgen05 GEMM on CTA pairs, D = A * B^T, with the
+// epilogues of the parallel block's two linear steps fused in:
 //   * [q | k | v | h] = LN(x) [Wqkv | W1], GeLU(h) applied in the epilogue (the fused
 //     QKV projection of the MegaScale reading notes, section 1.3, widened to the MLP's
 //     first linear because both read the same LN output in eq. (4));
 //   * y = x + [attn | GeLU(h)] [Wo ; W2] (+ bias), the residual sum of eq. (4) applied
 //     in the epilogue of the one GEMM that computes both branch outputs.
 //
-// CTA tile 128 x 256, K step 64 (one 128-byte swizzle row of bf16), 4-stage TMA ring.
-// Warp 0: TMA producer. Warp 1: TMEM allocation and the single MMA-issuing thread.
-// Warps 2-5: epilogue, one TMEM lane quadrant each (warp w reads lanes 32*(w%4)..+31).
-// The fp32 accumulator lives in tensor memory, double-buffered (2 x 256 columns), so
-// the epilogue of one tile overlaps the main loop of the next. Tiles are handed out
-// round-robin, M-block fastest, so CTAs running at the same time share B tiles in L2.
+// Two CTAs of a cluster (one per SM) compute one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256): each CTA loads, by TMA, its own 128 rows of A and
+// its half (128 rows) of the tile's 256 rows of B, 64 elements of K per stage, into a
+// 6-stage ring, and holds its 128 x 256 half of the fp32 accumulator in its tensor
+// memory (double-buffered, 2 x 256 columns, so the epilogue of one tile overlaps the
+// main loop of the next).
+//   warp 0     TMA producer (both CTAs), each CTA's copies signal its own barrier
+//   warp 1     even CTA: the MMA-issuing thread; odd CTA: relays "my stage landed" to
+//              the even CTA with a remote mbarrier arrive; both: tensor-memory owner
+//   warps 2-5  epilogue, one TMEM lane quadrant each (warp w reads lanes 32*(w%4)..+31)
+// MMA completion is multicast to both CTAs' barriers. Pair tiles are handed out
+// round-robin over the clusters, M fastest, so clusters running at the same time share
+// B tiles in L2.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace pb {
 namespace {
 
-constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int BM = kGemmBM;       // output rows per CTA
+constexpr int PM = 2 * kGemmBM;   // output rows per CTA pair
+constexpr int BN = kGemmBN;       // output columns per pair tile
+constexpr int BK = kGemmBK;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's rows of A
+constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr int NUM_BARS = 3 * STAGES + 5;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16;
 
 __device__ __forceinline__ float gelu_erf(float z) {
@@ -149,24 +159,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(STAGES) * STAGE_BYTES);
-  const uint32_t full0 = smem_u32(bars);                 // [STAGES] TMA landed
-  const uint32_t empty0 = smem_u32(bars + STAGES);       // [STAGES] MMAs done reading
-  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);   // [2] accumulator ready
-  const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);  // [2] accumulator drained
-  const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+  const uint32_t full0 = smem_u32(bars);                   // [STAGES] own copies landed
+  const uint32_t empty0 = smem_u32(bars + STAGES);         // [STAGES] pair MMAs done reading
+  const uint32_t peer0 = smem_u32(bars + 2 * STAGES);      // [STAGES] odd CTA's copies landed
+  const uint32_t tfull0 = smem_u32(bars + 3 * STAGES);     // [2] accumulator ready
+  const uint32_t tempty0 = smem_u32(bars + 3 * STAGES + 2);  // [2] accumulator drained (x8)
+  const uint32_t drain_bar = smem_u32(bars + 3 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  if (cta_should_skip(status)) return;
   const uint32_t warp = warp_id(), lane = lane_id();
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
+      mbar_init(peer0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, 8);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -177,11 +190,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
@@ -189,10 +203,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   // wait limit, so shared and tensor memory are never released under them.
   const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
 
-  const int num_m = (ep.M + BM - 1) / BM;
+  const int num_m = (ep.M + PM - 1) / PM;
   const int num_n = (ep.N + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int num_kb = K / BK;
+  const int cluster = int(blockIdx.x) >> 1, num_clusters = int(gridDim.x) >> 1;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -202,8 +217,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+      for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+        const int m0 = (t % num_m) * PM + int(rank) * BM;
+        const int n0 = (t / num_m) * BN + int(rank) * (BN / 2);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, wc, 1)) {
             ok = false;
@@ -226,20 +242,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (used & (1u << s)) mbar_wait_drain(full0 + 8 * s, last_par[s], drain_ns);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_f32acc(BM, BN, F16);
+      const uint32_t idesc = idesc_f32acc(PM, BN, F16);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_par = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
         if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1, wc, 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, wc, 3)) {
+          if (!mbar_wait(full0 + 8 * stage, phase, wc, 3) ||
+              !mbar_wait(peer0 + 8 * stage, phase, wc, 5)) {
             ok = false;
             break;
           }
@@ -249,21 +266,40 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_f16kind_ss(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-          mma_commit(empty0 + 8 * stage);
+            mma_f16kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(tfull0 + 8 * acc);
+        mma_commit_pair(tfull0 + 8 * acc, 0x3);
         acc ^= 1;
         if (acc == 0) acc_par ^= 1;
       }
-      // Every MMA this thread issued must finish before tensor memory is released.
-      mma_commit(drain_bar);
+      // Every MMA this thread issued (into both CTAs' tensor memory) must finish before
+      // either CTA releases it.
+      mma_commit_pair(drain_bar, 0x1);
       mbar_wait_drain(drain_bar, 0, drain_ns);
+    } else if (lane == 0) {
+      // ------------------------------------------------------------ odd CTA: relay
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, wc, 6)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(mapa_shared(peer0 + 8 * stage, 0));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
     }
     __syncwarp();
   } else {
@@ -271,10 +307,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t quad = warp & 3;
     int acc = 0;
     uint32_t acc_par = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int t = cluster; t < num_tiles; t += num_clusters) {
       if (!mbar_wait_warp(tfull0 + 8 * acc, acc_par, wc, 4)) break;
       tc_fence_after();
-      const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
+      const int m0 = (t % num_m) * PM + int(rank) * BM, n0 = (t / num_m) * BN;
       const int row = m0 + int(quad * 32 + lane);
       const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
@@ -288,7 +324,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(tempty0 + 8 * acc);
+        else
+          mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));
+      }
       acc ^= 1;
       if (acc == 0) acc_par ^= 1;
     }
@@ -296,9 +337,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still arrive on it or MMA into it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -306,17 +348,48 @@ template <int KIND, bool F16>
 cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
                         cudaStream_t stream) {
-  static cudaError_t attr = cudaFuncSetAttribute(
-      gemm_kernel<KIND, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
-  if (attr != cudaSuccess) return attr;
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
+  static int max_clusters = -1;
+  static cudaError_t attr_err = cudaSuccess;
+  if (max_clusters < 0) {
+    attr_err = cudaFuncSetAttribute(gemm_kernel<KIND, F16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
+    if (attr_err == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+      cfg.blockDim = dim3(THREADS, 1, 1);
+      cfg.dynamicSmemBytes = SMEM_BYTES;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      attr_err = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, F16>, &cfg);
+      max_clusters = (attr_err == cudaSuccess && n > 0) ? n : 0;
+    }
+  }
+  if (attr_err != cudaSuccess) return attr_err;
+  if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
+  const int tiles = ((M + PM - 1) / PM) * ((N + BN - 1) / BN);
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
   EpiParams e = ep;
   e.M = M;
   e.N = N;
-  gemm_kernel<KIND, F16><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, K, e, status,
-                                                                limit_ns);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, F16>, tmA, tmB, K, e, status, limit_ns);
 }
 
 }  // namespace

@@ -18,11 +18,12 @@ cudaError_t launch_layernorm(int64_t rows, int H, const void* x, bool x_f32,
                              void* out, bool out_f16, int* status, cudaStream_t stream);
 
 // ---------------------------------------------------------------- GEMM (gemm.cu)
-// D[M, N] = A[M, K] * B[N, K]^T with tcgen05; A and B come in through TMA tensor maps
-// (bf16, 128-byte swizzle, boxes of 64 x kGemmBM rows for A and 64 x kGemmBN rows for B).
-constexpr int kGemmBM = 128;
-constexpr int kGemmBN = 256;
+// D[M, N] = A[M, K] * B[N, K]^T with tcgen05 on CTA pairs; A and B come in through TMA
+// tensor maps (16-bit, 128-byte swizzle, boxes of 64 columns x kGemmBoxRows rows for both).
+constexpr int kGemmBM = 128;       // rows of A per CTA
+constexpr int kGemmBN = 256;       // columns of D per CTA pair (128 rows of B per CTA)
 constexpr int kGemmBK = 64;
+constexpr int kGemmBoxRows = 128;
 
 enum EpiKind : int {
   kEpiStore = 0,     // C = bf16(D)

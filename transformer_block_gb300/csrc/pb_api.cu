@@ -245,7 +245,7 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
 
   // 2. [q | k | v | h] = xn [Wqkv | W1], GeLU(h) in the epilogue
   CUtensorMap tm_xn, tm_act, tm_qk, tm_vt;
-  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, pb::kGemmBM, h->f16);
+  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, pb::kGemmBoxRows, h->f16);
   if (s != PB_OK) return s;
   EpiParams e1{};
   e1.status = h->status;
@@ -295,7 +295,7 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   PB_CUDA(mark(3), "cudaEventRecord");
 
   // 4. y = x + [attn | GeLU(h)] [Wo ; W2] (+ b_o + b2)
-  s = make_map_2d(&tm_act, act, T, H + F, H + F, pb::kGemmBM, h->f16);
+  s = make_map_2d(&tm_act, act, T, H + F, H + F, pb::kGemmBoxRows, h->f16);
   if (s != PB_OK) return s;
   EpiParams e2{};
   e2.status = h->status;
@@ -489,8 +489,8 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
   PB_CUDA_H(cudaMemcpyAsync(h->beta, w->ln_beta, H * 2, cudaMemcpyDeviceToDevice, st),
             "copy beta");
 #undef PB_CUDA_H
-  s = make_map_2d(&h->tm_w1cat, h->w1cat, 3 * H + F, H, H, pb::kGemmBN, h->f16);
-  if (s == PB_OK) s = make_map_2d(&h->tm_w2cat, h->w2cat, H, H + F, H + F, pb::kGemmBN, h->f16);
+  s = make_map_2d(&h->tm_w1cat, h->w1cat, 3 * H + F, H, H, pb::kGemmBoxRows, h->f16);
+  if (s == PB_OK) s = make_map_2d(&h->tm_w2cat, h->w2cat, H, H + F, H + F, pb::kGemmBoxRows, h->f16);
   if (s != PB_OK) return cleanup(s);
   *out = h;
   return PB_OK;
@@ -653,8 +653,8 @@ pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const voi
   PB_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
           "cudaDeviceGetAttribute");
   CUtensorMap ta, tb;
-  pb_status s = make_map_2d(&ta, A, uint64_t(M), uint64_t(K), uint64_t(K), pb::kGemmBM);
-  if (s == PB_OK) s = make_map_2d(&tb, B, uint64_t(N), uint64_t(K), uint64_t(K), pb::kGemmBN);
+  pb_status s = make_map_2d(&ta, A, uint64_t(M), uint64_t(K), uint64_t(K), pb::kGemmBoxRows);
+  if (s == PB_OK) s = make_map_2d(&tb, B, uint64_t(N), uint64_t(K), uint64_t(K), pb::kGemmBoxRows);
   if (s != PB_OK) return s;
   EpiParams ep{};
   ep.c = static_cast<__nv_bfloat16*>(C);
