@@ -103,6 +103,7 @@ typedef struct pb_weights {
  *   act  [T, H + F]      [attention output (before Wo) | GeLU(h)]  (bf16 / fp16)
  *   io   [T, H]          bf16 staging of the host-buffer entry point
  *   res0, res1 [T, H]    fp32 residual stream between the layers of a stack
+ *   sk                   stream-K partial tiles (fp32) and flags of the two GEMMs
  * T = batch * seq. */
 typedef struct pb_scratch_layout {
   size_t xn;
@@ -112,6 +113,7 @@ typedef struct pb_scratch_layout {
   size_t io;
   size_t res0;
   size_t res1;
+  size_t sk;  /* stream-K partial tiles and flags of the GEMMs */
   size_t seq_pad;
   size_t total;
 } pb_scratch_layout;
@@ -213,10 +215,14 @@ pb_status pb_layernorm(int64_t rows, int32_t H, const void* x, const void* gamma
 /* C[M, N] = A[M, K] * B[N, K]^T on the tensor cores (bf16 inputs, fp32 accumulation,
  * bf16 output rounded to nearest even): the contraction of every linear layer of the
  * block with the weight stored K-major. A, B, C 16-byte aligned; K % 64 == 0,
- * N % 32 == 0. `status` (device int, may be NULL) receives PB_ERR_DEVICE_TIMEOUT if a
- * bounded wait runs out. */
+ * N % 32 == 0. `scratch` (device, 256-byte aligned, >= pb_gemm_scratch_bytes, or NULL)
+ * lets the last waves of tiles be split along K across the SMs (stream-K); with NULL every
+ * tile is computed whole. Calls that share a scratch buffer must not overlap on the GPU.
+ * `status` (device int, may be NULL) receives PB_ERR_DEVICE_TIMEOUT if a bounded wait
+ * runs out. */
+pb_status pb_gemm_scratch_bytes(size_t* bytes);
 pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const void* B, void* C,
-                       int* status, void* stream);
+                       void* scratch, size_t scratch_bytes, int* status, void* stream);
 
 /* Sliding-window causal attention alone (section 1.1, eqs. (5)-(6)) from the scratch
  * layout's qk and vt buffers into columns [0, H) of `act` ([T, act_ld] bf16). */

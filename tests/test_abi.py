@@ -71,13 +71,14 @@ def test_workspace_and_scratch_sizes(lib):
     L = pb.scratch_layout(d)
     assert L.seq_pad == 128
     assert L.total == pb.scratch_bytes(d)
-    order = ["xn", "qk", "vt", "act", "io", "res0", "res1"]
+    order = ["xn", "qk", "vt", "act", "io", "res0", "res1", "sk"]
     for a, b in zip(order, order[1:]):
         assert getattr(L, a) < getattr(L, b) and getattr(L, b) % 1024 == 0
     assert L.act - L.vt >= 2 * 1 * H * 128
     assert L.res0 - L.io >= 2 * T * H
     assert L.res1 - L.res0 >= 4 * T * H          # fp32 residual stream
-    assert L.total - L.res1 >= 4 * T * H
+    assert L.sk - L.res1 >= 4 * T * H
+    assert L.total - L.sk >= pb.gemm_scratch_bytes()
     # ragged sequences pad the transposed V to a multiple of 8 tokens
     assert pb.scratch_layout(dims(seq=130)).seq_pad == 136
 
@@ -124,7 +125,9 @@ def test_null_handles(lib):
 
 
 def test_step_entry_points_validate(lib):
-    assert lib.pb_gemm_bf16(128, 100, 64, None, None, None, None, None) == 2  # N % 32
-    assert lib.pb_gemm_bf16(128, 128, 64, None, None, None, None, None) == 1  # NULL
+    assert lib.pb_gemm_bf16(128, 100, 64, None, None, None, None, 0, None, None) == 2  # N % 32
+    assert lib.pb_gemm_bf16(128, 128, 64, None, None, None, None, 0, None, None) == 1  # NULL
+    n = ctypes.c_size_t()
+    assert lib.pb_gemm_scratch_bytes(ctypes.byref(n)) == 0 and n.value > 0
     assert lib.pb_layernorm(4, 12, None, None, None, 1e-5, None, None) == 2   # H % 8
     assert lib.pb_layernorm(4, 16, None, None, None, 1e-5, None, None) == 1   # NULL

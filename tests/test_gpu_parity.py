@@ -45,6 +45,30 @@ def test_gemm_matches_oracle(M, N, K):
     assert_parity(host(c), ref, f"gemm {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(2048, 12288, 1024), (4160, 2080, 512), (256 * 77, 256, 640)])
+def test_gemm_stream_k_matches_oracle(M, N, K):
+    # Tile counts that leave a partial last wave on 76 CTA pairs, so the last waves are
+    # split along K (stream-K) when scratch is given; without scratch every tile is whole.
+    g = torch.Generator(device="cuda").manual_seed(M + N + K)
+    a = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(pb.gemm_scratch_bytes(), dtype=torch.uint8, device="cuda")
+    c_sk = pb.gemm(a, b, scratch=scratch, status=status)
+    c_sk2 = pb.gemm(a, b, scratch=scratch, status=status)  # flags from the previous call
+    c_dp = pb.gemm(a, b, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = torch.randperm(M, generator=torch.Generator().manual_seed(1))[:256].sort().values
+    ref = O.linear(host(a)[rows.numpy()], host(b).T)
+    assert_parity(host(c_sk)[rows.numpy()], ref, f"stream-K gemm {M}x{N}x{K}")
+    assert_parity(host(c_dp)[rows.numpy()], ref, f"whole-tile gemm {M}x{N}x{K}")
+    assert torch.equal(c_sk, c_sk2)
+    # the split changes the fp32 summation order, so some rounded outputs differ: the
+    # stream-K path really ran
+    assert not torch.equal(c_sk, c_dp)
+
+
 @pytest.mark.parametrize("rows,H", [(37, 256), (5, 2048), (3, 12288), (64, 16384)])
 def test_layernorm_matches_oracle(rows, H):
     g = torch.Generator(device="cuda").manual_seed(rows + H)

@@ -19,6 +19,10 @@
 // MMA completion is multicast to both CTAs' barriers. Pair tiles are handed out
 // round-robin over the clusters, M fastest, so clusters running at the same time share
 // B tiles in L2.
+#include <atomic>
+#include <chrono>
+#include <random>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -71,12 +75,8 @@ __device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]
 
 // Epilogue of 32 consecutive columns [col0, col0 + 32) of one output row.
 template <int KIND>
-__device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col0,
-                                           const uint32_t (&r)[32]) {
+__device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col0, float (&v)[32]) {
   if (row >= ep.M) return;
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
   if (KIND != kEpiStore && ep.bias != nullptr) {
     const float4* b4 = reinterpret_cast<const float4*>(ep.bias + col0);
 #pragma unroll
@@ -151,10 +151,62 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
   }
 }
 
+// The work of one CTA pair: first whole tiles t = cluster, cluster + clusters, ... below
+// dp_tiles, then its contiguous share [cluster * W, (cluster + 1) * W) of the linearised
+// (tile, k-block) iterations of the sk_tiles stream-K tiles that follow them.
+struct Sched {
+  int num_m, num_kb;
+  int cluster, clusters;
+  int dp_tiles, sk_tiles, W;
+};
+
+struct SkParams {
+  int dp_tiles, sk_tiles, W;
+  float* partials;  // [kSkMaxClusters][2][128][256]
+  uint64_t* flags;  // [kSkMaxClusters][2][4]
+  uint64_t epoch;
+};
+
+struct Unit {
+  int tile, kb0, kb1;
+};
+
+struct UnitIter {
+  int t;
+  int64_t it, it_end;
+  __device__ explicit UnitIter(const Sched& s)
+      : t(s.cluster),
+        it(int64_t(s.cluster) * s.W),
+        it_end(min(int64_t(s.cluster + 1) * s.W, int64_t(s.sk_tiles) * s.num_kb)) {}
+  __device__ bool next(const Sched& s, Unit& u) {
+    if (t < s.dp_tiles) {
+      u = Unit{t, 0, s.num_kb};
+      t += s.clusters;
+      return true;
+    }
+    if (it >= it_end) return false;
+    const int ts = int(it / s.num_kb);
+    const int kb0 = int(it - int64_t(ts) * s.num_kb);
+    const int kb1 = int(min(int64_t(s.num_kb), int64_t(kb0) + (it_end - it)));
+    u = Unit{s.dp_tiles + ts, kb0, kb1};
+    it += kb1 - kb0;
+    return true;
+  }
+};
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 template <int KIND, bool F16>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                int K, const EpiParams ep, int* status, uint64_t limit_ns) {
+                int K, const EpiParams ep, const SkParams sk, int* status, uint64_t limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,11 +255,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   // wait limit, so shared and tensor memory are never released under them.
   const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
 
-  const int num_m = (ep.M + PM - 1) / PM;
-  const int num_n = (ep.N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
-  const int num_kb = K / BK;
-  const int cluster = int(blockIdx.x) >> 1, num_clusters = int(gridDim.x) >> 1;
+  Sched sc;
+  sc.num_m = (ep.M + PM - 1) / PM;
+  sc.num_kb = K / BK;
+  sc.cluster = int(blockIdx.x) >> 1;
+  sc.clusters = int(gridDim.x) >> 1;
+  sc.dp_tiles = sk.dp_tiles;
+  sc.sk_tiles = sk.sk_tiles;
+  sc.W = sk.W;
+  const int num_m = sc.num_m;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -217,10 +273,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
-        const int m0 = (t % num_m) * PM + int(rank) * BM;
-        const int n0 = (t / num_m) * BN + int(rank) * (BN / 2);
-        for (int kb = 0; kb < num_kb; ++kb) {
+      UnitIter ui(sc);
+      Unit u;
+      while (ok && ui.next(sc, u)) {
+        const int m0 = (u.tile % num_m) * PM + int(rank) * BM;
+        const int n0 = (u.tile / num_m) * BN + int(rank) * (BN / 2);
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, wc, 1)) {
             ok = false;
             break;
@@ -250,11 +308,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       int acc = 0;
       uint32_t acc_par = 0;
       bool ok = true;
-      for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+      UnitIter ui(sc);
+      Unit u;
+      while (ok && ui.next(sc, u)) {
         if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1, wc, 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, wc, 3) ||
               !mbar_wait(peer0 + 8 * stage, phase, wc, 5)) {
             ok = false;
@@ -266,7 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_f16kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+            mma_f16kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb > u.kb0) || k > 0);
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
             stage = 0;
@@ -287,8 +347,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
-        for (int kb = 0; kb < num_kb; ++kb) {
+      UnitIter ui(sc);
+      Unit u;
+      while (ok && ui.next(sc, u)) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, wc, 6)) {
             ok = false;
             break;
@@ -307,20 +369,89 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t quad = warp & 3;
     int acc = 0;
     uint32_t acc_par = 0;
-    for (int t = cluster; t < num_tiles; t += num_clusters) {
+    UnitIter ui(sc);
+    Unit u;
+    bool ok = true;
+    while (ok && ui.next(sc, u)) {
       if (!mbar_wait_warp(tfull0 + 8 * acc, acc_par, wc, 4)) break;
       tc_fence_after();
-      const int m0 = (t % num_m) * PM + int(rank) * BM, n0 = (t / num_m) * BN;
+      const int m0 = (u.tile % num_m) * PM + int(rank) * BM, n0 = (u.tile / num_m) * BN;
       const int row = m0 + int(quad * 32 + lane);
       const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + uint32_t(acc * BN);
+      // This thread's row of a pair's partial tile ([2][128][256] fp32 per cluster).
+      const size_t part_off = (size_t(rank) * 128 + quad * 32 + lane) * BN;
+      if (u.kb0 > 0) {
+        // A K segment that does not start at 0: leave the partial sums for the pair that
+        // owns k-block 0 of this tile, then publish them (one flag per warp).
+        float* dst = sk.partials + size_t(sc.cluster) * (2 * 128 * BN) + part_off;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = n0 + c * 32;
-        if (col0 >= ep.N) break;
-        uint32_t r[32];
-        tmem_ld32(taddr + uint32_t(c * 32), r);
-        tmem_ld_wait(r);
-        epilogue32<KIND>(ep, row, col0, r);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + uint32_t(c * 32), r);
+          tmem_ld_wait(r);
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            __stcg(d4 + q, make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                       __uint_as_float(r[4 * q + 2]),
+                                       __uint_as_float(r[4 * q + 3])));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          st_release_u64(sk.flags + (size_t(sc.cluster) * 2 + rank) * 4 + quad, sk.epoch);
+      } else {
+        // K segment from 0: this pair finishes the tile. For a stream-K tile, the pairs
+        // cluster+1 .. last computed its other K segments; wait for their partials.
+        int last = sc.cluster;
+        if (u.tile >= sc.dp_tiles) {
+          const int64_t ts = u.tile - sc.dp_tiles;
+          last = int(((ts + 1) * sc.num_kb - 1) / sc.W);
+        }
+        for (int c2 = sc.cluster + 1; ok && c2 <= last; ++c2) {
+          const uint64_t* f = sk.flags + (size_t(c2) * 2 + rank) * 4 + quad;
+          if (ld_acquire_u64(f) != sk.epoch) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_u64(f) != sk.epoch) {
+              __nanosleep(100);
+              if (*abort_flag) {
+                ok = false;
+                break;
+              }
+              if (globaltimer_ns() - t0 > limit_ns) {
+                wait_give_up(wc, 7);
+                ok = false;
+                break;
+              }
+            }
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col0 = n0 + c * 32;
+          if (col0 >= ep.N) break;
+          uint32_t r[32];
+          tmem_ld32(taddr + uint32_t(c * 32), r);
+          tmem_ld_wait(r);
+          if (!ok) continue;
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          for (int c2 = sc.cluster + 1; c2 <= last; ++c2) {
+            const float4* p4 = reinterpret_cast<const float4*>(
+                sk.partials + size_t(c2) * (2 * 128 * BN) + part_off + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 pv = __ldcg(p4 + q);
+              v[4 * q] += pv.x;
+              v[4 * q + 1] += pv.y;
+              v[4 * q + 2] += pv.z;
+              v[4 * q + 3] += pv.w;
+            }
+          }
+          epilogue32<KIND>(ep, row, col0, v);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -344,27 +475,38 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Process-wide launch counter for the stream-K flags, seeded so that a stale flag left in
+// a reused buffer by an earlier process is not taken for this launch's.
+uint64_t next_epoch() {
+  static std::atomic<uint64_t> counter{
+      (uint64_t(std::random_device{}()) << 32) ^
+      uint64_t(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+      0x9E3779B97F4A7C15ull};
+  uint64_t e = ++counter;
+  return e == 0 ? ++counter : e;
+}
+
 template <int KIND, bool F16>
 cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
-                        cudaStream_t stream) {
+                        void* sk_scratch, cudaStream_t stream) {
   static int max_clusters = -1;
   static cudaError_t attr_err = cudaSuccess;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
   if (max_clusters < 0) {
     attr_err = cudaFuncSetAttribute(gemm_kernel<KIND, F16>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
     if (attr_err == cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = 2;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-      cfg.blockDim = dim3(THREADS, 1, 1);
-      cfg.dynamicSmemBytes = SMEM_BYTES;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
       int n = 0;
       attr_err = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, F16>, &cfg);
       max_clusters = (attr_err == cudaSuccess && n > 0) ? n : 0;
@@ -374,22 +516,29 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
   const int tiles = ((M + PM - 1) / PM) * ((N + BN - 1) / BN);
   const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  const int num_kb = K / BK;
+  // Stream-K for the last waves when they would leave pairs idle: every full wave but one
+  // runs whole tiles; the remaining (clusters + rem) tiles are split evenly along K.
+  SkParams sk{};
+  sk.dp_tiles = tiles;
+  const int rem = tiles % clusters;
+  if (sk_scratch != nullptr && clusters <= kSkMaxClusters && tiles > clusters && rem != 0 &&
+      num_kb >= 8) {
+    sk.sk_tiles = clusters + rem;
+    sk.dp_tiles = tiles - sk.sk_tiles;
+    const int64_t iters = int64_t(sk.sk_tiles) * num_kb;
+    sk.W = int((iters + clusters - 1) / clusters);
+    sk.partials = static_cast<float*>(sk_scratch);
+    sk.flags = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(sk_scratch) +
+                                           size_t(kSkMaxClusters) * kSkPartialBytes);
+    sk.epoch = next_epoch();
+  }
   EpiParams e = ep;
   e.M = M;
   e.N = N;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, F16>, tmA, tmB, K, e, status, limit_ns);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, F16>, tmA, tmB, K, e, sk, status, limit_ns);
 }
 
 }  // namespace
@@ -417,13 +566,13 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, int* status, cudaStream_t strea
 
 cudaError_t launch_gemm(EpiKind kind, bool ab_f16, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         int M, int N, int K, const EpiParams& ep, int num_sms, int* status,
-                        uint64_t limit_ns, cudaStream_t stream) {
+                        uint64_t limit_ns, void* sk_scratch, cudaStream_t stream) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
-#define PB_GEMM_CASE(KIND_)                                                                 \
-  return ab_f16 ? launch_kind<KIND_, true>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, \
-                                           stream)                                           \
+#define PB_GEMM_CASE(KIND_)                                                                  \
+  return ab_f16 ? launch_kind<KIND_, true>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,  \
+                                           sk_scratch, stream)                                \
                 : launch_kind<KIND_, false>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, \
-                                            stream)
+                                            sk_scratch, stream)
   switch (kind) {
     case kEpiStore:
       PB_GEMM_CASE(kEpiStore);

@@ -53,11 +53,20 @@ struct EpiParams {
   bool y_f32;
 };
 
+// Stream-K work space: the tiles of the last waves are split along K across all CTA
+// pairs; a pair whose K segment does not start at 0 leaves its fp32 partial tile here and
+// publishes it with a per-warp flag (the launch's epoch value).
+constexpr int kSkMaxClusters = 96;
+constexpr size_t kSkPartialBytes = size_t(2) * 128 * 256 * 4;  // one pair tile, fp32
+constexpr size_t kSkFlagBytes = size_t(2) * 4 * 8;             // 2 CTAs x 4 warps x u64
+constexpr size_t kSkScratchBytes = size_t(kSkMaxClusters) * (kSkPartialBytes + kSkFlagBytes);
+
 size_t gemm_smem_bytes();
-// ab_f16: A and B are fp16 (else bf16).
+// ab_f16: A and B are fp16 (else bf16). sk_scratch (kSkScratchBytes, 256-byte aligned) may
+// be null: then every tile is computed whole by one CTA pair.
 cudaError_t launch_gemm(EpiKind kind, bool ab_f16, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         int M, int N, int K, const EpiParams& ep, int num_sms, int* status,
-                        uint64_t limit_ns, cudaStream_t stream);
+                        uint64_t limit_ns, void* sk_scratch, cudaStream_t stream);
 
 // ---------------------------------------------------------------- attention (swa.cu)
 struct SwaParams {

@@ -144,6 +144,8 @@ pb_scratch_layout scratch_layout(const pb_dims& d) {
   off = align_up(off + T * H * 4, 1024);
   L.res1 = off;
   off = align_up(off + T * H * 4, 1024);
+  L.sk = off;
+  off = align_up(off + pb::kSkScratchBytes, 1024);
   L.total = off;
   return L;
 }
@@ -261,7 +263,7 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   e1.act_f16 = h->f16;
   e1.bias = h->has_bias ? h->bias1 : nullptr;
   PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, h->tm_w1cat, T, 3 * H + F, H, e1,
-                          h->num_sms, h->status, h->limit_ns, st),
+                          h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
           "first GEMM launch");
   PB_CUDA(mark(2), "cudaEventRecord");
 
@@ -305,7 +307,7 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   e2.y = y;
   e2.y_f32 = y_f32;
   PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->f16, tm_act, h->tm_w2cat, T, H, H + F, e2,
-                          h->num_sms, h->status, h->limit_ns, st),
+                          h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
           "second GEMM launch");
   PB_CUDA(mark(4), "cudaEventRecord");
   return PB_OK;
@@ -640,14 +642,23 @@ pb_status pb_layernorm(int64_t rows, int32_t H, const void* x, const void* gamma
   return PB_OK;
 }
 
+pb_status pb_gemm_scratch_bytes(size_t* bytes) {
+  if (bytes == nullptr) return fail(PB_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = pb::kSkScratchBytes;
+  return PB_OK;
+}
+
 pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const void* B, void* C,
-                       int* status, void* stream) {
+                       void* scratch, size_t scratch_bytes, int* status, void* stream) {
   if (M < 1 || N < 1 || K < 1) return fail(PB_ERR_INVALID_ARG, "M, N, K must be >= 1");
   if (K % 64 != 0 || N % 32 != 0)
     return fail(PB_ERR_UNSUPPORTED, "gemm needs K %% 64 == 0 and N %% 32 == 0");
   if (A == nullptr || B == nullptr || C == nullptr || !aligned(A, 16) || !aligned(B, 16) ||
       !aligned(C, 16))
     return fail(PB_ERR_INVALID_ARG, "A, B, C must be 16-byte aligned device pointers");
+  if (scratch != nullptr && (!aligned(scratch, 256) || scratch_bytes < pb::kSkScratchBytes))
+    return fail(PB_ERR_WORKSPACE, "scratch must be NULL or 256-byte aligned with >= %zu bytes",
+                pb::kSkScratchBytes);
   int dev = -1, sms = 0;
   PB_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   PB_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
@@ -660,7 +671,7 @@ pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const voi
   ep.c = static_cast<__nv_bfloat16*>(C);
   ep.ldc = N;
   PB_CUDA(pb::launch_gemm(pb::kEpiStore, false, ta, tb, M, N, K, ep, sms, status, kDefaultLimitNs,
-                          static_cast<cudaStream_t>(stream)),
+                          scratch, static_cast<cudaStream_t>(stream)),
           "gemm launch");
   return PB_OK;
 }

@@ -45,7 +45,7 @@ class pb_weights(ctypes.Structure):
 
 class pb_scratch_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("xn", "qk", "vt", "act", "io", "res0", "res1", "seq_pad", "total")]
+                ("xn", "qk", "vt", "act", "io", "res0", "res1", "sk", "seq_pad", "total")]
 
 
 class pb_options(ctypes.Structure):
@@ -76,7 +76,8 @@ SIGNATURES = {
     "pb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pb_last_error_message": (ctypes.c_char_p, []),
     "pb_layernorm": (ctypes.c_int, [_I64, _I32, _P, _P, _P, ctypes.c_float, _P, _P]),
-    "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "pb_gemm_scratch_bytes": (ctypes.c_int, [ctypes.POINTER(_S)]),
+    "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _S, _P, _P]),
     "pb_swa_attention": (ctypes.c_int, [_DP, _P, _P, _P, _I64, _P, _P]),
     "pb_wait_probe": (ctypes.c_int, [_U64, _P, _P]),
 }
@@ -268,14 +269,22 @@ def layernorm(x, gamma, beta, eps=1e-5, out=None, stream=None):
     return out
 
 
-def gemm(a, b, out=None, status=None, stream=None):
-    """``a [M, K] @ b[N, K]^T`` -> bf16 ``[M, N]`` on the tensor cores."""
+def gemm_scratch_bytes() -> int:
+    n = ctypes.c_size_t()
+    _check("pb_gemm_scratch_bytes", lib().pb_gemm_scratch_bytes(ctypes.byref(n)))
+    return n.value
+
+
+def gemm(a, b, out=None, scratch=None, status=None, stream=None):
+    """``a [M, K] @ b[N, K]^T`` -> bf16 ``[M, N]`` on the tensor cores; ``scratch`` (a uint8
+    CUDA tensor of ``gemm_scratch_bytes()``) enables stream-K for the last waves."""
     M, K = a.shape
     N = b.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
-    _check("pb_gemm_bf16", lib().pb_gemm_bf16(M, N, K, _ptr(a), _ptr(b), _ptr(out),
-                                              _ptr(status), _stream(stream)))
+    nbytes = 0 if scratch is None else scratch.numel()
+    _check("pb_gemm_bf16", lib().pb_gemm_bf16(M, N, K, _ptr(a), _ptr(b), _ptr(out), _ptr(scratch),
+                                              nbytes, _ptr(status), _stream(stream)))
     return out
 
 
