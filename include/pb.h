@@ -224,6 +224,20 @@ pb_status pb_gemm_scratch_bytes(size_t* bytes);
 pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const void* B, void* C,
                        void* scratch, size_t scratch_bytes, int* status, void* stream);
 
+/* pb_gemm_bf16 for callers that cannot allocate device memory: those capturing a CUDA
+ * graph (cudaMalloc is not allowed during capture), plugins whose device memory belongs
+ * to a host engine's allocator, and paths where an allocation could block. The pages have
+ * no counterpart; it is a convenience of this library. It computes the same product with
+ * the same stream-K schedule, with the scratch in a fixed array of the library's device
+ * memory (25,171,968 bytes per GPU, held until the process exits) instead of a caller
+ * buffer. It allocates nothing. Limits: GPUs with at most 192 SMs (96 CTA pairs);
+ * otherwise PB_ERR_UNSUPPORTED. The first call on each device looks up the array's
+ * address (cudaGetSymbolAddress); make that first call before any stream capture. All
+ * calls share the one array: calls that can overlap on the GPU (other streams, other
+ * host threads) race on it and must be serialised by the caller. */
+pb_status pb_gemm_bf16_static(int32_t M, int32_t N, int32_t K, const void* A, const void* B,
+                              void* C, int* status, void* stream);
+
 /* Sliding-window causal attention alone (section 1.1, eqs. (5)-(6)) from the scratch
  * layout's qk and vt buffers into columns [0, H) of `act` ([T, act_ld] bf16). */
 pb_status pb_swa_attention(const pb_dims* dims, const void* qk, const void* vt, void* act,

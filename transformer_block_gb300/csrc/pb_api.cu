@@ -358,6 +358,11 @@ pb_status run_stack(pb_handle* const* layers, int32_t n, const void* x, void* y,
 
 }  // namespace
 
+namespace pb {
+// Records a failure of an entry point defined in another file of the library.
+pb_status record_error(pb_status s, const char* message) { return fail(s, "%s", message); }
+}  // namespace pb
+
 extern "C" {
 
 const char* pb_status_string(pb_status s) {

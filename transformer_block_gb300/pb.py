@@ -80,6 +80,7 @@ SIGNATURES = {
     "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _S, _P, _P]),
     "pb_swa_attention": (ctypes.c_int, [_DP, _P, _P, _P, _I64, _P, _P]),
     "pb_wait_probe": (ctypes.c_int, [_U64, _P, _P]),
+    "pb_gemm_bf16_static": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -285,6 +286,18 @@ def gemm(a, b, out=None, scratch=None, status=None, stream=None):
     nbytes = 0 if scratch is None else scratch.numel()
     _check("pb_gemm_bf16", lib().pb_gemm_bf16(M, N, K, _ptr(a), _ptr(b), _ptr(out), _ptr(scratch),
                                               nbytes, _ptr(status), _stream(stream)))
+    return out
+
+
+def gemm_static(a, b, out=None, status=None, stream=None):
+    """``gemm`` without caller scratch: the stream-K partial tiles live in the library's
+    own fixed device array (for callers that cannot allocate; calls must not overlap)."""
+    M, K = a.shape
+    N = b.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _check("pb_gemm_bf16_static", lib().pb_gemm_bf16_static(M, N, K, _ptr(a), _ptr(b), _ptr(out),
+                                                            _ptr(status), _stream(stream)))
     return out
 
 
