@@ -6,21 +6,27 @@
 // token attends to the most recent w tokens; the FlashAttention tiling of section 1.3
 // keeps the score matrix on chip, so it never reaches HBM).
 //
-// One CTA per (query tile of 128 rows, head, sequence). Only the key tiles that meet
-// the window [i - w + 1, i] of some query of the tile are visited, and only tiles that
-// cross the diagonal or the window's far edge are masked element by element.
-//   warp 0     TMA producer: the Q tile once, then K and V^T tiles in a 2-stage ring
-//   warp 1     TMEM owner and the single MMA-issuing thread:
-//                S_j = Q K_j^T  -> tensor memory (two S buffers, so S_{j+1} is computed
-//                                  while the softmax works on S_j)
-//                O  += P_j V_j  -> tensor memory (P_j read from shared memory)
-//   warps 2-5  softmax, one query row per thread (the thread's TMEM lane): online
-//              max / sum in fp32 with exp2 (the 1/sqrt(dh) and log2(e) factors folded
-//              into one multiplier), P rounded to bf16 into shared memory, the running
-//              output rescaled in tensor memory when the row maximum grows, and the
-//              final O / l written as bf16.
-// V arrives transposed ([dh, keys] per head, written so by the first GEMM's epilogue),
-// so both products read K-major operands.
+// One CTA per (pair of 128-query tiles, head, sequence): both query tiles share every
+// K/V tile the CTA loads. Only key tiles that meet the window of some query of the pair
+// are visited; a key tile one query tile does not need is skipped for that tile (no MMA,
+// no softmax), and only tiles that cross the diagonal or the window's far edge are masked
+// element by element.
+//   warp 0     TMA producer: both query tiles once, then K and V^T tiles, 2-stage ring
+//   warp 1     tensor-memory owner and the single MMA-issuing thread, in the order
+//                S0 = Q0 K_j^T, S1 = Q1 K_j^T, then per tile h: O_h += P_h V_j followed
+//                by S_h = Q_h K_{j+1}^T
+//              so the tensor cores work on one query tile while the other's softmax runs
+//   warps 2-5  softmax of query tile 0, one row per thread (the thread's TMEM lane)
+//   warps 6-9  softmax of query tile 1
+// Tensor memory: S0 | S1 | O0 | O1 (128 columns each). The softmax writes P (bf16) over
+// the first 64 columns of its own S, and the PV product reads it from there (A operand in
+// tensor memory); the tensor pipe executes one thread's MMAs in issue order, so the next
+// S_h overwrites P_h only after O_h += P_h V has read it.
+// Online softmax in fp32 with exp2 (1/sqrt(dh) and log2(e) folded into one multiplier);
+// the output is rescaled only when a row maximum grows by more than 2^8, and the final
+// O / l uses the same reference maximum as every P, so the result is unchanged up to
+// rounding. V arrives transposed ([dh, keys] per head, written so by the first GEMM's
+// epilogue), so the PV product reads a K-major operand.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -28,24 +34,23 @@ namespace pb {
 namespace {
 
 constexpr int BQ = kSwaBQ, BKV = kSwaBKV;
-constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;  // S0 [0,128) | S1 [128,256) | O [256, 256+dh)
-constexpr int BOX = 128 * 64 * 2;    // one 128-row x 64-column bf16 box: 16 KB
+constexpr int THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BOX = 128 * 64 * 2;          // one 128-row x 64-column 16-bit box: 16 KB
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int DH>
 struct Layout {
-  static constexpr int Q_BYTES = BQ * DH * 2;
+  static constexpr int Q_TILE = BQ * DH * 2;
   static constexpr int K_BYTES = BKV * DH * 2;
   static constexpr int VHALF = DH * 64 * 2;  // V^T box: DH rows x 64 keys
   static constexpr int V_BYTES = 2 * VHALF;
-  static constexpr int P_BYTES = BQ * BKV * 2;
-  static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = Q_OFF + Q_BYTES;
   static constexpr int STAGE = K_BYTES + V_BYTES;
-  static constexpr int P_OFF = KV_OFF + 2 * STAGE;
-  static constexpr int BAR_OFF = P_OFF + P_BYTES;
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = 2 * Q_TILE;
+  static constexpr int BAR_OFF = KV_OFF + 2 * STAGE;
   static constexpr int NUM_BARS = 12;
-  // Request enough shared memory that only one CTA fits per SM: the CTA takes all 512
+  // Enough shared memory that only one CTA fits per SM: the CTA takes all 512
   // tensor-memory columns.
   static constexpr size_t SMEM = 200 * 1024;
   static_assert(BAR_OFF + NUM_BARS * 8 + 16 + 1024 <= SMEM, "shared memory layout");
@@ -63,24 +68,36 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t q_full = smem_u32(bars + 0);
   const uint32_t kv_full0 = smem_u32(bars + 1);   // [2]
   const uint32_t kv_empty0 = smem_u32(bars + 3);  // [2]
-  const uint32_t s_full0 = smem_u32(bars + 5);    // [2]
-  const uint32_t s_free0 = smem_u32(bars + 7);    // [2]
-  const uint32_t p_full = smem_u32(bars + 9);
-  const uint32_t o_ready = smem_u32(bars + 10);
+  const uint32_t s_full0 = smem_u32(bars + 5);    // [2] per query tile
+  const uint32_t p_full0 = smem_u32(bars + 7);    // [2] per query tile (4 warps each)
+  const uint32_t o_final0 = smem_u32(bars + 9);   // [2] per query tile: last PV done
   const uint32_t drain_bar = smem_u32(bars + 11);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  // Heaviest query tiles first: with a window >= seq the last tiles see the most keys.
+  // Heaviest query pairs first: with a window >= seq the last pairs see the most keys.
   const int nbh = p.nh * p.B;
-  const int q_tile = p.num_q_tiles - 1 - int(blockIdx.x) / nbh;
+  const int num_pairs = (p.num_q_tiles + 1) / 2;
+  const int pair = num_pairs - 1 - int(blockIdx.x) / nbh;
   const int head = int(blockIdx.x) % p.nh;
   const int b = (int(blockIdx.x) % nbh) / p.nh;
-  const int q0 = q_tile * BQ;
-  const int q_hi = min(q0 + BQ - 1, p.S - 1);
-  const int k_lo = max(0, q0 - p.window + 1);
-  const int kt_begin = k_lo / BKV;
-  const int nkv = q_hi / BKV - kt_begin + 1;
+  const int q0 = pair * 2 * BQ;
+  // Key-tile range [kb, ke] of each query tile h (rows q0 + 128h ..); empty past seq.
+  int kb[2], ke[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int qb = q0 + h * BQ;
+    if (qb < p.S) {
+      kb[h] = max(0, qb - p.window + 1) / BKV;
+      ke[h] = min(qb + BQ - 1, p.S - 1) / BKV;
+    } else {
+      kb[h] = 1;
+      ke[h] = 0;
+    }
+  }
+  const int kt_begin = kb[0];
+  const int kt_end = max(ke[0], ke[1]);
+  const int U = kt_end - kt_begin + 1;  // key tiles the pair visits
 
   if (cta_should_skip(status)) return;
   const uint32_t warp = warp_id(), lane = lane_id();
@@ -90,10 +107,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(kv_full0 + 8 * s, 1);
       mbar_init(kv_empty0 + 8 * s, 1);
       mbar_init(s_full0 + 8 * s, 1);
-      mbar_init(s_free0 + 8 * s, 4);
+      mbar_init(p_full0 + 8 * s, 4);
+      mbar_init(o_final0 + 8 * s, 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_ready, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -116,25 +132,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
   const uint32_t sQ = smem_u32(smem + L::Q_OFF);
   const uint32_t sKV = smem_u32(smem + L::KV_OFF);
-  const uint32_t sP = smem_u32(smem + L::P_OFF);
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
       uint32_t last_par[2] = {0, 0};
       uint32_t used = 0;
-      mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+      mbar_arrive_expect_tx(q_full, 2 * L::Q_TILE);
 #pragma unroll
-      for (int hb = 0; hb < DH / 64; ++hb)
-        tma_load_3d(sQ + hb * BOX, &tmQK, q_full, head * DH + hb * 64, q0, b);
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int hb = 0; hb < DH / 64; ++hb)
+          tma_load_3d(sQ + h * L::Q_TILE + hb * BOX, &tmQK, q_full, head * DH + hb * 64,
+                      q0 + h * BQ, b);
       const int vt_row = (b * p.nh + head) * DH;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t par = (j >> 1) & 1;
+      for (int idx = 0; idx < U; ++idx) {
+        const int st = idx & 1;
+        const uint32_t par = (idx >> 1) & 1;
         if (!mbar_wait(kv_empty0 + 8 * st, par ^ 1, wc, 11)) break;
         const uint32_t base = sKV + st * L::STAGE;
-        const int k0 = (kt_begin + j) * BKV;
-        mbar_arrive_expect_tx(kv_full0 + 8 * st, L::K_BYTES + L::V_BYTES);
+        const int k0 = (kt_begin + idx) * BKV;
+        mbar_arrive_expect_tx(kv_full0 + 8 * st, L::STAGE);
 #pragma unroll
         for (int hb = 0; hb < DH / 64; ++hb)
           tma_load_3d(base + hb * BOX, &tmQK, kv_full0 + 8 * st, p.H + head * DH + hb * 64, k0,
@@ -155,145 +173,157 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ---------------------------------------------------------------- MMA issuer
       const uint32_t id_s = idesc_bf16_f32(BQ, BKV);
       const uint32_t id_o = idesc_bf16_f32(BQ, DH);
-      const uint32_t t_o = tmem_base + 256;
-      bool ok = mbar_wait(q_full, 0, wc, 12);
-      // O += P_i V_i, once P_i is in shared memory.
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(p_full, i & 1, wc, 13)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sKV + (i & 1) * L::STAGE + L::K_BYTES;
+      bool first_pv[2] = {true, true};
+      // S_h = Q_h K^T for union key tile idx (nothing if query tile h does not need it).
+      auto issue_s = [&](int h, int idx) {
+        const int j = kt_begin + idx;
+        if (j >= kb[h] && j <= ke[h]) {
+          const uint32_t kbase = sKV + (idx & 1) * L::STAGE;
+          const uint32_t qbase = sQ + h * L::Q_TILE;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint64_t da = sdesc_kmajor_sw128(sP + (kk >> 2) * BOX) + 2 * (kk & 3);
-          const uint64_t db = sdesc_kmajor_sw128(vbase + (kk >> 2) * L::VHALF) + 2 * (kk & 3);
-          mma_f16kind_ss(t_o, da, db, id_o, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint64_t da = sdesc_kmajor_sw128(qbase + (kk >> 2) * BOX) + 2 * (kk & 3);
+            const uint64_t db = sdesc_kmajor_sw128(kbase + (kk >> 2) * BOX) + 2 * (kk & 3);
+            mma_f16kind_ss(tmem_base + uint32_t(h * BKV), da, db, id_s, kk > 0 ? 1u : 0u);
+          }
         }
-        mma_commit(kv_empty0 + 8 * (i & 1));
-        mma_commit(o_ready);
-        return true;
+        mma_commit(s_full0 + 8 * h);
       };
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t par = (j >> 1) & 1;
-        if (!mbar_wait(kv_full0 + 8 * st, par, wc, 14)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(s_free0 + 8 * st, par ^ 1, wc, 15)) {
-          ok = false;
-          break;
-        }
+      bool ok = mbar_wait(q_full, 0, wc, 12) && mbar_wait(kv_full0, 0, wc, 14);
+      if (ok) {
         tc_fence_after();
-        const uint32_t kbase = sKV + st * L::STAGE;
-        const uint32_t t_s = tmem_base + uint32_t(st * BKV);
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint64_t da = sdesc_kmajor_sw128(sQ + (kk >> 2) * BOX) + 2 * (kk & 3);
-          const uint64_t db = sdesc_kmajor_sw128(kbase + (kk >> 2) * BOX) + 2 * (kk & 3);
-          mma_f16kind_ss(t_s, da, db, id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full0 + 8 * st);
-        if (j > 0 && !issue_pv(j - 1)) ok = false;
+        issue_s(0, 0);
+        issue_s(1, 0);
       }
-      if (ok) issue_pv(nkv - 1);
+      for (int idx = 0; ok && idx < U; ++idx) {
+        const int j = kt_begin + idx;
+        const uint32_t vbase = sKV + (idx & 1) * L::STAGE + L::K_BYTES;
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(p_full0 + 8 * h, idx & 1, wc, 13)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (j >= kb[h] && j <= ke[h]) {
+            // O_h += P_h V: P_h (bf16) sits in the first 64 columns of S_h.
+            const uint32_t t_p = tmem_base + uint32_t(h * BKV);
+            const uint32_t t_o = tmem_base + 256u + uint32_t(h * 128);
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk) {
+              const uint64_t db =
+                  sdesc_kmajor_sw128(vbase + (kk >> 2) * L::VHALF) + 2 * (kk & 3);
+              mma_f16kind_ts(t_o, t_p + uint32_t(kk * 8), db, id_o,
+                             (!first_pv[h] || kk > 0) ? 1u : 0u);
+            }
+            first_pv[h] = false;
+          }
+          if (idx + 1 == U) mma_commit(o_final0 + 8 * h);  // completes exactly once
+          if (idx + 1 < U) {
+            if (h == 0 && !mbar_wait(kv_full0 + 8 * ((idx + 1) & 1), ((idx + 1) >> 1) & 1, wc,
+                                     15)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(h, idx + 1);
+          }
+        }
+        if (!ok) break;
+        mma_commit(kv_empty0 + 8 * (idx & 1));
+      }
       mma_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0, drain_ns);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax
+    const int h = (warp >= 6) ? 1 : 0;  // query tile of this warpgroup
     const uint32_t quad = warp & 3;
     const int r = int(quad * 32 + lane);  // query row inside the tile = TMEM lane
-    const int i = q0 + r;                 // query position in the sequence
+    const int qb = q0 + h * BQ;
+    const int i = qb + r;                 // query position in the sequence
     const uint32_t lane_addr = (quad * 32u) << 16;
+    const uint32_t t_s = tmem_base + lane_addr + uint32_t(h * BKV);
+    const uint32_t t_o = tmem_base + lane_addr + 256u + uint32_t(h * 128);
+    const uint32_t s_full = s_full0 + 8 * h, p_full = p_full0 + 8 * h;
     const float c = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      const uint32_t par = (j >> 1) & 1;
-      if (!mbar_wait_warp(s_full0 + 8 * st, par, wc, 16)) {
+    float m_used = -INFINITY, l = 0.f;
+    bool has_o = false, ok = true;
+    for (int idx = 0; idx < U; ++idx) {
+      const int j = kt_begin + idx;
+      if (!mbar_wait_warp(s_full, idx & 1, wc, 16)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[BKV];
+      if (j >= kb[h] && j <= ke[h]) {
+        float s[BKV];
 #pragma unroll
-      for (int ch = 0; ch < BKV / 32; ++ch) {
-        uint32_t u[32];
-        tmem_ld32(tmem_base + lane_addr + uint32_t(st * BKV + ch * 32), u);
-        tmem_ld_wait(u);
+        for (int ch = 0; ch < BKV / 32; ++ch) {
+          uint32_t u[32];
+          tmem_ld32(t_s + uint32_t(ch * 32), u);
+          tmem_ld_wait(u);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(u[e]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free0 + 8 * st);
-
-      const int k0 = (kt_begin + j) * BKV;
-      const bool whole = (k0 + BKV - 1 <= q0) && (q0 + BQ - 1 - k0 < p.window);
-      if (!whole) {
-#pragma unroll
-        for (int e = 0; e < BKV; ++e) {
-          const int d = i - (k0 + e);
-          if (d < 0 || d >= p.window) s[e] = -INFINITY;
+          for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(u[e]);
         }
-      }
-      float mx = m;
+        const int k0 = j * BKV;
+        const bool whole = (k0 + BKV - 1 <= qb) && (qb + BQ - 1 - k0 < p.window);
+        if (!whole) {
 #pragma unroll
-      for (int e = 0; e < BKV; ++e) mx = fmaxf(mx, s[e]);
-      const float ms = (mx == -INFINITY) ? 0.f : mx * c;
-      const float alpha = ex2_approx(m * c - ms);
-      float sum = 0.f;
-#pragma unroll
-      for (int e = 0; e < BKV; ++e) {
-        s[e] = ex2_approx(fmaf(s[e], c, -ms));
-        sum += s[e];
-      }
-      l = l * alpha + sum;
-      m = mx;
-
-      if (j > 0) {
-        // P_{j-1} V_{j-1} has finished: O is stable and the P buffer is free.
-        if (!mbar_wait_warp(o_ready, (j - 1) & 1, wc, 17)) {
-          ok = false;
-          break;
+          for (int e = 0; e < BKV; ++e) {
+            const int d = i - (k0 + e);
+            if (d < 0 || d >= p.window) s[e] = -INFINITY;
+          }
         }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        float mx = -INFINITY;
 #pragma unroll
+        for (int e = 0; e < BKV; ++e) mx = fmaxf(mx, s[e]);
+        const float mxs = mx * c;
+        // Move the reference maximum only when the row maximum grew by more than 2^8
+        // (from -inf, any finite maximum does); O is rescaled below, after P is stored.
+        const bool grow = mxs > m_used + kRescaleThreshold;
+        const float alpha = grow ? ex2_approx(m_used - mxs) : 1.f;
+        if (grow) {
+          l *= alpha;
+          m_used = mxs;
+        }
+        const float m_eff = (m_used == -INFINITY) ? 0.f : m_used;
+        float sum = 0.f;
+        // P_h over the first 64 columns of S_h: column m holds keys 2m (low) and 2m+1;
+        // 32 keys at a time.
+#pragma unroll
+        for (int ch = 0; ch < BKV / 32; ++ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a0 = ex2_approx(fmaf(s[ch * 32 + 2 * e], c, -m_eff));
+            const float a1 = ex2_approx(fmaf(s[ch * 32 + 2 * e + 1], c, -m_eff));
+            sum += a0 + a1;
+            pk[e] = pack_bf16x2(a0, a1);
+          }
+          tmem_st16(t_s + uint32_t(ch * 16), pk);
+        }
+        l += sum;
+        tmem_st_wait();
+        if (has_o && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
           for (int ch = 0; ch < DH / 32; ++ch) {
             uint32_t u[32];
-            const uint32_t ta = tmem_base + lane_addr + 256u + uint32_t(ch * 32);
-            tmem_ld32(ta, u);
+            tmem_ld32(t_o + uint32_t(ch * 32), u);
             tmem_ld_wait(u);
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            tmem_st32(ta, u);
+            tmem_st32(t_o + uint32_t(ch * 32), u);
           }
           tmem_st_wait();
         }
+        has_o = true;
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle the MMA expects.
-      uint8_t* prow = smem + L::P_OFF + r * 128;
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const float* f = s + kb * 64 + ch * 8;
-          uint4 v;
-          v.x = pack_bf16x2(f[0], f[1]);
-          v.y = pack_bf16x2(f[2], f[3]);
-          v.z = pack_bf16x2(f[4], f[5]);
-          v.w = pack_bf16x2(f[6], f[7]);
-          *reinterpret_cast<uint4*>(prow + kb * BOX + ((ch ^ (r & 7)) << 4)) = v;
-        }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && mbar_wait_warp(o_ready, (nkv - 1) & 1, wc, 18)) {
+    if (ok && has_o && mbar_wait_warp(o_final0 + 8 * h, 0, wc, 18)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const int64_t off = (int64_t(b) * p.S + i) * p.out_ld + head * DH;
@@ -301,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int ch = 0; ch < DH / 32; ++ch) {
         uint32_t u[32];
-        tmem_ld32(tmem_base + lane_addr + 256u + uint32_t(ch * 32), u);
+        tmem_ld32(t_o + uint32_t(ch * 32), u);
         tmem_ld_wait(u);
         if (i < p.S) {
           float o[32];
@@ -351,7 +381,7 @@ cudaError_t launch_dh(const CUtensorMap& tmQK, const CUtensorMap& tmVT, const Sw
   static cudaError_t attr = cudaFuncSetAttribute(
       swa_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::SMEM));
   if (attr != cudaSuccess) return attr;
-  const int64_t grid = int64_t(p.num_q_tiles) * p.nh * p.B;
+  const int64_t grid = int64_t((p.num_q_tiles + 1) / 2) * p.nh * p.B;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
   swa_kernel<DH><<<unsigned(grid), THREADS, L::SMEM, stream>>>(tmQK, tmVT, p, status, limit_ns);
