@@ -155,7 +155,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
 // dp_tiles, then its contiguous share [cluster * W, (cluster + 1) * W) of the linearised
 // (tile, k-block) iterations of the sk_tiles stream-K tiles that follow them.
 struct Sched {
-  int num_m, num_kb;
+  int num_m, num_n, num_kb;
   int cluster, clusters;
   int dp_tiles, sk_tiles, W;
 };
@@ -170,6 +170,21 @@ struct SkParams {
 struct Unit {
   int tile, kb0, kb1;
 };
+
+// Tile index -> (pair-row block, column block). Tiles are ordered in groups of kGroupM
+// pair-rows, M fastest inside a group, so the CTA pairs running at the same time cover a
+// compact block of about kGroupM x (pairs / kGroupM) tiles and share both their A rows
+// and their B columns in L2.
+constexpr int kGroupM = 8;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m, int& n) {
+  const int per_group = kGroupM * num_n;
+  const int g = tile / per_group;
+  const int first_m = g * kGroupM;
+  const int gm = min(kGroupM, num_m - first_m);
+  const int r = tile - g * per_group;
+  m = first_m + r % gm;
+  n = r / gm;
+}
 
 struct UnitIter {
   int t;
@@ -257,6 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   Sched sc;
   sc.num_m = (ep.M + PM - 1) / PM;
+  sc.num_n = (ep.N + BN - 1) / BN;
   sc.num_kb = K / BK;
   sc.cluster = int(blockIdx.x) >> 1;
   sc.clusters = int(gridDim.x) >> 1;
@@ -276,8 +292,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       UnitIter ui(sc);
       Unit u;
       while (ok && ui.next(sc, u)) {
-        const int m0 = (u.tile % num_m) * PM + int(rank) * BM;
-        const int n0 = (u.tile / num_m) * BN + int(rank) * (BN / 2);
+        int tm, tn;
+        tile_coords(u.tile, num_m, sc.num_n, tm, tn);
+        const int m0 = tm * PM + int(rank) * BM;
+        const int n0 = tn * BN + int(rank) * (BN / 2);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, wc, 1)) {
             ok = false;
@@ -375,7 +393,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     while (ok && ui.next(sc, u)) {
       if (!mbar_wait_warp(tfull0 + 8 * acc, acc_par, wc, 4)) break;
       tc_fence_after();
-      const int m0 = (u.tile % num_m) * PM + int(rank) * BM, n0 = (u.tile / num_m) * BN;
+      int tm, tn;
+      tile_coords(u.tile, num_m, sc.num_n, tm, tn);
+      const int m0 = tm * PM + int(rank) * BM, n0 = tn * BN;
       const int row = m0 + int(quad * 32 + lane);
       const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + uint32_t(acc * BN);
       // This thread's row of a pair's partial tile ([2][128][256] fp32 per cluster).

@@ -7,11 +7,14 @@
 // keeps the score matrix on chip, so it never reaches HBM).
 //
 // One CTA per (pair of 128-query tiles, head, sequence): both query tiles share every
-// K/V tile the CTA loads. Only key tiles that meet the window of some query of the pair
+// K/V tile the CTA loads. CTAs are numbered head by head (heaviest pair first within a
+// head), so the CTAs running together mostly share their heads' K/V in L2. Only key tiles that meet the window of some query of the pair
 // are visited; a key tile one query tile does not need is skipped for that tile (no MMA,
 // no softmax), and only tiles that cross the diagonal or the window's far edge are masked
 // element by element.
-//   warp 0     TMA producer: both query tiles once, then K and V^T tiles, 2-stage ring
+//   warp 0     TMA producer: both query tiles once, then K tiles (3-stage ring, freed as
+//              soon as both S products have read them, loaded one tile ahead of V) and
+//              V^T tiles (2-stage ring)
 //   warp 1     tensor-memory owner and the single MMA-issuing thread, in the order
 //                S0 = Q0 K_j^T, S1 = Q1 K_j^T, then per tile h: O_h += P_h V_j followed
 //                by S_h = Q_h K_{j+1}^T
@@ -45,15 +48,17 @@ struct Layout {
   static constexpr int K_BYTES = BKV * DH * 2;
   static constexpr int VHALF = DH * 64 * 2;  // V^T box: DH rows x 64 keys
   static constexpr int V_BYTES = 2 * VHALF;
-  static constexpr int STAGE = K_BYTES + V_BYTES;
+  static constexpr int K_STAGES = 3, V_STAGES = 2;
   static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = 2 * Q_TILE;
-  static constexpr int BAR_OFF = KV_OFF + 2 * STAGE;
-  static constexpr int NUM_BARS = 12;
-  // Enough shared memory that only one CTA fits per SM: the CTA takes all 512
+  static constexpr int K_OFF = 2 * Q_TILE;
+  static constexpr int V_OFF = K_OFF + K_STAGES * K_BYTES;
+  static constexpr int BAR_OFF = V_OFF + V_STAGES * V_BYTES;
+  static constexpr int NUM_BARS = 18;
+  static constexpr size_t NEED = size_t(BAR_OFF) + NUM_BARS * 8 + 16 + 1024;
+  // At least enough shared memory that only one CTA fits per SM: the CTA takes all 512
   // tensor-memory columns.
-  static constexpr size_t SMEM = 200 * 1024;
-  static_assert(BAR_OFF + NUM_BARS * 8 + 16 + 1024 <= SMEM, "shared memory layout");
+  static constexpr size_t SMEM = NEED > 200 * 1024 ? NEED : 200 * 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory layout");
 };
 
 template <int DH>
@@ -66,21 +71,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   const uint32_t q_full = smem_u32(bars + 0);
-  const uint32_t kv_full0 = smem_u32(bars + 1);   // [2]
-  const uint32_t kv_empty0 = smem_u32(bars + 3);  // [2]
-  const uint32_t s_full0 = smem_u32(bars + 5);    // [2] per query tile
-  const uint32_t p_full0 = smem_u32(bars + 7);    // [2] per query tile (4 warps each)
-  const uint32_t o_final0 = smem_u32(bars + 9);   // [2] per query tile: last PV done
-  const uint32_t drain_bar = smem_u32(bars + 11);
+  const uint32_t k_full0 = smem_u32(bars + 1);    // [3]
+  const uint32_t k_empty0 = smem_u32(bars + 4);   // [3]
+  const uint32_t v_full0 = smem_u32(bars + 7);    // [2]
+  const uint32_t v_empty0 = smem_u32(bars + 9);   // [2]
+  const uint32_t s_full0 = smem_u32(bars + 11);   // [2] per query tile
+  const uint32_t p_full0 = smem_u32(bars + 13);   // [2] per query tile (4 warps each)
+  const uint32_t o_final0 = smem_u32(bars + 15);  // [2] per query tile: last PV done
+  const uint32_t drain_bar = smem_u32(bars + 17);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   // Heaviest query pairs first: with a window >= seq the last pairs see the most keys.
-  const int nbh = p.nh * p.B;
   const int num_pairs = (p.num_q_tiles + 1) / 2;
-  const int pair = num_pairs - 1 - int(blockIdx.x) / nbh;
-  const int head = int(blockIdx.x) % p.nh;
-  const int b = (int(blockIdx.x) % nbh) / p.nh;
+  const int pair = num_pairs - 1 - int(blockIdx.x) % num_pairs;
+  const int head = (int(blockIdx.x) / num_pairs) % p.nh;
+  const int b = int(blockIdx.x) / (num_pairs * p.nh);
   const int q0 = pair * 2 * BQ;
   // Key-tile range [kb, ke] of each query tile h (rows q0 + 128h ..); empty past seq.
   int kb[2], ke[2];
@@ -103,9 +109,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(k_full0 + 8 * s, 1);
+      mbar_init(k_empty0 + 8 * s, 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full0 + 8 * s, 1);
-      mbar_init(kv_empty0 + 8 * s, 1);
+      mbar_init(v_full0 + 8 * s, 1);
+      mbar_init(v_empty0 + 8 * s, 1);
       mbar_init(s_full0 + 8 * s, 1);
       mbar_init(p_full0 + 8 * s, 4);
       mbar_init(o_final0 + 8 * s, 1);
@@ -131,13 +141,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   // wait limit, so shared and tensor memory are never released under them.
   const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
   const uint32_t sQ = smem_u32(smem + L::Q_OFF);
-  const uint32_t sKV = smem_u32(smem + L::KV_OFF);
+  const uint32_t sK = smem_u32(smem + L::K_OFF);
+  const uint32_t sV = smem_u32(smem + L::V_OFF);
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
-      uint32_t last_par[2] = {0, 0};
-      uint32_t used = 0;
+      uint32_t k_par[3] = {0, 0, 0}, v_par[2] = {0, 0};
+      uint32_t k_used = 0, v_used = 0;
       mbar_arrive_expect_tx(q_full, 2 * L::Q_TILE);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -146,27 +157,46 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_3d(sQ + h * L::Q_TILE + hb * BOX, &tmQK, q_full, head * DH + hb * 64,
                       q0 + h * BQ, b);
       const int vt_row = (b * p.nh + head) * DH;
-      for (int idx = 0; idx < U; ++idx) {
-        const int st = idx & 1;
-        const uint32_t par = (idx >> 1) & 1;
-        if (!mbar_wait(kv_empty0 + 8 * st, par ^ 1, wc, 11)) break;
-        const uint32_t base = sKV + st * L::STAGE;
-        const int k0 = (kt_begin + idx) * BKV;
-        mbar_arrive_expect_tx(kv_full0 + 8 * st, L::STAGE);
+      auto load_k = [&](int idx) -> bool {
+        const int st = idx % 3;
+        const uint32_t par = (idx / 3) & 1;
+        if (!mbar_wait(k_empty0 + 8 * st, par ^ 1, wc, 11)) return false;
+        const uint32_t dst = sK + st * L::K_BYTES;
+        mbar_arrive_expect_tx(k_full0 + 8 * st, L::K_BYTES);
 #pragma unroll
         for (int hb = 0; hb < DH / 64; ++hb)
-          tma_load_3d(base + hb * BOX, &tmQK, kv_full0 + 8 * st, p.H + head * DH + hb * 64, k0,
-                      b);
+          tma_load_3d(dst + hb * BOX, &tmQK, k_full0 + 8 * st, p.H + head * DH + hb * 64,
+                      (kt_begin + idx) * BKV, b);
+        k_par[st] = par;
+        k_used |= 1u << st;
+        return true;
+      };
+      auto load_v = [&](int idx) -> bool {
+        const int st = idx & 1;
+        const uint32_t par = (idx >> 1) & 1;
+        if (!mbar_wait(v_empty0 + 8 * st, par ^ 1, wc, 10)) return false;
+        const uint32_t dst = sV + st * L::V_BYTES;
+        mbar_arrive_expect_tx(v_full0 + 8 * st, L::V_BYTES);
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh)
-          tma_load_2d(base + L::K_BYTES + kh * L::VHALF, &tmVT, kv_full0 + 8 * st, k0 + kh * 64,
-                      vt_row);
-        last_par[st] = par;
-        used |= 1u << st;
+          tma_load_2d(dst + kh * L::VHALF, &tmVT, v_full0 + 8 * st,
+                      (kt_begin + idx) * BKV + kh * 64, vt_row);
+        v_par[st] = par;
+        v_used |= 1u << st;
+        return true;
+      };
+      // K runs one tile ahead of V: S_h of the next tile is issued before P_h V of this one
+      // can be.
+      bool ok = load_k(0);
+      for (int idx = 0; ok && idx < U; ++idx) {
+        if (idx + 1 < U) ok = load_k(idx + 1);
+        if (ok) ok = load_v(idx);
       }
       mbar_wait_drain(q_full, 0, drain_ns);
+      for (int s = 0; s < 3; ++s)
+        if (k_used & (1u << s)) mbar_wait_drain(k_full0 + 8 * s, k_par[s], drain_ns);
       for (int s = 0; s < 2; ++s)
-        if (used & (1u << s)) mbar_wait_drain(kv_full0 + 8 * s, last_par[s], drain_ns);
+        if (v_used & (1u << s)) mbar_wait_drain(v_full0 + 8 * s, v_par[s], drain_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -178,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto issue_s = [&](int h, int idx) {
         const int j = kt_begin + idx;
         if (j >= kb[h] && j <= ke[h]) {
-          const uint32_t kbase = sKV + (idx & 1) * L::STAGE;
+          const uint32_t kbase = sK + (idx % 3) * L::K_BYTES;
           const uint32_t qbase = sQ + h * L::Q_TILE;
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
@@ -188,8 +218,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         mma_commit(s_full0 + 8 * h);
+        if (h == 1) mma_commit(k_empty0 + 8 * (idx % 3));  // both S products have K
       };
-      bool ok = mbar_wait(q_full, 0, wc, 12) && mbar_wait(kv_full0, 0, wc, 14);
+      bool ok = mbar_wait(q_full, 0, wc, 12) && mbar_wait(k_full0, 0, wc, 14);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -197,9 +228,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       for (int idx = 0; ok && idx < U; ++idx) {
         const int j = kt_begin + idx;
-        const uint32_t vbase = sKV + (idx & 1) * L::STAGE + L::K_BYTES;
+        const uint32_t vbase = sV + (idx & 1) * L::V_BYTES;
         for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait(p_full0 + 8 * h, idx & 1, wc, 13)) {
+          if (!mbar_wait(p_full0 + 8 * h, idx & 1, wc, 13) ||
+              (h == 0 && !mbar_wait(v_full0 + 8 * (idx & 1), (idx >> 1) & 1, wc, 17))) {
             ok = false;
             break;
           }
@@ -217,10 +249,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             first_pv[h] = false;
           }
-          if (idx + 1 == U) mma_commit(o_final0 + 8 * h);  // completes exactly once
+          if (h == 1) mma_commit(v_empty0 + 8 * (idx & 1));  // both PV products have V
+          if (idx + 1 == U) mma_commit(o_final0 + 8 * h);     // completes exactly once
           if (idx + 1 < U) {
-            if (h == 0 && !mbar_wait(kv_full0 + 8 * ((idx + 1) & 1), ((idx + 1) >> 1) & 1, wc,
-                                     15)) {
+            if (h == 0 &&
+                !mbar_wait(k_full0 + 8 * ((idx + 1) % 3), ((idx + 1) / 3) & 1, wc, 15)) {
               ok = false;
               break;
             }
@@ -228,8 +261,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             issue_s(h, idx + 1);
           }
         }
-        if (!ok) break;
-        mma_commit(kv_empty0 + 8 * (idx & 1));
       }
       mma_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0, drain_ns);
@@ -257,15 +288,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       if (j >= kb[h] && j <= ke[h]) {
+        // The whole S row, four loads in flight, one wait.
+        uint32_t u[BKV];
+#pragma unroll
+        for (int ch = 0; ch < BKV / 32; ++ch)
+          tmem_ld32(t_s + uint32_t(ch * 32), *reinterpret_cast<uint32_t(*)[32]>(u + ch * 32));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(u));
+        tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(u + 64));
+        tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(u + 96));
         float s[BKV];
 #pragma unroll
-        for (int ch = 0; ch < BKV / 32; ++ch) {
-          uint32_t u[32];
-          tmem_ld32(t_s + uint32_t(ch * 32), u);
-          tmem_ld_wait(u);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(u[e]);
-        }
+        for (int e = 0; e < BKV; ++e) s[e] = __uint_as_float(u[e]);
         const int k0 = j * BKV;
         const bool whole = (k0 + BKV - 1 <= qb) && (qb + BQ - 1 - k0 < p.window);
         if (!whole) {
@@ -275,9 +309,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (d < 0 || d >= p.window) s[e] = -INFINITY;
           }
         }
-        float mx = -INFINITY;
+        // Row maximum as a tree (8 independent chains), not one 128-long chain.
+        float mx8[8];
 #pragma unroll
-        for (int e = 0; e < BKV; ++e) mx = fmaxf(mx, s[e]);
+        for (int q = 0; q < 8; ++q) mx8[q] = s[q];
+#pragma unroll
+        for (int e = 8; e < BKV; e += 8)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx8[q] = fmaxf(mx8[q], s[e + q]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float mxs = mx * c;
         // Move the reference maximum only when the row maximum grew by more than 2^8
         // (from -inf, any finite maximum does); O is rescaled below, after P is stored.
@@ -288,9 +329,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           m_used = mxs;
         }
         const float m_eff = (m_used == -INFINITY) ? 0.f : m_used;
-        float sum = 0.f;
         // P_h over the first 64 columns of S_h: column m holds keys 2m (low) and 2m+1;
-        // 32 keys at a time.
+        // 32 keys at a time. The row sum runs in 8 independent partial sums.
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ch = 0; ch < BKV / 32; ++ch) {
           uint32_t pk[16];
@@ -298,12 +339,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int e = 0; e < 16; ++e) {
             const float a0 = ex2_approx(fmaf(s[ch * 32 + 2 * e], c, -m_eff));
             const float a1 = ex2_approx(fmaf(s[ch * 32 + 2 * e + 1], c, -m_eff));
-            sum += a0 + a1;
+            sum8[e & 7] += a0 + a1;
             pk[e] = pack_bf16x2(a0, a1);
           }
           tmem_st16(t_s + uint32_t(ch * 16), pk);
         }
-        l += sum;
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         tmem_st_wait();
         if (has_o && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
