@@ -77,10 +77,13 @@ struct SwaParams {
   int64_t out_ld;
   bool out_f16;  // write fp16 (else bf16)
 };
-constexpr int kSwaBQ = 128;
-constexpr int kSwaBKV = 128;
-cudaError_t launch_swa(const CUtensorMap& tmQK, const CUtensorMap& tmVT, const SwaParams& p,
-                       int* status, uint64_t limit_ns, cudaStream_t stream);
+constexpr int kSwaBQ = 128;  // query rows per tile (two tiles per CTA)
+constexpr int kSwaBKV = 128;  // keys per tile
+// tmQ: the [B][S][2H] q|k buffer in boxes of 64 columns x kSwaBQ rows; tmK: the same buffer
+// in boxes of 64 columns x kSwaBKV rows; tmVT: v^T [B*nh*dh][seq_pad] in boxes of kSwaBKV
+// keys x dh rows.
+cudaError_t launch_swa(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmVT,
+                       const SwaParams& p, int* status, uint64_t limit_ns, cudaStream_t stream);
 
 // ---------------------------------------------------------------- packing (pack.cu)
 // out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols; with out_f16 the bf16

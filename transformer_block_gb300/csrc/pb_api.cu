@@ -206,6 +206,24 @@ pb_status make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
   return make_map(m, base, 2, dims, strides, box, f16);
 }
 
+// Tensor maps of the attention step: q|k [B][S][2H] read as query tiles and as key tiles,
+// and v^T [B*H][seq_pad] read in boxes of 64 keys x dh rows.
+pb_status make_swa_maps(const pb_dims& d, const void* qk, const void* vt, size_t seq_pad,
+                        CUtensorMap* tm_q, CUtensorMap* tm_k, CUtensorMap* tm_vt) {
+  const uint64_t H = uint64_t(d.hidden);
+  const uint64_t dims[3] = {2 * H, uint64_t(d.seq), uint64_t(d.batch)};
+  const uint64_t strides[2] = {2 * H * 2, 2 * H * 2 * uint64_t(d.seq)};
+  const uint32_t qbox[3] = {64, uint32_t(pb::kSwaBQ), 1};
+  const uint32_t kbox[3] = {64, uint32_t(pb::kSwaBKV), 1};
+  pb_status s = make_map(tm_q, qk, 3, dims, strides, qbox);
+  if (s == PB_OK) s = make_map(tm_k, qk, 3, dims, strides, kbox);
+  if (s != PB_OK) return s;
+  const uint64_t vdims[2] = {uint64_t(d.seq), uint64_t(d.batch) * H};
+  const uint64_t vstr[1] = {uint64_t(seq_pad) * 2};
+  const uint32_t vbox[2] = {64, uint32_t(d.head_dim)};  // 64 keys = one 128-byte swizzle row
+  return make_map(tm_vt, vt, 2, vdims, vstr, vbox);
+}
+
 pb_status check_handle(pb_handle* h) {
   if (h == nullptr) return fail(PB_ERR_BAD_HANDLE, "handle is NULL");
   if (h->magic != kMagic) return fail(PB_ERR_BAD_HANDLE, "handle is destroyed or invalid");
@@ -268,19 +286,9 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   PB_CUDA(mark(2), "cudaEventRecord");
 
   // 3. sliding-window attention -> act[:, 0:H]
-  {
-    const uint64_t dims[3] = {uint64_t(2 * H), uint64_t(d.seq), uint64_t(d.batch)};
-    const uint64_t strides[2] = {uint64_t(2 * H) * 2, uint64_t(2 * H) * 2 * uint64_t(d.seq)};
-    const uint32_t box[3] = {64, uint32_t(pb::kSwaBQ), 1};
-    s = make_map(&tm_qk, qk, 3, dims, strides, box);
-    if (s != PB_OK) return s;
-    const uint64_t rows = uint64_t(d.batch) * uint64_t(H);
-    const uint64_t vdims[2] = {uint64_t(d.seq), rows};
-    const uint64_t vstr[1] = {uint64_t(L.seq_pad) * 2};
-    const uint32_t vbox[2] = {64, uint32_t(d.head_dim)};
-    s = make_map(&tm_vt, vt, 2, vdims, vstr, vbox);
-    if (s != PB_OK) return s;
-  }
+  CUtensorMap tm_k;
+  s = make_swa_maps(d, qk, vt, L.seq_pad, &tm_qk, &tm_k, &tm_vt);
+  if (s != PB_OK) return s;
   pb::SwaParams sp{};
   sp.B = d.batch;
   sp.S = d.seq;
@@ -293,7 +301,7 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   sp.out = act;
   sp.out_ld = H + F;
   sp.out_f16 = h->f16;
-  PB_CUDA(pb::launch_swa(tm_qk, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
+  PB_CUDA(pb::launch_swa(tm_qk, tm_k, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
   PB_CUDA(mark(3), "cudaEventRecord");
 
   // 4. y = x + [attn | GeLU(h)] [Wo ; W2] (+ b_o + b2)
@@ -693,16 +701,8 @@ pb_status pb_swa_attention(const pb_dims* dims, const void* qk, const void* vt, 
     return fail(PB_ERR_INVALID_ARG, "act_ld must be >= hidden and a multiple of 8");
   const int H = d.hidden;
   const size_t seq_pad = align_up(size_t(d.seq), 8);
-  CUtensorMap tm_qk, tm_vt;
-  const uint64_t dims3[3] = {uint64_t(2 * H), uint64_t(d.seq), uint64_t(d.batch)};
-  const uint64_t str3[2] = {uint64_t(2 * H) * 2, uint64_t(2 * H) * 2 * uint64_t(d.seq)};
-  const uint32_t box3[3] = {64, uint32_t(pb::kSwaBQ), 1};
-  s = make_map(&tm_qk, qk, 3, dims3, str3, box3);
-  if (s != PB_OK) return s;
-  const uint64_t vdims[2] = {uint64_t(d.seq), uint64_t(d.batch) * uint64_t(H)};
-  const uint64_t vstr[1] = {uint64_t(seq_pad) * 2};
-  const uint32_t vbox[2] = {64, uint32_t(d.head_dim)};
-  s = make_map(&tm_vt, vt, 2, vdims, vstr, vbox);
+  CUtensorMap tm_qk, tm_k, tm_vt;
+  s = make_swa_maps(d, qk, vt, seq_pad, &tm_qk, &tm_k, &tm_vt);
   if (s != PB_OK) return s;
   pb::SwaParams sp{};
   sp.B = d.batch;
@@ -716,7 +716,7 @@ pb_status pb_swa_attention(const pb_dims* dims, const void* qk, const void* vt, 
   sp.out = act;
   sp.out_ld = act_ld;
   sp.out_f16 = false;
-  PB_CUDA(pb::launch_swa(tm_qk, tm_vt, sp, status, kDefaultLimitNs,
+  PB_CUDA(pb::launch_swa(tm_qk, tm_k, tm_vt, sp, status, kDefaultLimitNs,
                          static_cast<cudaStream_t>(stream)),
           "attention launch");
   return PB_OK;

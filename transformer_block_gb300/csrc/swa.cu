@@ -65,6 +65,7 @@ template <int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     swa_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmVT,
                const SwaParams p, int* status, uint64_t limit_ns) {
+  static_assert(BKV == 128 && BQ == 128, "tile shape of this kernel");
   using L = Layout<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -431,10 +432,11 @@ cudaError_t launch_dh(const CUtensorMap& tmQK, const CUtensorMap& tmVT, const Sw
 
 }  // namespace
 
-cudaError_t launch_swa(const CUtensorMap& tmQK, const CUtensorMap& tmVT, const SwaParams& p,
-                       int* status, uint64_t limit_ns, cudaStream_t stream) {
-  if (p.dh == 64) return launch_dh<64>(tmQK, tmVT, p, status, limit_ns, stream);
-  if (p.dh == 128) return launch_dh<128>(tmQK, tmVT, p, status, limit_ns, stream);
+// Query and key tiles are both 128 rows, so tmK (the same q|k buffer) is not needed here.
+cudaError_t launch_swa(const CUtensorMap& tmQ, const CUtensorMap& /*tmK*/, const CUtensorMap& tmVT,
+                       const SwaParams& p, int* status, uint64_t limit_ns, cudaStream_t stream) {
+  if (p.dh == 64) return launch_dh<64>(tmQ, tmVT, p, status, limit_ns, stream);
+  if (p.dh == 128) return launch_dh<128>(tmQ, tmVT, p, status, limit_ns, stream);
   return cudaErrorInvalidValue;
 }
 
