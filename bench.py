@@ -199,6 +199,21 @@ def run_reference(args, wl):
     return 0
 
 
+def aggregate_timing(ms_local: float, world: int, model_flops: int, steps: int, device) -> tuple:
+    """Whole-job timing over the ranks: the job takes as long as its slowest rank, and every
+    rank processed its own replica's steps. Returns (max ms over ranks, TFLOP/s of the job).
+    Collective only when world > 1 (any torch.distributed backend: nccl or gloo)."""
+    import torch
+    import torch.distributed as dist
+
+    ms = float(ms_local)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * model_flops * steps / (ms / 1e3) / 1e12
+
+
 def config_of(wl, args):
     return {"workload": wl.name, "batch": wl.batch, "seq": wl.seq, "hidden": wl.hidden,
             "heads": wl.heads, "head_dim": wl.head_dim, "ffn": wl.ffn, "window": wl.window,
@@ -267,7 +282,7 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end)
+    ms_local = start.elapsed_time(end)
     per_kernel = [0.0] * 4
     for b in blocks:
         k_ms, n = b.trace_read()
@@ -277,13 +292,8 @@ def main():
     for b in blocks:
         if b.status() != pb.PB_OK:
             raise RuntimeError("device status word reports an error in the timed region")
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
     model = flops.model_flops(wl)
-    value = world * model * args.steps / (ms / 1e3) / 1e12
+    ms, value = aggregate_timing(ms_local, world, model, args.steps, "cuda")
 
     # ---- end to end through the host-buffer entry point (pinned x in, y out)
     e2e = None
@@ -302,13 +312,9 @@ def main():
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e_ms = t0.elapsed_time(t1)
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms, e_value = aggregate_timing(t0.elapsed_time(t1), world, model, n_e2e, "cuda")
         nbytes = x.numel() * x.element_size()
-        e2e = {"value": world * model * n_e2e / (e_ms / 1e3) / 1e12, "unit": UNIT,
+        e2e = {"value": e_value, "unit": UNIT,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
                "steps": n_e2e, "ms_per_step": e_ms / n_e2e,
                "api": "pb_forward_stack_host"}
