@@ -7,11 +7,11 @@
 // keeps the score matrix on chip, so it never reaches HBM).
 //
 // One CTA per (pair of 128-query tiles, head, sequence): both query tiles share every
-// K/V tile the CTA loads. CTAs are numbered head by head (heaviest pair first within a
-// head), so the CTAs running together mostly share their heads' K/V in L2. Only key tiles that meet the window of some query of the pair
-// are visited; a key tile one query tile does not need is skipped for that tile (no MMA,
-// no softmax), and only tiles that cross the diagonal or the window's far edge are masked
-// element by element.
+// K/V tile the CTA loads. CTAs are numbered by pair index, heaviest first, then sequence
+// and head. Only key tiles that meet the window of some query of the pair are visited; a
+// key tile one query tile does not need is skipped for that tile (no MMA, no softmax), and
+// only tiles that cross the diagonal or the window's far edge are masked element by
+// element.
 //   warp 0     TMA producer: both query tiles once, then K tiles (3-stage ring, freed as
 //              soon as both S products have read them, loaded one tile ahead of V) and
 //              V^T tiles (2-stage ring)
@@ -41,6 +41,35 @@ constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX = 128 * 64 * 2;          // one 128-row x 64-column 16-bit box: 16 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// One softmax row of a tile: p_k = 2^(s_k c - m) rounded to bf16 into tensor memory at t_s
+// (column m holds keys 2m and 2m + 1), 32 keys per store; returns the fp32 sum of the
+// unrounded p_k. Scale, shift and sum run on packed pairs.
+__device__ __forceinline__ float probs_to_tmem(const float (&s)[kSwaBKV], float c, float m,
+                                               uint32_t t_s) {
+  const uint64_t c2 = f2(c, c), nm2 = f2(-m, -m);
+  uint64_t acc[4] = {0, 0, 0, 0};  // four independent partial sums of pairs
+#pragma unroll
+  for (int ch = 0; ch < kSwaBKV / 32; ++ch) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint64_t x2 = f2_fma(f2(s[ch * 32 + 2 * e], s[ch * 32 + 2 * e + 1]), c2, nm2);
+      float x0, x1;
+      f2_split(x2, x0, x1);
+      const uint64_t a2 = f2(ex2_approx(x0), ex2_approx(x1));
+      acc[e & 3] = f2_add(acc[e & 3], a2);
+      float a0, a1;
+      f2_split(a2, a0, a1);
+      pk[e] = pack_bf16x2(a0, a1);
+    }
+    tmem_st16(t_s + uint32_t(ch * 16), pk);
+  }
+  const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  float lo, hi;
+  f2_split(t, lo, hi);
+  return lo + hi;
+}
 
 template <int DH>
 struct Layout {
@@ -83,11 +112,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  // Heaviest query pairs first: with a window >= seq the last pairs see the most keys.
+  // Longest work first: a pair's key-tile count never falls as the pair index grows (it
+  // grows until the window is full, then stays), so CTAs run in descending pair order,
+  // every (sequence, head) of one pair index before the next. CTAs start in index order
+  // as SMs free up, which makes this the longest-processing-time-first schedule.
   const int num_pairs = (p.num_q_tiles + 1) / 2;
-  const int pair = num_pairs - 1 - int(blockIdx.x) % num_pairs;
-  const int head = (int(blockIdx.x) / num_pairs) % p.nh;
-  const int b = int(blockIdx.x) / (num_pairs * p.nh);
+  const int pair = num_pairs - 1 - int(blockIdx.x) / (p.nh * p.B);
+  const int head = int(blockIdx.x) % p.nh;
+  const int b = (int(blockIdx.x) / p.nh) % p.B;
   const int q0 = pair * 2 * BQ;
   // Key-tile range [kb, ke] of each query tile h (rows q0 + 128h ..); empty past seq.
   int kb[2], ke[2];
@@ -310,16 +342,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (d < 0 || d >= p.window) s[e] = -INFINITY;
           }
         }
-        // Row maximum as a tree (8 independent chains), not one 128-long chain.
-        float mx8[8];
+        // Row maximum: four independent chains of three-input maxima.
+        float mx4[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) mx8[q] = s[q];
+        for (int q = 0; q < 4; ++q) {
+          float a = s[32 * q];
 #pragma unroll
-        for (int e = 8; e < BKV; e += 8)
-#pragma unroll
-          for (int q = 0; q < 8; ++q) mx8[q] = fmaxf(mx8[q], s[e + q]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int e = 1; e < 31; e += 2) a = max3f(a, s[32 * q + e], s[32 * q + e + 1]);
+          mx4[q] = fmaxf(a, s[32 * q + 31]);
+        }
+        const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]);
         const float mxs = mx * c;
         // Move the reference maximum only when the row maximum grew by more than 2^8
         // (from -inf, any finite maximum does); O is rescaled below, after P is stored.
@@ -330,22 +362,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           m_used = mxs;
         }
         const float m_eff = (m_used == -INFINITY) ? 0.f : m_used;
-        // P_h over the first 64 columns of S_h: column m holds keys 2m (low) and 2m+1;
-        // 32 keys at a time. The row sum runs in 8 independent partial sums.
-        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ch = 0; ch < BKV / 32; ++ch) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float a0 = ex2_approx(fmaf(s[ch * 32 + 2 * e], c, -m_eff));
-            const float a1 = ex2_approx(fmaf(s[ch * 32 + 2 * e + 1], c, -m_eff));
-            sum8[e & 7] += a0 + a1;
-            pk[e] = pack_bf16x2(a0, a1);
-          }
-          tmem_st16(t_s + uint32_t(ch * 16), pk);
-        }
-        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        // P_h over the first 64 columns of S_h (masked keys give exactly 0).
+        l += probs_to_tmem(s, c, m_eff, t_s);
         tmem_st_wait();
         if (has_o && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
