@@ -156,6 +156,19 @@ __device__ __forceinline__ void cluster_sync() {
                ::: "memory");
 }
 
+// ------------------------------------------------------------------------- registers
+// Per-warpgroup register budgets (all four warps of the warpgroup execute it). The sum
+// over the block must stay within what the block was launched with (threads x registers
+// per thread at launch), or the increase waits forever.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
