@@ -12,9 +12,10 @@
 // 6-stage ring, and holds its 128 x 256 half of the fp32 accumulator in its tensor
 // memory (double-buffered, 2 x 256 columns, so the epilogue of one tile overlaps the
 // main loop of the next).
-//   warp 0     TMA producer (both CTAs), each CTA's copies signal its own barrier
-//   warp 1     even CTA: the MMA-issuing thread; odd CTA: relays "my stage landed" to
-//              the even CTA with a remote mbarrier arrive; both: tensor-memory owner
+//   warp 0     TMA producer (both CTAs); every copy of the pair completes on the even
+//              CTA's stage barrier (the pair form of the TMA load), so the MMA issuer
+//              waits on one barrier per stage
+//   warp 1     even CTA: the MMA-issuing thread; both: tensor-memory owner
 //   warps 2-5  epilogue, one TMEM lane quadrant each (warp w reads lanes 32*(w%4)..+31)
 // MMA completion is multicast to both CTAs' barriers. Pair tiles are handed out
 // round-robin over the clusters, M fastest, so clusters running at the same time share
@@ -39,7 +40,7 @@ constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 3 * STAGES + 5;
+constexpr int NUM_BARS = 2 * STAGES + 5;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16;
 
 __device__ __forceinline__ float gelu_erf(float z) {
@@ -226,12 +227,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(STAGES) * STAGE_BYTES);
-  const uint32_t full0 = smem_u32(bars);                   // [STAGES] own copies landed
-  const uint32_t empty0 = smem_u32(bars + STAGES);         // [STAGES] pair MMAs done reading
-  const uint32_t peer0 = smem_u32(bars + 2 * STAGES);      // [STAGES] odd CTA's copies landed
-  const uint32_t tfull0 = smem_u32(bars + 3 * STAGES);     // [2] accumulator ready
-  const uint32_t tempty0 = smem_u32(bars + 3 * STAGES + 2);  // [2] accumulator drained (x8)
-  const uint32_t drain_bar = smem_u32(bars + 3 * STAGES + 4);
+  // full: both CTAs' copies of a stage landed (used in the even CTA only: the odd CTA's
+  // copies complete on the even CTA's barrier). empty: the pair's MMAs are done reading.
+  const uint32_t full0 = smem_u32(bars);                   // [STAGES]
+  const uint32_t empty0 = smem_u32(bars + STAGES);         // [STAGES]
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);     // [2] accumulator ready
+  const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);  // [2] accumulator drained (x8)
+  const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -242,7 +244,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
-      mbar_init(peer0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -286,6 +287,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ------------------------------------------------------------ TMA producer
       uint32_t last_par[STAGES];
       uint32_t used = 0;
+      // The stage's full barrier in the even CTA, as a cluster address.
+      const uint32_t full_pair0 = mapa_shared(full0, 0);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -302,9 +305,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const uint32_t sa = smem_u32(smem + size_t(stage) * STAGE_BYTES);
-          mbar_arrive_expect_tx(full0 + 8 * stage, STAGE_BYTES);
-          tma_load_2d(sa, &tmA, full0 + 8 * stage, kb * BK, m0);
-          tma_load_2d(sa + A_BYTES, &tmB, full0 + 8 * stage, kb * BK, n0);
+          // The even CTA announces both CTAs' bytes; copies that land before it does only
+          // drive the transaction count below zero, and the phase cannot complete without
+          // its arrival. The odd CTA reuses a stage only after the pair's MMAs read it, so
+          // its copies always count toward the phase the MMA issuer waits for next.
+          if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
+          tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, kb * BK, m0);
+          tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, kb * BK, n0);
           last_par[stage] = phase;
           used |= 1u << stage;
           if (++stage == STAGES) {
@@ -313,9 +320,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // Every copy this thread started must land before the CTA exits.
-      for (int s = 0; s < STAGES; ++s)
-        if (used & (1u << s)) mbar_wait_drain(full0 + 8 * s, last_par[s], drain_ns);
+      // Every copy of the pair must land before either CTA exits: the even CTA waits for
+      // its full barriers (which count the odd CTA's bytes too); the odd CTA is held at the
+      // final cluster barrier until then.
+      if (leader)
+        for (int s = 0; s < STAGES; ++s)
+          if (used & (1u << s)) mbar_wait_drain(full0 + 8 * s, last_par[s], drain_ns);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -333,8 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, wc, 3) ||
-              !mbar_wait(peer0 + 8 * stage, phase, wc, 5)) {
+          if (!mbar_wait(full0 + 8 * stage, phase, wc, 3)) {
             ok = false;
             break;
           }
@@ -360,26 +369,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       // either CTA releases it.
       mma_commit_pair(drain_bar, 0x1);
       mbar_wait_drain(drain_bar, 0, drain_ns);
-    } else if (lane == 0) {
-      // ------------------------------------------------------------ odd CTA: relay
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      UnitIter ui(sc);
-      Unit u;
-      while (ok && ui.next(sc, u)) {
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, wc, 6)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_remote(mapa_shared(peer0 + 8 * stage, 0));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
     }
     __syncwarp();
   } else {
