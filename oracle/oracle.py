@@ -246,6 +246,47 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
     return y, stages
 
 
+def serial_block_forward(dims: Dims, x, params: dict, rows: dict | None = None,
+                         threads: int = 0, lib=None):
+    """The standard (serial) transformer block of eq. (3), in float64, on the same weights:
+
+        h = x + Attn(LN(x)),   y = h + MLP(LN'(h))
+
+    (MegaScale reading notes, section 1.1, "Parallel Transformer Block", eq. (3)). The
+    printed eq. (3) leaves the attention term out of the outer sum; the derivation under it
+    (the parallel block replaces the MLP input LN(x + h2) by LN(x), h2 = Attention(LN(x)))
+    only holds with the attention output in the residual stream, as in eq. (4), so it is
+    kept here. LN' uses ``ln2_gamma``/``ln2_beta`` when given, else the block's one
+    LayerNorm (eq. (3) writes the same LN twice). ``Attn(LN(x)) = softmax(..) V Wo + b_o``
+    is the attention term of eq. (4), taken from ``block_forward``; the MLP is
+    ``GeLU(LN'(h) W1 + b1) W2 + b2``. ``rows`` as in ``block_forward``.
+    """
+    lib = lib or load()
+    B, S, H = dims.batch, dims.seq, dims.hidden
+    x = np.asarray(x).reshape(B, S, H)
+    _, st = block_forward(dims, x, params, rows=rows, threads=threads, keep_stages=True,
+                          lib=lib)
+    if rows is None:
+        xq = _f64(x.reshape(B * S, H))
+    else:
+        parts = []
+        for b in range(B):
+            pos = np.unique(np.asarray(rows.get(b, []), dtype=np.int64))
+            if pos.size:
+                parts.append(x[b][pos])
+        xq = _f64(np.concatenate(parts)) if parts else np.zeros((0, H))
+    h = xq + st["att_proj"]
+    g2 = _param(params, "ln2_gamma")
+    b2n = _param(params, "ln2_beta")
+    if g2 is None:
+        g2, b2n = _param(params, "ln_gamma"), _param(params, "ln_beta")
+    hn = layernorm(h, g2, b2n, dims.ln_eps, threads, lib)
+    m = linear(gelu(linear(hn, params["w1"], _param(params, "b1"), threads, lib), threads, lib),
+               params["w2"], _param(params, "b2"), threads, lib)
+    y = h + m
+    return y.reshape(B, S, H) if rows is None else y
+
+
 def stack_forward(dims: Dims, x, layers: list, prefix: int | None = None, threads: int = 0,
                   lib=None):
     """``len(layers)`` blocks applied in turn, ``x_{l+1} = block_l(x_l)`` (float64 between

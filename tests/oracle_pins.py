@@ -13,7 +13,10 @@ What pins what:
 * identities of the method: window >= seq is full causal attention; the concatenated
   weight form ``x + [attn | GeLU(h)] [Wo ; W2]`` equals the two-branch sum;
 * invariants: LayerNorm statistics, value rows all equal give that value, head
-  permutation, translation of a window, per-row shift of x, batch independence.
+  permutation, translation of a window, per-row shift of x, batch independence;
+* the serial block of eq. (3): restated with torch routines, equal to the parallel
+  block when either branch's output weight is zero, and first-order in the attention
+  term when compared with the parallel block.
 """
 
 from __future__ import annotations
@@ -322,10 +325,99 @@ def pin_block_rows_mode(lib):
     return _close(part, want, 1e-13)
 
 
+# ----------------------------------------------------------------------------- serial block
+
+
+def torch_serial_block(dims, x, p):
+    """The serial block (h = x + Attn(LN(x)), y = h + MLP(LN'(h))) with torch float64
+    library routines."""
+    B, S, H, nh, dh = dims.batch, dims.seq, dims.hidden, dims.heads, dims.head_dim
+    T = lambda a: None if a is None else torch.from_numpy(np.asarray(a, dtype=np.float64))
+    X = T(x).reshape(B, S, H)
+    xn = F.layer_norm(X, (H,), T(p["ln_gamma"]), T(p["ln_beta"]), dims.ln_eps)
+    qkv = xn @ T(p["wqkv"])
+    if p.get("b_qkv") is not None:
+        qkv = qkv + T(p["b_qkv"])
+    q, k, v = (qkv[..., i * H:(i + 1) * H].reshape(B, S, nh, dh).transpose(1, 2) for i in range(3))
+    a = F.scaled_dot_product_attention(q, k, v, attn_mask=band_mask(S, dims.window))
+    a = a.transpose(1, 2).reshape(B, S, H) @ T(p["wo"])
+    if p.get("b_o") is not None:
+        a = a + T(p["b_o"])
+    h = X + a
+    g2 = T(p.get("ln2_gamma", p["ln_gamma"]))
+    b2 = T(p.get("ln2_beta", p["ln_beta"]))
+    hn = F.layer_norm(h, (H,), g2, b2, dims.ln_eps)
+    z = hn @ T(p["w1"])
+    if p.get("b1") is not None:
+        z = z + T(p["b1"])
+    m = F.gelu(z, approximate="none") @ T(p["w2"])
+    if p.get("b2") is not None:
+        m = m + T(p["b2"])
+    return (h + m).numpy()
+
+
+def pin_serial_library(lib):
+    ok, detail = True, []
+    for w, second_ln in ((1, False), (3, True), (8, False), (13, True)):
+        dims = O.Dims(2, 8, 8, 2, 4, 16, w)
+        p = tiny_params(8, 2, 16, seed=120 + w)
+        if second_ln:
+            r = _rng(130 + w)
+            p["ln2_gamma"] = 1 + 0.1 * r.normal(size=8)
+            p["ln2_beta"] = 0.1 * r.normal(size=8)
+        x = _rng(140 + w).normal(size=(2, 8, 8))
+        o, d = _close(O.serial_block_forward(dims, x, p, lib=lib), torch_serial_block(dims, x, p),
+                      1e-12)
+        ok &= o
+        detail.append(f"w={w}: {d}")
+    return ok, "; ".join(detail)
+
+
+def pin_serial_reduces_to_parallel(lib):
+    # Without the attention output (Wo = 0, b_o absent) or without the MLP output
+    # (W2 = 0, b2 absent), eq. (3) and eq. (4) are the same function.
+    dims = O.Dims(2, 10, 16, 4, 4, 32, 4)
+    x = _rng(151).normal(size=(2, 10, 16))
+    out = []
+    for name, zero in (("no attention", {"wo": np.zeros((16, 16)), "b_o": None}),
+                       ("no MLP", {"w2": np.zeros((32, 16)), "b2": None})):
+        p = tiny_params(16, 4, 32, seed=150)
+        p.update(zero)
+        out.append((name, _close(O.serial_block_forward(dims, x, p, lib=lib),
+                                 O.block_forward(dims, x, p, lib=lib), 1e-12)))
+    return all(o for _, (o, _) in out), "; ".join(f"{n}: {d}" for n, (_, d) in out)
+
+
+def pin_serial_first_order(lib):
+    # With the attention term scaled by eps, serial - parallel = J_MLP(LN) . h2 + O(eps^2):
+    # nonzero, and halving eps halves it (the MLP really reads LN(x + h2)).
+    dims = O.Dims(1, 12, 16, 4, 4, 32, 5)
+    x = _rng(161).normal(size=(1, 12, 16))
+    diffs = []
+    for eps in (1e-3, 5e-4):
+        p = tiny_params(16, 4, 32, seed=160, biases=False)
+        p["wo"] = eps * p["wo"]
+        diffs.append(np.max(np.abs(O.serial_block_forward(dims, x, p, lib=lib)
+                                   - O.block_forward(dims, x, p, lib=lib))))
+    ratio = diffs[0] / diffs[1] if diffs[1] > 0 else float("inf")
+    return bool(diffs[1] > 0 and abs(ratio - 2.0) < 0.05), f"diffs={diffs}, ratio={ratio:.4f}"
+
+
+def pin_serial_rows_mode(lib):
+    dims = O.Dims(2, 30, 16, 4, 4, 32, 6)
+    p = tiny_params(16, 4, 32, seed=170)
+    x = _rng(171).normal(size=(2, 30, 16))
+    full = O.serial_block_forward(dims, x, p, lib=lib)
+    rows = {0: [0, 29], 1: [4, 5, 17]}
+    part = O.serial_block_forward(dims, x, p, rows=rows, lib=lib)
+    return _close(part, np.concatenate([full[b][rows[b]] for b in (0, 1)]), 1e-13)
+
+
 ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_layernorm_library,
             pin_layernorm_stats, pin_linear_library, pin_attention_window1_is_v,
             pin_attention_window2_closed_form, pin_attention_full_causal,
             pin_attention_band_library, pin_attention_rows_sum_to_one,
             pin_attention_translation, pin_block_library, pin_block_concat_identity,
             pin_block_zero_affine, pin_block_zero_output_weights, pin_block_invariants,
-            pin_block_rows_mode]
+            pin_block_rows_mode, pin_serial_library, pin_serial_reduces_to_parallel,
+            pin_serial_first_order, pin_serial_rows_mode]

@@ -38,3 +38,32 @@ def test_threads_do_not_change_results():
     a = O.block_forward(dims, x, p, threads=1)
     b = O.block_forward(dims, x, p, threads=5)
     assert np.array_equal(a, b)
+
+
+def _serial_mutants():
+    """Plausible mistakes in the serial block's composition (each must break a pin)."""
+    real = O.serial_block_forward
+
+    def parallel_instead(dims, x, p, rows=None, threads=0, lib=None):
+        return O.block_forward(dims, x, p, rows=rows, threads=threads, lib=lib)
+
+    def literal_eq3(dims, x, p, rows=None, threads=0, lib=None):
+        # y = x + MLP(LN(x + Attn(LN(x)))): the attention term left out of the output
+        y = real(dims, x, p, rows=rows, threads=threads, lib=lib)
+        _, st = O.block_forward(dims, x, p, rows=rows, threads=threads, keep_stages=True,
+                                lib=lib)
+        return y - st["att_proj"].reshape(y.shape)
+
+    def first_ln_twice(dims, x, p, rows=None, threads=0, lib=None):
+        q = {k: v for k, v in p.items() if k not in ("ln2_gamma", "ln2_beta")}
+        return real(dims, x, q, rows=rows, threads=threads, lib=lib)
+
+    return [parallel_instead, literal_eq3, first_ln_twice]
+
+
+@pytest.mark.parametrize("mutant", _serial_mutants(), ids=lambda f: f.__name__)
+def test_serial_pins_catch_mutant(mutant, monkeypatch):
+    monkeypatch.setattr(O, "serial_block_forward", mutant)
+    serial_pins = [P.pin_serial_library, P.pin_serial_reduces_to_parallel,
+                   P.pin_serial_first_order, P.pin_serial_rows_mode]
+    assert not all(pin(O.load())[0] for pin in serial_pins)

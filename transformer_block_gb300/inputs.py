@@ -5,8 +5,9 @@ is drawn in float32 from ``torch.randn`` on a generator seeded with
 ``seed * 1000 + layer`` and rounded to bf16 (round to nearest even), so both sides
 consume identical bf16 values. Draw order per layer stream: ``x`` (layer 0 only), then
 ``ln_gamma = 1 + 0.1 N``, ``ln_beta = 0.1 N``, ``Wq, Wk, Wv, W1, Wo, W2 = std * N``
-(``[in, out]`` layout), then, if requested, the biases ``b_qkv, b1, b_o, b2 = 0.02 N``.
-``x ~ N(0, 1)``.
+(``[in, out]`` layout), then, if requested, the biases ``b_qkv, b1, b_o, b2 = 0.02 N``,
+then, if requested, a second LayerNorm ``ln2_gamma = 1 + 0.1 N``, ``ln2_beta = 0.1 N`` (the
+serial block's). ``x ~ N(0, 1)``.
 """
 
 from __future__ import annotations
@@ -31,7 +32,8 @@ def _draw(g, shape, device, scale=1.0, shift=0.0) -> torch.Tensor:
     return t.to(torch.bfloat16)
 
 
-def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu", biases: bool = False):
+def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu", biases: bool = False,
+               ln2: bool = False):
     """Returns ``(x or None, params)``; ``x`` is ``[B*S, H]`` bf16 and only drawn for layer 0."""
     H, F = wl.hidden, wl.ffn
     g = _gen(device, seed, layer)
@@ -53,6 +55,9 @@ def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu", biases
         p["b1"] = _draw(g, (F,), device, 0.02)
         p["b_o"] = _draw(g, (H,), device, 0.02)
         p["b2"] = _draw(g, (H,), device, 0.02)
+    if ln2:
+        p["ln2_gamma"] = _draw(g, (H,), device, 0.1, 1.0)
+        p["ln2_beta"] = _draw(g, (H,), device, 0.1)
     return x, p
 
 
