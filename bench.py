@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ab-serial", action="store_true",
+                    help="instead of the contract line, time the parallel block (eq. (4)) and "
+                         "the serial block (eq. (3)) on the same weights, one GPU, and print "
+                         "one JSON line with both")
     ap.add_argument("--cpu-rows", type=int, default=192,
                     help="tokens of the oracle's CPU-baseline sample")
     return ap.parse_args()
@@ -224,6 +228,59 @@ def config_of(wl, args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def run_ab_serial(args, wl) -> int:
+    """Parallel (eq. (4), pb_forward: 4 launches) against serial (eq. (3),
+    pb_forward_serial: 7 launches) on one handle, same weights and inputs, same model
+    FLOPs. Rounds alternate the two so clock drift affects both alike."""
+    import torch
+
+    from transformer_block_gb300 import flops, inputs, pb
+
+    if wl.layers != 1:
+        raise SystemExit("--ab-serial compares one block: pick a single-layer workload")
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    x, params = inputs.make_layer(wl, 0, device="cuda")
+    dims = pb.make_dims(wl)
+    block = pb.ParallelBlock(dims, params)
+    del params
+    scratch = pb.new_scratch(dims)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    runs = {"parallel": lambda: block.forward(x, y=y, scratch=scratch),
+            "serial": lambda: block.forward_serial(x, y=y, scratch=scratch)}
+    for fn in runs.values():
+        for _ in range(args.warmup):
+            fn()
+    torch.cuda.synchronize()
+    ms = {k: [] for k in runs}
+    rounds = 4
+    per_round = max(1, args.steps // rounds)
+    for _ in range(rounds):
+        for name, fn in runs.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(per_round):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms[name].append(a.elapsed_time(b) / per_round)
+    if block.status() != pb.PB_OK:
+        raise RuntimeError("device status word reports an error")
+    model = flops.model_flops(wl)
+    med = {k: sorted(v)[len(v) // 2] for k, v in ms.items()}
+    line = {"metric": "parallel (eq. 4) vs serial (eq. 3) block fwd TFLOP/s, same weights, 1 GPU",
+            "unit": UNIT, "higher_is_better": True, "steps": per_round * rounds,
+            "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl, args),
+            "parallel": {"value": model / (med["parallel"] * 1e-3) / 1e12,
+                         "ms_per_step": med["parallel"], "launches": 4},
+            "serial": {"value": model / (med["serial"] * 1e-3) / 1e12,
+                       "ms_per_step": med["serial"], "launches": 7},
+            "parallel_over_serial": med["serial"] / med["parallel"]}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     from transformer_block_gb300 import BENCH_WORKLOAD, WORKLOADS
@@ -231,6 +288,8 @@ def main():
     wl = WORKLOADS[args.workload or BENCH_WORKLOAD]
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.ab_serial:
+        return run_ab_serial(args, wl)
 
     import torch
     import torch.distributed as dist

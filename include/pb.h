@@ -162,6 +162,20 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* weights, const pb_
 pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t scratch_bytes,
                      void* stream);
 
+/* The serial (standard) transformer block of eq. (3) (MegaScale reading notes, section 1.1,
+ * "Parallel Transformer Block") on the handle's weights, for comparison with pb_forward:
+ *   h = x + Attn(LN(x)),   y = h + MLP(LN'(h)),   MLP(z) = GeLU(z W1 + b1) W2 + b2,
+ * with Attn(.) W_o + b_o as in pb_forward. The printed eq. (3) omits the attention term from
+ * the outer sum; the derivation beside it (the parallel block replaces LN(x + h2) by LN(x))
+ * requires it, so it is included. LN' has parameters ln2_gamma / ln2_beta (device bf16
+ * [H], 16-byte aligned), or the handle's LayerNorm when both are NULL (eq. (3) writes the
+ * same LN twice). x, y, scratch as in pb_forward (x == y allowed); h is kept in fp32 in
+ * scratch res0. Seven kernel launches instead of four: the MLP waits for the attention
+ * output. */
+pb_status pb_forward_serial(pb_handle* h, const void* x, void* y, const void* ln2_gamma,
+                            const void* ln2_beta, void* scratch, size_t scratch_bytes,
+                            void* stream);
+
 /* A stack of residual blocks (MegaScale reading notes, section 1.1: L layers give a
  * receptive field of L*w), x_{l+1} = block_l(x_l). All handles must have the same
  * dims. Between layers the residual stream stays in fp32 (scratch res0/res1; the pages

@@ -117,6 +117,7 @@ def test_create_rejects_bad_options(lib):
 
 def test_null_handles(lib):
     assert lib.pb_forward(None, None, None, None, 0, None) == 6
+    assert lib.pb_forward_serial(None, None, None, None, None, None, 0, None) == 6
     assert lib.pb_destroy(None) == 6
     assert lib.pb_get_status(None) == 6
     arr = (ctypes.c_void_p * 1)(None)

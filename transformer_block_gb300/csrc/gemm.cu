@@ -93,10 +93,11 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
     store_row32<false>(ep.c + int64_t(row) * ep.ldc + col0, v);
   } else if (KIND == kEpiBlockIn) {
     const int H = ep.H;
-    if (col0 < 2 * H) {  // q | k
-      store_row32<false>(ep.qk + int64_t(row) * (2 * H) + col0, v);
-    } else if (col0 < 3 * H) {  // v, stored transposed per (sequence, head)
-      const int c = col0 - 2 * H;
+    const int cc = col0 + ep.col_base;  // column of [q | k | v | h]
+    if (cc < 2 * H) {  // q | k
+      store_row32<false>(ep.qk + int64_t(row) * (2 * H) + cc, v);
+    } else if (cc < 3 * H) {  // v, stored transposed per (sequence, head)
+      const int c = cc - 2 * H;
       const int head = c / ep.dh, d0 = c - head * ep.dh;
       const int b = row / ep.S, s = row - b * ep.S;
       __nv_bfloat16* dst =
@@ -106,7 +107,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
     } else {  // h -> GeLU(h), next to the attention output in the second GEMM's A operand
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-      const int64_t off = int64_t(row) * (H + ep.F) + H + (col0 - 3 * H);
+      const int64_t off = int64_t(row) * (H + ep.F) + H + (cc - 3 * H);
       if (ep.act_f16) {
         bool bad = false;
 #pragma unroll

@@ -37,7 +37,10 @@ struct EpiParams {
   // kEpiStore
   __nv_bfloat16* c;
   int64_t ldc;
-  // kEpiBlockIn
+  // kEpiBlockIn. Output column c of this GEMM is routed as column c + col_base of
+  // [q | k | v | h]: 0 for the parallel block's one GEMM over [Wqkv | W1], 3H for a GEMM
+  // over W1 alone (the serial block's MLP input projection).
+  int col_base;
   int H, F, S, nh, dh;
   int64_t seq_pad;
   __nv_bfloat16* qk;   // [T, 2H]
@@ -91,10 +94,12 @@ cudaError_t launch_swa(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
                              void* out, int64_t ld_out, bool out_f16, int* status,
                              cudaStream_t stream);
-// bias1[3H + F] = [b_qkv | b1] (0 where absent); bias2[H] = b_o + b2.
+// bias1[3H + F] = [b_qkv | b1] (0 where absent); bias2[H] = b_o + b2; bias_o[H] = b_o and
+// bias_2[H] = b2 apart (the serial block adds them in two different GEMMs).
 cudaError_t launch_bias_prep(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
                              const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
-                             float* bias1, float* bias2, cudaStream_t stream);
+                             float* bias1, float* bias2, float* bias_o, float* bias_2,
+                             cudaStream_t stream);
 
 // ---------------------------------------------------------------- self-test (gemm.cu)
 cudaError_t launch_wait_probe(uint64_t limit_ns, int* status, cudaStream_t stream);

@@ -48,7 +48,7 @@ __global__ void transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t r
 
 __global__ void bias_prep_kernel(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
                                  const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
-                                 float* bias1, float* bias2) {
+                                 float* bias1, float* bias2, float* bias_o, float* bias_2) {
   const int n1 = 3 * H + F;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n1; i += gridDim.x * blockDim.x) {
     float v = 0.f;
@@ -59,10 +59,11 @@ __global__ void bias_prep_kernel(const __nv_bfloat16* b_qkv, const __nv_bfloat16
     }
     bias1[i] = v;
     if (i < H) {
-      float w = 0.f;
-      if (b_o) w += __bfloat162float(b_o[i]);
-      if (b2) w += __bfloat162float(b2[i]);
-      bias2[i] = w;
+      const float o = b_o ? __bfloat162float(b_o[i]) : 0.f;
+      const float t = b2 ? __bfloat162float(b2[i]) : 0.f;
+      bias2[i] = o + t;
+      bias_o[i] = o;
+      bias_2[i] = t;
     }
   }
 }
@@ -88,8 +89,10 @@ cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols
 
 cudaError_t launch_bias_prep(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
                              const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
-                             float* bias1, float* bias2, cudaStream_t stream) {
-  bias_prep_kernel<<<256, 256, 0, stream>>>(b_qkv, b1, b_o, b2, H, F, bias1, bias2);
+                             float* bias1, float* bias2, float* bias_o, float* bias_2,
+                             cudaStream_t stream) {
+  bias_prep_kernel<<<256, 256, 0, stream>>>(b_qkv, b1, b_o, b2, H, F, bias1, bias2, bias_o,
+                                            bias_2);
   return cudaGetLastError();
 }
 

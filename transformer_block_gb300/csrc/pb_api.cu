@@ -32,7 +32,9 @@ struct pb_handle {
   void* w1cat;             // [3H + F, H], bf16 or fp16
   void* w2cat;             // [H, H + F], bf16 or fp16
   float* bias1;            // [3H + F]
-  float* bias2;            // [H]
+  float* bias2;            // [H] = b_o + b2
+  float* bias_o;           // [H] = b_o (serial block)
+  float* bias_2;           // [H] = b2 (serial block)
   __nv_bfloat16* gamma;    // [H]
   __nv_bfloat16* beta;     // [H]
   bool has_bias;
@@ -99,7 +101,7 @@ pb_status check_dims(const pb_dims* d) {
 }
 
 struct WsLayout {
-  size_t status, w1cat, w2cat, bias1, bias2, gamma, beta, total;
+  size_t status, w1cat, w2cat, bias1, bias2, bias_o, bias_2, gamma, beta, total;
 };
 
 WsLayout ws_layout(const pb_dims& d) {
@@ -115,6 +117,10 @@ WsLayout ws_layout(const pb_dims& d) {
   L.bias1 = off;
   off = align_up(off + (3 * H + F) * 4, 1024);
   L.bias2 = off;
+  off = align_up(off + H * 4, 1024);
+  L.bias_o = off;
+  off = align_up(off + H * 4, 1024);
+  L.bias_2 = off;
   off = align_up(off + H * 4, 1024);
   L.gamma = off;
   off = align_up(off + H * 2, 1024);
@@ -321,6 +327,119 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   return PB_OK;
 }
 
+// The serial (standard) block of eq. (3) on the same packed weights, for comparison with
+// the parallel block (MegaScale reading notes, section 1.1):
+//   h = x + Attn(LN(x))        (fp32, scratch res0)
+//   y = h + MLP(LN'(h))
+// Seven launches: LN, GEMM over the Wqkv rows of W1cat, attention, GEMM over the Wo
+// columns of W2cat (+ x), LN', GEMM over the W1 rows of W1cat (GeLU), GEMM over the W2
+// columns of W2cat (+ h). The two output projections cannot share one GEMM here: the MLP
+// reads LN'(h), which needs the attention output first.
+pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* gamma2,
+                     const __nv_bfloat16* beta2, uint8_t* scratch, cudaStream_t st) {
+  const pb_dims& d = h->d;
+  const pb_scratch_layout L = scratch_layout(d);
+  const int H = d.hidden, F = d.ffn, T = d.batch * d.seq;
+  const uint32_t box = pb::kGemmBoxRows;
+  const size_t esz = 2;  // bf16 or fp16 operands
+  void* xn = scratch + L.xn;
+  auto* qk = reinterpret_cast<__nv_bfloat16*>(scratch + L.qk);
+  auto* vt = reinterpret_cast<__nv_bfloat16*>(scratch + L.vt);
+  uint8_t* act = scratch + L.act;
+  float* hres = reinterpret_cast<float*>(scratch + L.res0);
+  uint8_t* w1c = static_cast<uint8_t*>(h->w1cat);
+  uint8_t* w2c = static_cast<uint8_t*>(h->w2cat);
+
+  // 1. LN(x)
+  PB_CUDA(pb::launch_layernorm(T, H, x, false, h->gamma, h->beta, d.ln_eps, xn, h->f16,
+                               h->status, st),
+          "layernorm launch");
+  // 2. [q | k | v] = xn Wqkv (+ b_qkv): rows [0, 3H) of W1cat
+  CUtensorMap tm_xn, tm_wqkv;
+  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, box, h->f16);
+  if (s == PB_OK) s = make_map_2d(&tm_wqkv, w1c, 3 * uint64_t(H), H, H, box, h->f16);
+  if (s != PB_OK) return s;
+  EpiParams e1{};
+  e1.status = h->status;
+  e1.H = H;
+  e1.F = F;
+  e1.S = d.seq;
+  e1.nh = d.heads;
+  e1.dh = d.head_dim;
+  e1.seq_pad = int64_t(L.seq_pad);
+  e1.qk = qk;
+  e1.vt = vt;
+  e1.act = act;
+  e1.act_f16 = h->f16;
+  e1.bias = h->has_bias ? h->bias1 : nullptr;
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, tm_wqkv, T, 3 * H, H, e1, h->num_sms,
+                          h->status, h->limit_ns, scratch + L.sk, st),
+          "QKV GEMM launch");
+  // 3. sliding-window attention -> act[:, 0:H]
+  CUtensorMap tm_qk, tm_k, tm_vt;
+  s = make_swa_maps(d, qk, vt, L.seq_pad, &tm_qk, &tm_k, &tm_vt);
+  if (s != PB_OK) return s;
+  pb::SwaParams sp{};
+  sp.B = d.batch;
+  sp.S = d.seq;
+  sp.H = H;
+  sp.nh = d.heads;
+  sp.dh = d.head_dim;
+  sp.window = d.window;
+  sp.num_q_tiles = (d.seq + pb::kSwaBQ - 1) / pb::kSwaBQ;
+  sp.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d.head_dim)));
+  sp.out = act;
+  sp.out_ld = H + F;
+  sp.out_f16 = h->f16;
+  PB_CUDA(pb::launch_swa(tm_qk, tm_k, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
+  // 4. h = x + attn Wo (+ b_o): columns [0, H) of W2cat, result in fp32
+  CUtensorMap tm_attn, tm_wo;
+  s = make_map_2d(&tm_attn, act, T, H, H + F, box, h->f16);
+  if (s == PB_OK) s = make_map_2d(&tm_wo, w2c, H, H, H + F, box, h->f16);
+  if (s != PB_OK) return s;
+  EpiParams e2{};
+  e2.status = h->status;
+  e2.bias = h->has_bias ? h->bias_o : nullptr;
+  e2.resid = x;
+  e2.resid_f32 = false;
+  e2.y = hres;
+  e2.y_f32 = true;
+  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->f16, tm_attn, tm_wo, T, H, H, e2, h->num_sms,
+                          h->status, h->limit_ns, scratch + L.sk, st),
+          "attention projection GEMM launch");
+  // 5. LN'(h) -> xn
+  PB_CUDA(pb::launch_layernorm(T, H, hres, true, gamma2, beta2, d.ln_eps, xn, h->f16, h->status,
+                               st),
+          "second layernorm launch");
+  // 6. GeLU(LN'(h) W1 (+ b1)) -> act[:, H:H+F]: rows [3H, 3H + F) of W1cat, routed as the
+  // h columns of [q | k | v | h]
+  CUtensorMap tm_w1;
+  s = make_map_2d(&tm_w1, w1c + 3 * size_t(H) * H * esz, F, H, H, box, h->f16);
+  if (s != PB_OK) return s;
+  EpiParams e3 = e1;
+  e3.col_base = 3 * H;
+  e3.bias = h->has_bias ? h->bias1 + 3 * size_t(H) : nullptr;
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, tm_w1, T, F, H, e3, h->num_sms,
+                          h->status, h->limit_ns, scratch + L.sk, st),
+          "MLP input GEMM launch");
+  // 7. y = h + GeLU(.) W2 (+ b2): A = act[:, H:H+F], columns [H, H + F) of W2cat
+  CUtensorMap tm_g, tm_w2;
+  s = make_map_2d(&tm_g, act + size_t(H) * esz, T, F, H + F, box, h->f16);
+  if (s == PB_OK) s = make_map_2d(&tm_w2, w2c + size_t(H) * esz, H, F, H + F, box, h->f16);
+  if (s != PB_OK) return s;
+  EpiParams e4{};
+  e4.status = h->status;
+  e4.bias = h->has_bias ? h->bias_2 : nullptr;
+  e4.resid = hres;
+  e4.resid_f32 = true;
+  e4.y = y;
+  e4.y_f32 = false;
+  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->f16, tm_g, tm_w2, T, H, F, e4, h->num_sms,
+                          h->status, h->limit_ns, scratch + L.sk, st),
+          "MLP output GEMM launch");
+  return PB_OK;
+}
+
 void trace_free(pb_handle* h) {
   for (cudaEvent_t e : h->trace) cudaEventDestroy(e);
   h->trace.clear();
@@ -465,6 +584,8 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
   h->w2cat = h->ws + L.w2cat;
   h->bias1 = reinterpret_cast<float*>(h->ws + L.bias1);
   h->bias2 = reinterpret_cast<float*>(h->ws + L.bias2);
+  h->bias_o = reinterpret_cast<float*>(h->ws + L.bias_o);
+  h->bias_2 = reinterpret_cast<float*>(h->ws + L.bias_2);
   h->gamma = reinterpret_cast<__nv_bfloat16*>(h->ws + L.gamma);
   h->beta = reinterpret_cast<__nv_bfloat16*>(h->ws + L.beta);
   h->has_bias = w->b_qkv || w->b1 || w->b_o || w->b2;
@@ -497,7 +618,7 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
   PB_CUDA_H(pb::launch_transpose(bf(w->w2), F, H, H, w2c + H * 2, H + F, h->f16, h->status, st),
             "pack W2");
   PB_CUDA_H(pb::launch_bias_prep(bf(w->b_qkv), bf(w->b1), bf(w->b_o), bf(w->b2), int(H), int(F),
-                                 h->bias1, h->bias2, st),
+                                 h->bias1, h->bias2, h->bias_o, h->bias_2, st),
             "bias prep");
   PB_CUDA_H(cudaMemcpyAsync(h->gamma, w->ln_gamma, H * 2, cudaMemcpyDeviceToDevice, st),
             "copy gamma");
@@ -525,6 +646,30 @@ pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t
     return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
   return run_block(h, x, false, y, false, static_cast<uint8_t*>(scratch),
                    static_cast<cudaStream_t>(stream));
+}
+
+pb_status pb_forward_serial(pb_handle* h, const void* x, void* y, const void* ln2_gamma,
+                            const void* ln2_beta, void* scratch, size_t scratch_bytes,
+                            void* stream) {
+  pb_status s = check_stack(&h, 1, scratch, scratch_bytes);
+  if (s != PB_OK) return s;
+  if (x == nullptr || y == nullptr || !aligned(x, 16) || !aligned(y, 16))
+    return fail(PB_ERR_INVALID_ARG, "x and y must be 16-byte aligned device pointers");
+  if ((ln2_gamma == nullptr) != (ln2_beta == nullptr))
+    return fail(PB_ERR_INVALID_ARG, "ln2_gamma and ln2_beta must both be given or both NULL");
+  if ((ln2_gamma != nullptr && !aligned(ln2_gamma, 16)) ||
+      (ln2_beta != nullptr && !aligned(ln2_beta, 16)))
+    return fail(PB_ERR_INVALID_ARG, "ln2_gamma and ln2_beta must be 16-byte aligned");
+  const size_t n = size_t(h->d.batch) * h->d.seq * h->d.hidden * 2;
+  if (x != y && overlap(x, n, y, n))
+    return fail(PB_ERR_INVALID_ARG, "x and y overlap without being equal");
+  const pb_scratch_layout L = scratch_layout(h->d);
+  if (overlap(x, n, scratch, L.total) || overlap(y, n, scratch, L.total))
+    return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
+  const auto* g2 = ln2_gamma ? static_cast<const __nv_bfloat16*>(ln2_gamma) : h->gamma;
+  const auto* b2 = ln2_beta ? static_cast<const __nv_bfloat16*>(ln2_beta) : h->beta;
+  return run_serial(h, x, y, g2, b2, static_cast<uint8_t*>(scratch),
+                    static_cast<cudaStream_t>(stream));
 }
 
 pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const void* x, void* y,

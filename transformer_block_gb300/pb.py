@@ -65,6 +65,7 @@ SIGNATURES = {
     "pb_create_ex": (ctypes.c_int, [_DP, ctypes.POINTER(pb_weights),
                                     ctypes.POINTER(pb_options), _P, _S, _P, ctypes.POINTER(_P)]),
     "pb_forward": (ctypes.c_int, [_P, _P, _P, _P, _S, _P]),
+    "pb_forward_serial": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _S, _P]),
     "pb_forward_stack": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
     "pb_forward_stack_host": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
     "pb_get_status": (ctypes.c_int, [_P]),
@@ -205,6 +206,20 @@ class ParallelBlock:
         return y
 
     __call__ = forward
+
+    def forward_serial(self, x: torch.Tensor, y: torch.Tensor | None = None,
+                       ln2_gamma: torch.Tensor | None = None, ln2_beta: torch.Tensor | None = None,
+                       scratch: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """The serial block of eq. (3) on the same weights (``pb_forward_serial``)."""
+        if y is None:
+            y = torch.empty_like(x)
+        if scratch is None:
+            scratch = new_scratch(self.dims, x.device)
+        _check("pb_forward_serial",
+               self._lib.pb_forward_serial(self.handle, _ptr(x), _ptr(y), _ptr(ln2_gamma),
+                                           _ptr(ln2_beta), _ptr(scratch), scratch.numel(),
+                                           _stream(stream)))
+        return y
 
     def status(self) -> int:
         return self._lib.pb_get_status(self.handle)
