@@ -81,6 +81,23 @@ void oracle_layernorm(int64_t rows, int64_t H, const double* x, const double* ga
   });
 }
 
+// RMSNorm over the last dimension (the normalisation of the fused "RMSNorm" kernel the
+// MegaScale reading notes list in section 1.3; the pages do not define it, this is the
+// standard form): out[r,c] = x[r,c] / sqrt(mean_c x[r,c]^2 + eps) * gamma[c].
+void oracle_rmsnorm(int64_t rows, int64_t H, const double* x, const double* gamma, double eps,
+                    double* out, int threads) {
+  for_row_ranges(rows, threads, [=](int64_t r0, int64_t r1) {
+    for (int64_t r = r0; r < r1; ++r) {
+      const double* xr = x + r * H;
+      double sq = 0.0;
+      for (int64_t c = 0; c < H; ++c) sq += xr[c] * xr[c];
+      const double inv = 1.0 / std::sqrt(sq / (double)H + eps);
+      double* o = out + r * H;
+      for (int64_t c = 0; c < H; ++c) o[c] = xr[c] * inv * gamma[c];
+    }
+  });
+}
+
 // Linear layer in the pages' convention Y = X W (Megatron-LM notes section 2.1, with W
 // stored [in, out] row-major):
 //   C[i, j] = bias[j] + sum_{k=0}^{K-1} A[i, k] * W[k, j]      (bias may be NULL)
@@ -118,6 +135,14 @@ void oracle_gelu(int64_t n, const double* in, double* out, int threads) {
   const double inv_sqrt2 = 0.70710678118654752440;
   for_row_ranges(n, threads, [=](int64_t b, int64_t e) {
     for (int64_t i = b; i < e; ++i) out[i] = 0.5 * in[i] * (1.0 + std::erf(in[i] * inv_sqrt2));
+  });
+}
+
+// SwiGLU activation (the "SiLU + elementwise multiply" fusion of section 1.3):
+// out[i] = silu(gate[i]) * up[i],  silu(z) = z / (1 + exp(-z)).
+void oracle_swiglu(int64_t n, const double* gate, const double* up, double* out, int threads) {
+  for_row_ranges(n, threads, [=](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i) out[i] = gate[i] / (1.0 + std::exp(-gate[i])) * up[i];
   });
 }
 

@@ -19,6 +19,13 @@ step by step, in the pages' order, with the ORIGINAL separate weights:
 4. ``attn = concat_heads(o) Wo``, ``mlp = GeLU(h) W2``.
 5. ``y = x + mlp + attn``.
 
+Two further block forms, on the same primitives:
+* ``Dims(variant=1)``: RMSNorm and a SwiGLU MLP (the fused "RMSNorm" and "SiLU +
+  elementwise multiply" kernels of section 1.3, which the pages name without defining;
+  the standard forms are taken: ``x / sqrt(mean x^2 + eps) * gamma`` and
+  ``silu(x W_gate) * (x W_up)``, ``w1 = [W_gate | W_up]``).
+* ``serial_block_forward``: the standard block of eq. (3), for comparison.
+
 All arithmetic is float64 in oracle.cpp (built here with g++); inputs are the exact
 bf16 values the GPU receives, passed as float32/float64 arrays.
 
@@ -67,8 +74,10 @@ def _bind(lib):
     lib.oracle_gelu.argtypes = [i64, d, d, i32]
     lib.oracle_swa_attention.argtypes = [i64, d, d, i64, d, d, d, i64, i64, i64, d, i32]
     lib.oracle_add3.argtypes = [i64, d, d, d, d]
+    lib.oracle_rmsnorm.argtypes = [i64, i64, d, d, ctypes.c_double, d, i32]
+    lib.oracle_swiglu.argtypes = [i64, d, d, d, i32]
     for f in ("oracle_layernorm", "oracle_linear", "oracle_gelu", "oracle_swa_attention",
-              "oracle_add3"):
+              "oracle_add3", "oracle_rmsnorm", "oracle_swiglu"):
         getattr(lib, f).restype = None
     return lib
 
@@ -101,6 +110,9 @@ class Dims:
     ffn: int
     window: int
     ln_eps: float = 1e-5
+    # 0: LayerNorm + GeLU MLP (eq. (4) as written); 1: RMSNorm + SwiGLU MLP (the fused
+    # kernels of section 1.3), w1 = [W_gate | W_up] of [H, 2F].
+    variant: int = 0
 
 
 # ----------------------------------------------------------------------------- primitives
@@ -117,6 +129,39 @@ def layernorm(x, gamma, beta, eps, threads=0, lib=None) -> np.ndarray:
     out = np.empty_like(x)
     lib.oracle_layernorm(rows, H, _ptr(x), _ptr(g), _ptr(b), float(eps), _ptr(out), threads)
     return out
+
+
+def rmsnorm(x, gamma, eps, threads=0, lib=None) -> np.ndarray:
+    lib = lib or load()
+    x, g = _f64(x), _f64(gamma)
+    rows, H = x.shape
+    out = np.empty_like(x)
+    lib.oracle_rmsnorm(rows, H, _ptr(x), _ptr(g), float(eps), _ptr(out), threads)
+    return out
+
+
+def swiglu(gate, up, threads=0, lib=None) -> np.ndarray:
+    lib = lib or load()
+    gate, up = _f64(gate), _f64(up)
+    assert gate.shape == up.shape
+    out = np.empty_like(gate)
+    lib.oracle_swiglu(gate.size, _ptr(gate), _ptr(up), _ptr(out), threads)
+    return out
+
+
+def _norm(dims, x, gamma, beta, threads, lib):
+    """The block's normalisation: LayerNorm (variant 0) or RMSNorm (variant 1, no beta)."""
+    if dims.variant == 1:
+        return rmsnorm(x, gamma, dims.ln_eps, threads, lib)
+    return layernorm(x, gamma, beta, dims.ln_eps, threads, lib)
+
+
+def _mlp_act(dims, h, threads, lib):
+    """GeLU(h) (variant 0), or SwiGLU over h = [gate | up] (variant 1)."""
+    if dims.variant == 1:
+        F = dims.ffn
+        return swiglu(h[:, :F], h[:, F:], threads, lib)
+    return gelu(h, threads, lib)
 
 
 def linear(a, w, bias=None, threads=0, lib=None) -> np.ndarray:
@@ -167,7 +212,10 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
 
     ``x``: ``[B, S, H]``; ``params``: ``ln_gamma, ln_beta [H]``, ``wqkv [H, 3H]``,
     ``w1 [H, F]``, ``wo [H, H]``, ``w2 [F, H]`` (all ``Y = X W``, ``[in, out]``) and
-    optional ``b_qkv [3H]``, ``b1 [F]``, ``b_o [H]``, ``b2 [H]``.
+    optional ``b_qkv [3H]``, ``b1 [F]``, ``b_o [H]``, ``b2 [H]``. With ``dims.variant == 1``
+    the normalisation is RMSNorm (``ln_beta`` unused) and the MLP is SwiGLU:
+    ``w1 = [W_gate | W_up]`` is ``[H, 2F]``, ``b1`` is ``[2F]``, and the MLP's activation is
+    ``silu(gate) * up`` (the fused kernels of section 1.3).
 
     ``rows=None`` returns ``y [B, S, H]``. ``rows={b: positions}`` returns only those
     output rows, ``[sum_b len(positions), H]``, ordered by ``b`` then position.
@@ -203,7 +251,7 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
 
     cone_x = np.concatenate([x[b][cone[b]] for b in want]) if want else np.zeros((0, H))
     # 1. one LayerNorm, shared by both branches
-    xn_cone = layernorm(cone_x, gamma, beta, dims.ln_eps, threads, lib)
+    xn_cone = _norm(dims, cone_x, gamma, beta, threads, lib)
     # rows of the cone that are wanted queries
     sel, off = [], 0
     for b in want:
@@ -229,7 +277,7 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
         koff += nk
 
     # 4. the two output projections
-    g = gelu(h, threads, lib)
+    g = _mlp_act(dims, h, threads, lib)
     mlp = linear(g, params["w2"], _param(params, "b2"), threads, lib)
     att = linear(attn, params["wo"], _param(params, "b_o"), threads, lib)
 
@@ -241,7 +289,7 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
         y = y.reshape(B, S, H)
     if not keep_stages:
         return y
-    stages = {"xn": xn_q, "q": q, "k": k[sel], "v": v[sel], "h": h, "gelu_h": g,
+    stages = {"xn": xn_q, "q": q, "k": k[sel], "v": v[sel], "h": h, "gelu_h": g, "mlp_act": g,
               "attn": attn, "mlp": mlp, "att_proj": att}
     return y, stages
 
@@ -280,8 +328,9 @@ def serial_block_forward(dims: Dims, x, params: dict, rows: dict | None = None,
     b2n = _param(params, "ln2_beta")
     if g2 is None:
         g2, b2n = _param(params, "ln_gamma"), _param(params, "ln_beta")
-    hn = layernorm(h, g2, b2n, dims.ln_eps, threads, lib)
-    m = linear(gelu(linear(hn, params["w1"], _param(params, "b1"), threads, lib), threads, lib),
+    hn = _norm(dims, h, g2, b2n, threads, lib)
+    m = linear(_mlp_act(dims, linear(hn, params["w1"], _param(params, "b1"), threads, lib),
+                        threads, lib),
                params["w2"], _param(params, "b2"), threads, lib)
     y = h + m
     return y.reshape(B, S, H) if rows is None else y

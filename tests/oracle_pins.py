@@ -14,6 +14,9 @@ What pins what:
   weight form ``x + [attn | GeLU(h)] [Wo ; W2]`` equals the two-branch sum;
 * invariants: LayerNorm statistics, value rows all equal give that value, head
   permutation, translation of a window, per-row shift of x, batch independence;
+* RMSNorm + SwiGLU (the fused kernels of section 1.3): closed forms (constant rows,
+  sigmoid(ln 3) = 3/4), torch ``rms_norm`` / ``silu``, RMSNorm's scale invariance, and
+  the variant block restated with torch routines;
 * the serial block of eq. (3): restated with torch routines, equal to the parallel
   block when either branch's output weight is zero, and first-order in the attention
   term when compared with the parallel block.
@@ -413,6 +416,110 @@ def pin_serial_rows_mode(lib):
     return _close(part, np.concatenate([full[b][rows[b]] for b in (0, 1)]), 1e-13)
 
 
+# ----------------------------------------------------------------------------- RMSNorm + SwiGLU
+
+
+def pin_rmsnorm_closed_form(lib):
+    # a constant row c: rms = |c|; a 2-vector (a, b): rms = sqrt((a^2 + b^2) / 2)
+    eps = 1e-5
+    x = np.array([[3.0, 3.0, 3.0, 3.0], [-2.0, -2.0, -2.0, -2.0]])
+    g = np.array([1.0, 2.0, -1.0, 0.5])
+    want = np.sign(x) * np.abs(x) / np.sqrt(x ** 2 + eps) * g
+    ok1, d1 = _close(O.rmsnorm(x, g, eps, lib=lib), want, 1e-15)
+    x2 = np.array([[3.0, 4.0]])
+    want2 = x2 / math.sqrt(12.5 + eps)
+    ok2, d2 = _close(O.rmsnorm(x2, np.ones(2), eps, lib=lib), want2, 1e-15)
+    return ok1 and ok2, f"{d1}; {d2}"
+
+
+def pin_rmsnorm_library(lib):
+    x = _rng(180).normal(0, 2, size=(7, 48))
+    g = 1 + 0.1 * _rng(181).normal(size=48)
+    want = F.rms_norm(torch.from_numpy(x), (48,), torch.from_numpy(g), 1e-5).numpy()
+    return _close(O.rmsnorm(x, g, 1e-5, lib=lib), want, 1e-14)
+
+
+def pin_rmsnorm_scale_invariance(lib):
+    # RMSNorm(a x) = RMSNorm(x) for a > 0 (eps -> 0), and it does not remove the row mean
+    x = _rng(182).normal(0.5, 1, size=(5, 32))
+    g = _rng(183).normal(size=32)
+    a = O.rmsnorm(x, g, 1e-30, lib=lib)
+    b = O.rmsnorm(7.5 * x, g, 1e-30, lib=lib)
+    ok, d = _close(a, b, 1e-13)
+    shifted = O.rmsnorm(x + 3.0, g, 1e-30, lib=lib)
+    return ok and float(np.max(np.abs(shifted - a))) > 1e-3, d
+
+
+def pin_swiglu_closed_form(lib):
+    # sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4; silu(0) = 0
+    l3 = math.log(3.0)
+    gate = np.array([l3, -l3, 0.0, l3])
+    up = np.array([1.0, 1.0, 5.0, -2.0])
+    want = np.array([0.75 * l3, -0.25 * l3, 0.0, -1.5 * l3])
+    return _close(O.swiglu(gate, up, lib=lib), want, 1e-15)
+
+
+def pin_swiglu_library(lib):
+    gate = _rng(184).normal(0, 4, 500)
+    up = _rng(185).normal(0, 1, 500)
+    want = (F.silu(torch.from_numpy(gate)) * torch.from_numpy(up)).numpy()
+    return _close(O.swiglu(gate, up, lib=lib), want, 1e-14)
+
+
+def swiglu_params(H, nh, F_, seed, biases=True, std=0.3):
+    p = tiny_params(H, nh, F_, seed, biases, std)
+    r = _rng(seed + 1000)
+    p["w1"] = std * r.normal(size=(H, 2 * F_))
+    if biases:
+        p["b1"] = 0.1 * r.normal(size=2 * F_)
+    return p
+
+
+def torch_block_swiglu(dims, x, p):
+    """The RMSNorm + SwiGLU parallel block restated with torch float64 routines."""
+    B, S, H, nh, dh, F_ = dims.batch, dims.seq, dims.hidden, dims.heads, dims.head_dim, dims.ffn
+    T = lambda a: None if a is None else torch.from_numpy(np.asarray(a, dtype=np.float64))
+    X = T(x).reshape(B, S, H)
+    xn = F.rms_norm(X, (H,), T(p["ln_gamma"]), dims.ln_eps)
+    qkv = xn @ T(p["wqkv"])
+    if p.get("b_qkv") is not None:
+        qkv = qkv + T(p["b_qkv"])
+    q, k, v = (qkv[..., i * H:(i + 1) * H].reshape(B, S, nh, dh).transpose(1, 2) for i in range(3))
+    a = F.scaled_dot_product_attention(q, k, v, attn_mask=band_mask(S, dims.window))
+    a = a.transpose(1, 2).reshape(B, S, H) @ T(p["wo"])
+    if p.get("b_o") is not None:
+        a = a + T(p["b_o"])
+    z = xn @ T(p["w1"])
+    if p.get("b1") is not None:
+        z = z + T(p["b1"])
+    m = (F.silu(z[..., :F_]) * z[..., F_:]) @ T(p["w2"])
+    if p.get("b2") is not None:
+        m = m + T(p["b2"])
+    return (X + m + a).numpy()
+
+
+def pin_block_swiglu_library(lib):
+    ok, detail = True, []
+    for w in (1, 3, 13):
+        dims = O.Dims(2, 8, 8, 2, 4, 16, w, variant=1)
+        p = swiglu_params(8, 2, 16, seed=190 + w)
+        x = _rng(200 + w).normal(size=(2, 8, 8))
+        o, d = _close(O.block_forward(dims, x, p, lib=lib), torch_block_swiglu(dims, x, p), 1e-12)
+        ok &= o
+        detail.append(f"w={w}: {d}")
+    return ok, "; ".join(detail)
+
+
+def pin_block_swiglu_rows_mode(lib):
+    dims = O.Dims(2, 30, 16, 4, 4, 32, 6, variant=1)
+    p = swiglu_params(16, 4, 32, seed=210)
+    x = _rng(211).normal(size=(2, 30, 16))
+    full = O.block_forward(dims, x, p, lib=lib)
+    rows = {0: [0, 29], 1: [4, 5, 17]}
+    part = O.block_forward(dims, x, p, rows=rows, lib=lib)
+    return _close(part, np.concatenate([full[b][rows[b]] for b in (0, 1)]), 1e-13)
+
+
 ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_layernorm_library,
             pin_layernorm_stats, pin_linear_library, pin_attention_window1_is_v,
             pin_attention_window2_closed_form, pin_attention_full_causal,
@@ -420,4 +527,6 @@ ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_laye
             pin_attention_translation, pin_block_library, pin_block_concat_identity,
             pin_block_zero_affine, pin_block_zero_output_weights, pin_block_invariants,
             pin_block_rows_mode, pin_serial_library, pin_serial_reduces_to_parallel,
-            pin_serial_first_order, pin_serial_rows_mode]
+            pin_serial_first_order, pin_serial_rows_mode, pin_rmsnorm_closed_form,
+            pin_rmsnorm_library, pin_rmsnorm_scale_invariance, pin_swiglu_closed_form,
+            pin_swiglu_library, pin_block_swiglu_library, pin_block_swiglu_rows_mode]

@@ -16,7 +16,7 @@ from tests import oracle_pins as P
 MUTANTS = {
     "window_off_by_one": ("dist >= w", "dist > w"),
     "not_causal": ("dist < 0 || dist >= w", "dist >= w || -dist >= w"),
-    "ln_unbiased_variance": ("sq / (double)H", "sq / (double)(H - 1)"),
+    "ln_unbiased_variance": ("var = sq / (double)H;", "var = sq / (double)(H - 1);"),
     "ln_no_eps": ("std::sqrt(var + eps)", "std::sqrt(var)"),
     "ln_no_beta": ("inv * gamma[c] + beta[c]", "inv * gamma[c]"),
     "ln_no_centering": ("o[c] = (xr[c] - mu) * inv", "o[c] = xr[c] * inv"),
@@ -28,6 +28,11 @@ MUTANTS = {
     "linear_no_bias": ("bias ? bias[j] : 0.0", "0.0"),
     "linear_transposed": ("ci[j] += a * wk[j]", "ci[j] += a * W[(j % K) * ldw + (k % N)]"),
     "add3_drops_term": ("out[i] = a[i] + b[i] + c[i]", "out[i] = a[i] + b[i]"),
+    "rms_no_eps": ("std::sqrt(sq / (double)H + eps)", "std::sqrt(sq / (double)H)"),
+    "rms_mean_not_square": ("sq += xr[c] * xr[c]", "sq += xr[c] * std::fabs(xr[c])"),
+    "rms_no_gamma": ("o[c] = xr[c] * inv * gamma[c]", "o[c] = xr[c] * inv"),
+    "silu_sign": ("(1.0 + std::exp(-gate[i]))", "(1.0 + std::exp(gate[i]))"),
+    "swiglu_drops_up": ("std::exp(-gate[i])) * up[i]", "std::exp(-gate[i]))"),
 }
 
 
