@@ -222,6 +222,7 @@ def config_of(wl, args):
     return {"workload": wl.name, "batch": wl.batch, "seq": wl.seq, "hidden": wl.hidden,
             "heads": wl.heads, "head_dim": wl.head_dim, "ffn": wl.ffn, "window": wl.window,
             "layers": wl.layers, "weight_std": wl.weight_std,
+            "block": "RMSNorm + SwiGLU" if getattr(wl, "variant", 0) == 1 else "LayerNorm + GeLU",
             "parallelism": f"replicas x{args.gpus} (no collective on the data path)",
             "l2": "inputs larger than L2 (weights alone exceed the 129 MB L2)"}
 
@@ -387,7 +388,8 @@ def main():
     peaks, peak_src = load_peaks()
     launches = args.steps * wl.layers
     g1_ms = per_kernel[1] / launches
-    g1_flops = 2 * wl.tokens * wl.hidden * (3 * wl.hidden + wl.ffn)
+    glu = getattr(wl, "variant", 0) == 1  # SwiGLU: the first GEMM also computes W_up
+    g1_flops = 2 * wl.tokens * wl.hidden * (3 * wl.hidden + (2 if glu else 1) * wl.ffn)
     achieved = g1_flops / (g1_ms / 1e3) / 1e12
     traffic = profiled_traffic(wl.name)
     roofline = {"kernel": "gemm_block_in (LN(x) [Wqkv | W1], GeLU epilogue)", "bound": "tensor",

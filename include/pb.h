@@ -68,16 +68,25 @@ typedef struct pb_dims {
   int32_t ffn;       /* F, width of the MLP (4H on the pages) */
   int32_t window;    /* w: key k is visible to query i iff 0 <= i - k < w */
   float ln_eps;      /* LayerNorm epsilon, inside the square root */
+  int32_t variant;   /* PB_BLOCK_LN_GELU (eq. (4) as written) or PB_BLOCK_RMS_SWIGLU */
 } pb_dims;
+
+/* Block variants. PB_BLOCK_RMS_SWIGLU replaces the LayerNorm by RMSNorm
+ * (x / sqrt(mean x^2 + eps) * gamma; ln_beta unused) and the GeLU MLP by SwiGLU,
+ * silu(z W_gate) * (z W_up) then W2: the fused "RMSNorm" and "SiLU + elementwise
+ * multiply" kernels of the MegaScale reading notes, section 1.3 (named there without a
+ * definition; the standard forms are used). */
+typedef enum pb_block_variant { PB_BLOCK_LN_GELU = 0, PB_BLOCK_RMS_SWIGLU = 1 } pb_block_variant;
 
 /*
  * Parameters of one block (device pointers, bf16). They are read only by pb_create,
  * which packs them into the workspace; they may be freed once the stream has passed
  * pb_create's work.
- *   ln_gamma, ln_beta : [H]
+ *   ln_gamma, ln_beta : [H]     (ln_beta unused, may be NULL, for PB_BLOCK_RMS_SWIGLU)
  *   wqkv              : [H, 3H]; columns [Q | K | V], head j of each owns columns
  *                       [j*dh, (j+1)*dh) of its H-wide block
- *   w1                : [H, F]    (first MLP linear, "A" of Y = GeLU(XA)B)
+ *   w1                : [H, F]    (first MLP linear, "A" of Y = GeLU(XA)B); for
+ *                       PB_BLOCK_RMS_SWIGLU [H, 2F] = [W_gate | W_up], and b1 is [2F]
  *   wo                : [H, H]    (attention output projection)
  *   w2                : [F, H]    (second MLP linear, "B")
  *   b_qkv [3H], b1 [F], b_o [H], b2 [H] : optional biases, NULL = none.
@@ -222,7 +231,8 @@ const char* pb_last_error_message(void);
 
 /* LayerNorm (the LN of eq. (4)): out[r,:] = (x[r,:] - mean) / sqrt(var + eps) * gamma
  * + beta, biased variance, fp32 statistics. x, out: [rows, H] bf16; gamma, beta: [H]
- * bf16. H % 8 == 0, H <= 16384. */
+ * bf16. H % 8 == 0, H <= 16384. beta == NULL gives RMSNorm instead (the fused kernel of
+ * section 1.3): out[r,:] = x[r,:] / sqrt(mean x^2 + eps) * gamma. */
 pb_status pb_layernorm(int64_t rows, int32_t H, const void* x, const void* gamma,
                        const void* beta, float eps, void* out, void* stream);
 

@@ -52,4 +52,4 @@ def host_params(params: dict) -> dict:
 
 def oracle_dims(wl) -> O.Dims:
     return O.Dims(wl.batch, wl.seq, wl.hidden, wl.heads, wl.head_dim, wl.ffn, wl.window,
-                  wl.ln_eps)
+                  wl.ln_eps, getattr(wl, "variant", 0))

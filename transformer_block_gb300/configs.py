@@ -25,6 +25,8 @@ class Workload:
     layers: int
     weight_std: float
     ln_eps: float = 1e-5
+    # 0: LayerNorm + GeLU MLP; 1: RMSNorm + SwiGLU MLP (w1 = [W_gate | W_up], [H, 2F])
+    variant: int = 0
 
     @property
     def tokens(self) -> int:
@@ -43,6 +45,11 @@ WORKLOADS = {
                                 0.006),
     "long-swa-32k": Workload("long-swa-32k", 1, 32768, 4096, 32, 128, 16384, 4096, 1, 0.02),
     "stack8-h5120": Workload("stack8-h5120", 2, 4096, 5120, 40, 128, 20480, 1024, 8, 0.01),
+    # RMSNorm + SwiGLU variants; F = 8H/3 keeps the MLP's weights and FLOPs equal to the
+    # GeLU block's with F = 4H
+    "tiny-swiglu": Workload("tiny-swiglu", 1, 128, 256, 4, 64, 704, 32, 1, 0.02, variant=1),
+    "gpt3-175b-layer-swiglu": Workload("gpt3-175b-layer-swiglu", 1, 2048, 12288, 96, 128, 32768,
+                                       2048, 1, 0.006, variant=1),
 }
 
 # The single-GPU workload the throughput figure is quoted on.

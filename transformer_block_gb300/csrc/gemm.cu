@@ -68,6 +68,27 @@ __device__ __forceinline__ void store_row32(void* dst, const float (&v)[32]) {
   }
 }
 
+template <bool F16>
+__device__ __forceinline__ void store_row16(void* dst, const float (&v)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint4 u;
+    if (F16) {
+      u.x = pack_f16x2(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack_f16x2(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack_f16x2(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack_f16x2(v[8 * q + 6], v[8 * q + 7]);
+    } else {
+      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    }
+    d[q] = u;
+  }
+}
+
 __device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]) {
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -104,6 +125,22 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
           ep.vt + (int64_t(b * ep.nh + head) * ep.dh + d0) * ep.seq_pad + s;
 #pragma unroll
       for (int i = 0; i < 32; ++i) dst[int64_t(i) * ep.seq_pad] = __float2bfloat16_rn(v[i]);
+    } else if (ep.glu) {
+      // [gate | up] of 16 MLP features -> silu(gate) * up, next to the attention output
+      // in the second GEMM's A operand
+      float o[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = v[i] / (1.0f + __expf(-v[i])) * v[16 + i];
+      const int64_t off = int64_t(row) * (H + ep.F) + H + (cc - 3 * H) / 2;
+      if (ep.act_f16) {
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bad |= !(fabsf(o[i]) <= kF16Max);
+        if (bad) report_range(ep.status);
+        store_row16<true>(static_cast<__half*>(ep.act) + off, o);
+      } else {
+        store_row16<false>(static_cast<__nv_bfloat16*>(ep.act) + off, o);
+      }
     } else {  // h -> GeLU(h), next to the attention output in the second GEMM's A operand
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);

@@ -13,6 +13,7 @@ constexpr int kLnMaxH = 16384;
 constexpr int kStatusRange = 7;  // == PB_ERR_RANGE
 // x: [rows, H] bf16 (x_f32 false) or fp32; out: bf16 (out_f16 false) or fp16. With fp16
 // output a value beyond the fp16 range records kStatusRange in *status (may be null).
+// beta == nullptr selects RMSNorm: x / sqrt(mean x^2 + eps) * gamma.
 cudaError_t launch_layernorm(int64_t rows, int H, const void* x, bool x_f32,
                              const __nv_bfloat16* gamma, const __nv_bfloat16* beta, float eps,
                              void* out, bool out_f16, int* status, cudaStream_t stream);
@@ -41,6 +42,9 @@ struct EpiParams {
   // [q | k | v | h]: 0 for the parallel block's one GEMM over [Wqkv | W1], 3H for a GEMM
   // over W1 alone (the serial block's MLP input projection).
   int col_base;
+  // SwiGLU: the h columns are [gate | up] interleaved in 16s (see launch_transpose); each
+  // 32-column block gives 16 outputs silu(gate) * up at act column H + (c - 3H) / 2.
+  bool glu;
   int H, F, S, nh, dh;
   int64_t seq_pad;
   __nv_bfloat16* qk;   // [T, 2H]
@@ -91,14 +95,18 @@ cudaError_t launch_swa(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 // ---------------------------------------------------------------- packing (pack.cu)
 // out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols; with out_f16 the bf16
 // value is converted to fp16 (kStatusRange in *status if it is beyond the fp16 range).
+// glu_F > 0 (cols == 2 glu_F): output row c takes input column 16t + i of the gate half
+// or of the up half, t = c / 32, i = c % 32 (< 16: gate, else up, i - 16) -- the SwiGLU
+// interleave of the first GEMM's B operand.
 cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
-                             void* out, int64_t ld_out, bool out_f16, int* status,
+                             void* out, int64_t ld_out, bool out_f16, int64_t glu_F, int* status,
                              cudaStream_t stream);
-// bias1[3H + F] = [b_qkv | b1] (0 where absent); bias2[H] = b_o + b2; bias_o[H] = b_o and
-// bias_2[H] = b2 apart (the serial block adds them in two different GEMMs).
+// bias1[3H + F] = [b_qkv | b1] (0 where absent; with glu b1 is [2F] and is interleaved like
+// W1's rows, bias1 [3H + 2F]); bias2[H] = b_o + b2; bias_o[H] = b_o and bias_2[H] = b2
+// apart (the serial block adds them in two different GEMMs).
 cudaError_t launch_bias_prep(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1,
                              const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
-                             float* bias1, float* bias2, float* bias_o, float* bias_2,
+                             bool glu, float* bias1, float* bias2, float* bias_o, float* bias_2,
                              cudaStream_t stream);
 
 // ---------------------------------------------------------------- self-test (gemm.cu)

@@ -60,7 +60,8 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-template <typename TIn, bool F16>
+// RMS: RMSNorm, x / sqrt(mean x^2 + eps) * gamma (no centring, no beta).
+template <typename TIn, bool F16, bool RMS>
 __global__ void __launch_bounds__(THREADS) layernorm_kernel(const TIn* __restrict__ x,
                                                             const __nv_bfloat16* __restrict__ gamma,
                                                             const __nv_bfloat16* __restrict__ beta,
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(THREADS) layernorm_kernel(const TIn* __restric
       for (int e = 0; e < 8; ++e) sum += v[i][e];
     }
   }
-  const float mean = block_sum(sum, red) / float(H);
+  const float mean = RMS ? 0.f : block_sum(sum, red) / float(H);
   float sq = 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -99,9 +100,9 @@ __global__ void __launch_bounds__(THREADS) layernorm_kernel(const TIn* __restric
   for (int i = 0; i < MAXV; ++i) {
     const int idx = threadIdx.x + i * THREADS;
     if (idx < nv) {
-      float g[8], b[8], o[8];
+      float g[8], b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, o[8];
       load8(gamma, idx, g);
-      load8(beta, idx, b);
+      if (!RMS) load8(beta, idx, b);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         o[e] = (v[i][e] - mean) * rstd * g[e] + b[e];
@@ -122,8 +123,12 @@ template <typename TIn, bool F16>
 cudaError_t launch_t(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
                      const __nv_bfloat16* beta, float eps, void* out, int* status,
                      cudaStream_t stream) {
-  layernorm_kernel<TIn, F16><<<unsigned(rows), THREADS, 0, stream>>>(
-      static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), H, eps, status);
+  if (beta == nullptr)
+    layernorm_kernel<TIn, F16, true><<<unsigned(rows), THREADS, 0, stream>>>(
+        static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), H, eps, status);
+  else
+    layernorm_kernel<TIn, F16, false><<<unsigned(rows), THREADS, 0, stream>>>(
+        static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), H, eps, status);
   return cudaGetLastError();
 }
 

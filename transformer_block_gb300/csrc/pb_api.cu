@@ -95,9 +95,19 @@ pb_status check_dims(const pb_dims* d) {
     return fail(PB_ERR_UNSUPPORTED, "hidden %d > %d", d->hidden, pb::kLnMaxH);
   const int64_t T = int64_t(d->batch) * d->seq;
   if (T >= (int64_t(1) << 31)) return fail(PB_ERR_UNSUPPORTED, "batch * seq >= 2^31");
-  if (int64_t(3) * d->hidden + d->ffn >= (int64_t(1) << 31))
-    return fail(PB_ERR_UNSUPPORTED, "3 * hidden + ffn >= 2^31");
+  if (int64_t(3) * d->hidden + 2 * int64_t(d->ffn) >= (int64_t(1) << 31))
+    return fail(PB_ERR_UNSUPPORTED, "3 * hidden + 2 * ffn >= 2^31");
+  if (d->variant != PB_BLOCK_LN_GELU && d->variant != PB_BLOCK_RMS_SWIGLU)
+    return fail(PB_ERR_INVALID_ARG, "variant %d is not a pb_block_variant", d->variant);
   return PB_OK;
+}
+
+bool is_glu(const pb_dims& d) { return d.variant == PB_BLOCK_RMS_SWIGLU; }
+
+// Output columns of the first GEMM / rows of W1cat: [q | k | v | h], h = F columns (GeLU)
+// or 2F (SwiGLU gate and up, interleaved).
+int64_t w1_rows(const pb_dims& d) {
+  return 3 * int64_t(d.hidden) + (is_glu(d) ? 2 : 1) * int64_t(d.ffn);
 }
 
 struct WsLayout {
@@ -111,11 +121,11 @@ WsLayout ws_layout(const pb_dims& d) {
   L.status = off;
   off = align_up(off + 256, 1024);
   L.w1cat = off;
-  off = align_up(off + (3 * H + F) * H * 2, 1024);
+  off = align_up(off + size_t(w1_rows(d)) * H * 2, 1024);
   L.w2cat = off;
   off = align_up(off + H * (H + F) * 2, 1024);
   L.bias1 = off;
-  off = align_up(off + (3 * H + F) * 4, 1024);
+  off = align_up(off + size_t(w1_rows(d)) * 4, 1024);
   L.bias2 = off;
   off = align_up(off + H * 4, 1024);
   L.bias_o = off;
@@ -263,9 +273,10 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], st) : cudaSuccess; };
   PB_CUDA(mark(0), "cudaEventRecord");
 
-  // 1. the shared LayerNorm
-  PB_CUDA(pb::launch_layernorm(T, H, x, x_f32, h->gamma, h->beta, d.ln_eps, xn, h->f16,
-                               h->status, st),
+  // 1. the shared LayerNorm (RMSNorm for the SwiGLU variant: no beta)
+  const bool glu = is_glu(d);
+  PB_CUDA(pb::launch_layernorm(T, H, x, x_f32, h->gamma, glu ? nullptr : h->beta, d.ln_eps, xn,
+                               h->f16, h->status, st),
           "layernorm launch");
   PB_CUDA(mark(1), "cudaEventRecord");
 
@@ -286,8 +297,9 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   e1.act = act;
   e1.act_f16 = h->f16;
   e1.bias = h->has_bias ? h->bias1 : nullptr;
-  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, h->tm_w1cat, T, 3 * H + F, H, e1,
-                          h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
+  e1.glu = glu;
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, h->tm_w1cat, T, int(w1_rows(d)), H,
+                          e1, h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
           "first GEMM launch");
   PB_CUDA(mark(2), "cudaEventRecord");
 
@@ -350,9 +362,10 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   uint8_t* w1c = static_cast<uint8_t*>(h->w1cat);
   uint8_t* w2c = static_cast<uint8_t*>(h->w2cat);
 
-  // 1. LN(x)
-  PB_CUDA(pb::launch_layernorm(T, H, x, false, h->gamma, h->beta, d.ln_eps, xn, h->f16,
-                               h->status, st),
+  // 1. LN(x) (RMSNorm for the SwiGLU variant)
+  const bool glu = is_glu(d);
+  PB_CUDA(pb::launch_layernorm(T, H, x, false, h->gamma, glu ? nullptr : h->beta, d.ln_eps, xn,
+                               h->f16, h->status, st),
           "layernorm launch");
   // 2. [q | k | v] = xn Wqkv (+ b_qkv): rows [0, 3H) of W1cat
   CUtensorMap tm_xn, tm_wqkv;
@@ -372,6 +385,7 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   e1.act = act;
   e1.act_f16 = h->f16;
   e1.bias = h->has_bias ? h->bias1 : nullptr;
+  e1.glu = glu;
   PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, tm_wqkv, T, 3 * H, H, e1, h->num_sms,
                           h->status, h->limit_ns, scratch + L.sk, st),
           "QKV GEMM launch");
@@ -408,18 +422,19 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
                           h->status, h->limit_ns, scratch + L.sk, st),
           "attention projection GEMM launch");
   // 5. LN'(h) -> xn
-  PB_CUDA(pb::launch_layernorm(T, H, hres, true, gamma2, beta2, d.ln_eps, xn, h->f16, h->status,
-                               st),
+  PB_CUDA(pb::launch_layernorm(T, H, hres, true, gamma2, glu ? nullptr : beta2, d.ln_eps, xn,
+                               h->f16, h->status, st),
           "second layernorm launch");
-  // 6. GeLU(LN'(h) W1 (+ b1)) -> act[:, H:H+F]: rows [3H, 3H + F) of W1cat, routed as the
-  // h columns of [q | k | v | h]
+  // 6. GeLU(LN'(h) W1 (+ b1)) (or SwiGLU) -> act[:, H:H+F]: rows [3H, 3H + F) of W1cat
+  // ([3H, 3H + 2F) for SwiGLU), routed as the h columns of [q | k | v | h]
+  const int n_h = int(w1_rows(d) - 3 * int64_t(H));
   CUtensorMap tm_w1;
-  s = make_map_2d(&tm_w1, w1c + 3 * size_t(H) * H * esz, F, H, H, box, h->f16);
+  s = make_map_2d(&tm_w1, w1c + 3 * size_t(H) * H * esz, n_h, H, H, box, h->f16);
   if (s != PB_OK) return s;
   EpiParams e3 = e1;
   e3.col_base = 3 * H;
   e3.bias = h->has_bias ? h->bias1 + 3 * size_t(H) : nullptr;
-  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, tm_w1, T, F, H, e3, h->num_sms,
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, tm_w1, T, n_h, H, e3, h->num_sms,
                           h->status, h->limit_ns, scratch + L.sk, st),
           "MLP input GEMM launch");
   // 7. y = h + GeLU(.) W2 (+ b2): A = act[:, H:H+F], columns [H, H + F) of W2cat
@@ -547,6 +562,7 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
   const void* req[6] = {w->ln_gamma, w->ln_beta, w->wqkv, w->w1, w->wo, w->w2};
   const char* names[6] = {"ln_gamma", "ln_beta", "wqkv", "w1", "wo", "w2"};
   for (int i = 0; i < 6; ++i) {
+    if (i == 1 && is_glu(*dims) && req[i] == nullptr) continue;  // RMSNorm has no beta
     if (req[i] == nullptr) return fail(PB_ERR_INVALID_ARG, "weights.%s is NULL", names[i]);
     if (!aligned(req[i], 16))
       return fail(PB_ERR_INVALID_ARG, "weights.%s is not 16-byte aligned", names[i]);
@@ -604,28 +620,33 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
     if (e_ != cudaSuccess) return cleanup(cuda_fail(e_, what)); \
   } while (0)
   PB_CUDA_H(cudaMemsetAsync(h->status, 0, 256, st), "cudaMemsetAsync(status)");
-  // W1cat rows [0, 3H) = Wqkv^T, rows [3H, 3H + F) = W1^T
+  // W1cat rows [0, 3H) = Wqkv^T, rows [3H, 3H + F) = W1^T (SwiGLU: rows [3H, 3H + 2F) =
+  // [W_gate | W_up]^T interleaved in groups of 16)
+  const bool glu = is_glu(*dims);
+  const int64_t w1_cols = glu ? 2 * F : F;
   uint8_t* w1c = static_cast<uint8_t*>(h->w1cat);
   uint8_t* w2c = static_cast<uint8_t*>(h->w2cat);
-  PB_CUDA_H(pb::launch_transpose(bf(w->wqkv), H, 3 * H, 3 * H, w1c, H, h->f16, h->status, st),
+  PB_CUDA_H(pb::launch_transpose(bf(w->wqkv), H, 3 * H, 3 * H, w1c, H, h->f16, 0, h->status, st),
             "pack Wqkv");
-  PB_CUDA_H(pb::launch_transpose(bf(w->w1), H, F, F, w1c + 3 * H * H * 2, H, h->f16, h->status,
-                                 st),
+  PB_CUDA_H(pb::launch_transpose(bf(w->w1), H, w1_cols, w1_cols, w1c + 3 * H * H * 2, H, h->f16,
+                                 glu ? F : 0, h->status, st),
             "pack W1");
   // W2cat columns [0, H) = Wo^T, columns [H, H + F) = W2^T
-  PB_CUDA_H(pb::launch_transpose(bf(w->wo), H, H, H, w2c, H + F, h->f16, h->status, st),
+  PB_CUDA_H(pb::launch_transpose(bf(w->wo), H, H, H, w2c, H + F, h->f16, 0, h->status, st),
             "pack Wo");
-  PB_CUDA_H(pb::launch_transpose(bf(w->w2), F, H, H, w2c + H * 2, H + F, h->f16, h->status, st),
+  PB_CUDA_H(pb::launch_transpose(bf(w->w2), F, H, H, w2c + H * 2, H + F, h->f16, 0, h->status,
+                                 st),
             "pack W2");
   PB_CUDA_H(pb::launch_bias_prep(bf(w->b_qkv), bf(w->b1), bf(w->b_o), bf(w->b2), int(H), int(F),
-                                 h->bias1, h->bias2, h->bias_o, h->bias_2, st),
+                                 glu, h->bias1, h->bias2, h->bias_o, h->bias_2, st),
             "bias prep");
   PB_CUDA_H(cudaMemcpyAsync(h->gamma, w->ln_gamma, H * 2, cudaMemcpyDeviceToDevice, st),
             "copy gamma");
-  PB_CUDA_H(cudaMemcpyAsync(h->beta, w->ln_beta, H * 2, cudaMemcpyDeviceToDevice, st),
-            "copy beta");
+  if (w->ln_beta != nullptr)
+    PB_CUDA_H(cudaMemcpyAsync(h->beta, w->ln_beta, H * 2, cudaMemcpyDeviceToDevice, st),
+              "copy beta");
 #undef PB_CUDA_H
-  s = make_map_2d(&h->tm_w1cat, h->w1cat, 3 * H + F, H, H, pb::kGemmBoxRows, h->f16);
+  s = make_map_2d(&h->tm_w1cat, h->w1cat, w1_rows(*dims), H, H, pb::kGemmBoxRows, h->f16);
   if (s == PB_OK) s = make_map_2d(&h->tm_w2cat, h->w2cat, H, H + F, H + F, pb::kGemmBoxRows, h->f16);
   if (s != PB_OK) return cleanup(s);
   *out = h;
@@ -667,7 +688,7 @@ pb_status pb_forward_serial(pb_handle* h, const void* x, void* y, const void* ln
   if (overlap(x, n, scratch, L.total) || overlap(y, n, scratch, L.total))
     return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
   const auto* g2 = ln2_gamma ? static_cast<const __nv_bfloat16*>(ln2_gamma) : h->gamma;
-  const auto* b2 = ln2_beta ? static_cast<const __nv_bfloat16*>(ln2_beta) : h->beta;
+  const auto* b2 = ln2_beta ? static_cast<const __nv_bfloat16*>(ln2_beta) : h->beta;  // unused by RMSNorm
   return run_serial(h, x, y, g2, b2, static_cast<uint8_t*>(scratch),
                     static_cast<cudaStream_t>(stream));
 }
@@ -789,10 +810,12 @@ pb_status pb_layernorm(int64_t rows, int32_t H, const void* x, const void* gamma
                 pb::kLnMaxH);
   if (rows >= (int64_t(1) << 31)) return fail(PB_ERR_UNSUPPORTED, "rows >= 2^31");
   if (!(eps > 0.f)) return fail(PB_ERR_INVALID_ARG, "eps must be > 0");
-  const void* ps[4] = {x, gamma, beta, out};
+  const void* ps[3] = {x, gamma, out};
   for (const void* p : ps)
     if (p == nullptr || !aligned(p, 16))
       return fail(PB_ERR_INVALID_ARG, "pointers must be 16-byte aligned device pointers");
+  if (beta != nullptr && !aligned(beta, 16))
+    return fail(PB_ERR_INVALID_ARG, "beta must be 16-byte aligned (or NULL for RMSNorm)");
   PB_CUDA(pb::launch_layernorm(rows, H, x, false, static_cast<const __nv_bfloat16*>(gamma),
                                static_cast<const __nv_bfloat16*>(beta), eps, out, false, nullptr,
                                static_cast<cudaStream_t>(stream)),

@@ -21,9 +21,11 @@ def windowed_pairs(seq: int, window: int) -> int:
 
 
 def gemm_flops(wl: Workload) -> int:
-    """Per layer: 2 * tokens * (Wq, Wk, Wv, Wo: 4 H^2  +  W1, W2: 2 H F)."""
+    """Per layer: 2 * tokens * (Wq, Wk, Wv, Wo: 4 H^2  +  W1, W2: 2 H F); the SwiGLU
+    variant has W_gate, W_up, W2: 3 H F."""
     H, F = wl.hidden, wl.ffn
-    return 2 * wl.tokens * (4 * H * H + 2 * H * F)
+    mlp = 3 if getattr(wl, "variant", 0) == 1 else 2
+    return 2 * wl.tokens * (4 * H * H + mlp * H * F)
 
 
 def attention_flops(wl: Workload) -> int:

@@ -5,7 +5,8 @@ is drawn in float32 from ``torch.randn`` on a generator seeded with
 ``seed * 1000 + layer`` and rounded to bf16 (round to nearest even), so both sides
 consume identical bf16 values. Draw order per layer stream: ``x`` (layer 0 only), then
 ``ln_gamma = 1 + 0.1 N``, ``ln_beta = 0.1 N``, ``Wq, Wk, Wv, W1, Wo, W2 = std * N``
-(``[in, out]`` layout), then, if requested, the biases ``b_qkv, b1, b_o, b2 = 0.02 N``,
+(``[in, out]`` layout; for the RMSNorm + SwiGLU variant W1 is ``[H, 2F]`` = gate | up and
+``ln_beta`` is drawn but unused), then, if requested, the biases ``b_qkv, b1, b_o, b2 = 0.02 N``,
 then, if requested, a second LayerNorm ``ln2_gamma = 1 + 0.1 N``, ``ln2_beta = 0.1 N`` (the
 serial block's). ``x ~ N(0, 1)``.
 """
@@ -47,12 +48,13 @@ def make_layer(wl: Workload, layer: int = 0, seed: int = 0, device="cpu", biases
     wv = _draw(g, (H, H), device, wl.weight_std)
     p["wqkv"] = torch.cat([wq, wk, wv], dim=1).contiguous()
     del wq, wk, wv
-    p["w1"] = _draw(g, (H, F), device, wl.weight_std)
+    glu = getattr(wl, "variant", 0) == 1  # SwiGLU: w1 = [W_gate | W_up]
+    p["w1"] = _draw(g, (H, 2 * F if glu else F), device, wl.weight_std)
     p["wo"] = _draw(g, (H, H), device, wl.weight_std)
     p["w2"] = _draw(g, (F, H), device, wl.weight_std)
     if biases:
         p["b_qkv"] = _draw(g, (3 * H,), device, 0.02)
-        p["b1"] = _draw(g, (F,), device, 0.02)
+        p["b1"] = _draw(g, (2 * F if glu else F,), device, 0.02)
         p["b_o"] = _draw(g, (H,), device, 0.02)
         p["b2"] = _draw(g, (H,), device, 0.02)
     if ln2:

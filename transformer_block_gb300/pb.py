@@ -33,7 +33,8 @@ class PbError(RuntimeError):
 class pb_dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("seq", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
-                ("window", ctypes.c_int32), ("ln_eps", ctypes.c_float)]
+                ("window", ctypes.c_int32), ("ln_eps", ctypes.c_float),
+                ("variant", ctypes.c_int32)]
 
 
 WEIGHT_FIELDS = ["ln_gamma", "ln_beta", "wqkv", "w1", "wo", "w2", "b_qkv", "b1", "b_o", "b2"]
@@ -128,7 +129,8 @@ def make_dims(wl: Workload | None = None, **kw) -> pb_dims:
     src = dict(wl.__dict__) if wl is not None else {}
     src.update(kw)
     return pb_dims(src["batch"], src["seq"], src["hidden"], src["heads"], src["head_dim"],
-                   src["ffn"], src["window"], float(src.get("ln_eps", 1e-5)))
+                   src["ffn"], src["window"], float(src.get("ln_eps", 1e-5)),
+                   int(src.get("variant", 0)))
 
 
 def weight_workspace_bytes(dims: pb_dims) -> int:
