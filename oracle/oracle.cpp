@@ -146,6 +146,63 @@ void oracle_swiglu(int64_t n, const double* gate, const double* up, double* out,
   });
 }
 
+// FP8 E4M3 (the "E4M3" format of the performance notes, "BF16 / FP16 / FP8": 1 sign bit,
+// 4 exponent bits with bias 7, 3 mantissa bits; no infinities; largest finite 448 =
+// 1.75 * 2^8; smallest normal 2^-6; subnormals m * 2^-9, m = 1..7). Rounds v to the
+// nearest representable value, ties to the even mantissa, and saturates at +-448.
+// Returns the 8-bit code; *value gets the decoded value.
+static uint8_t e4m3_round(double v, double* value) {
+  const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+  double a = std::fabs(v);
+  if (std::isnan(v)) a = 0.0;  // never produced by the callers below
+  uint8_t code;
+  double q;
+  if (a < std::ldexp(1.0, -6)) {
+    // subnormal grid, step 2^-9 (m = 8 reaches the smallest normal, code 0x08)
+    const double m = std::nearbyint(a * 512.0);  // round half to even (default mode)
+    q = m / 512.0;
+    code = uint8_t(m);  // m in 0..8; 8 encodes exponent 1, mantissa 0
+  } else {
+    int e;
+    std::frexp(a, &e);   // a = f * 2^e, f in [0.5, 1)
+    const int ex = e - 1;  // a in [2^ex, 2^(ex+1))
+    const double step = std::ldexp(1.0, ex - 3);
+    q = std::nearbyint(a / step) * step;  // may reach 2^(ex+1): still representable
+    if (q > 448.0) q = 448.0;
+    int qe;
+    const double qf = std::frexp(q, &qe);  // q = qf * 2^qe
+    const int E = qe - 1;                  // q in [2^E, 2^(E+1))
+    const int mant = int(std::nearbyint((qf * 2.0 - 1.0) * 8.0));
+    code = uint8_t(((E + 7) << 3) | mant);
+  }
+  *value = sign ? -q : q;
+  return uint8_t(sign | code);
+}
+
+// Per-row current scaling to E4M3, the same fp32 steps as the GPU quantizer:
+//   amax = max_c |float(x[r,c])|,  inv = 448.0f / amax,  s[r] = amax / 448.0f   (fp32)
+//   code[r,c] = e4m3(float(x[r,c]) * inv),  deq[r,c] = e4m3 value * s[r]
+// (amax = 0: inv = s = 0, codes 0). deq may be NULL.
+void oracle_quantize_e4m3_rows(int64_t rows, int64_t cols, const double* x, uint8_t* codes,
+                               float* scales, double* deq, int threads) {
+  for_row_ranges(rows, threads, [=](int64_t r0, int64_t r1) {
+    for (int64_t r = r0; r < r1; ++r) {
+      const double* xr = x + r * cols;
+      float amax = 0.0f;
+      for (int64_t c = 0; c < cols; ++c) amax = std::max(amax, std::fabs(float(xr[c])));
+      const float inv = amax > 0.0f ? 448.0f / amax : 0.0f;
+      const float s = amax / 448.0f;
+      scales[r] = s;
+      for (int64_t c = 0; c < cols; ++c) {
+        const float t = float(xr[c]) * inv;
+        double q;
+        codes[r * cols + c] = e4m3_round(double(t), &q);
+        if (deq) deq[r * cols + c] = q * double(s);
+      }
+    }
+  });
+}
+
 // Sliding-window causal multi-head attention for ONE sequence (eqs. (5)-(6): each token
 // attends only to the most recent w tokens, itself included).
 //

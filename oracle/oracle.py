@@ -25,6 +25,9 @@ Two further block forms, on the same primitives:
   the standard forms are taken: ``x / sqrt(mean x^2 + eps) * gamma`` and
   ``silu(x W_gate) * (x W_up)``, ``w1 = [W_gate | W_up]``).
 * ``serial_block_forward``: the standard block of eq. (3), for comparison.
+* ``block_forward(fp8=True)``: both GEMMs on FP8 E4M3 operands with per-row current
+  scaling (the performance notes' FP8 recipe), the quantizer's fp32 steps in
+  ``oracle_quantize_e4m3_rows`` (E4M3 rounding written from the format definition).
 
 All arithmetic is float64 in oracle.cpp (built here with g++); inputs are the exact
 bf16 values the GPU receives, passed as float32/float64 arrays.
@@ -76,8 +79,9 @@ def _bind(lib):
     lib.oracle_add3.argtypes = [i64, d, d, d, d]
     lib.oracle_rmsnorm.argtypes = [i64, i64, d, d, ctypes.c_double, d, i32]
     lib.oracle_swiglu.argtypes = [i64, d, d, d, i32]
+    lib.oracle_quantize_e4m3_rows.argtypes = [i64, i64, d, d, d, d, i32]
     for f in ("oracle_layernorm", "oracle_linear", "oracle_gelu", "oracle_swa_attention",
-              "oracle_add3", "oracle_rmsnorm", "oracle_swiglu"):
+              "oracle_add3", "oracle_rmsnorm", "oracle_swiglu", "oracle_quantize_e4m3_rows"):
         getattr(lib, f).restype = None
     return lib
 
@@ -149,6 +153,26 @@ def swiglu(gate, up, threads=0, lib=None) -> np.ndarray:
     return out
 
 
+def quantize_e4m3_rows(x, threads=0, lib=None):
+    """Per-row current scaling to FP8 E4M3 with the quantizer's fp32 steps (oracle.cpp):
+    returns ``(codes uint8 [rows, cols], scales float32 [rows], dequantized float64)``."""
+    lib = lib or load()
+    x = _f64(x)
+    rows, cols = x.shape
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    scales = np.empty(rows, dtype=np.float32)
+    deq = np.empty_like(x)
+    lib.oracle_quantize_e4m3_rows(rows, cols, _ptr(x), codes.ctypes.data_as(ctypes.c_void_p),
+                                  scales.ctypes.data_as(ctypes.c_void_p), _ptr(deq), threads)
+    return codes, scales, deq
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round to bf16 (nearest even) and back: the storage of a 16-bit intermediate."""
+    import torch
+    return torch.from_numpy(_f64(x)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
 def _norm(dims, x, gamma, beta, threads, lib):
     """The block's normalisation: LayerNorm (variant 0) or RMSNorm (variant 1, no beta)."""
     if dims.variant == 1:
@@ -207,7 +231,7 @@ def _param(params, name):
 
 
 def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads: int = 0,
-                  keep_stages: bool = False, lib=None):
+                  keep_stages: bool = False, lib=None, fp8: bool = False):
     """One parallel transformer block (eq. (4)) in float64.
 
     ``x``: ``[B, S, H]``; ``params``: ``ln_gamma, ln_beta [H]``, ``wqkv [H, 3H]``,
@@ -220,6 +244,14 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
     ``rows=None`` returns ``y [B, S, H]``. ``rows={b: positions}`` returns only those
     output rows, ``[sum_b len(positions), H]``, ordered by ``b`` then position.
     ``keep_stages=True`` also returns the intermediates of step 1-4 for the same rows.
+
+    ``fp8=True``: both GEMMs take FP8 E4M3 operands with per-row current scaling (the
+    performance notes' FP8 recipe, "BF16 / FP16 / FP8": E4M3 for the forward pass, only the
+    GEMMs in FP8). The operands are quantized where the fused path quantizes them and from
+    the precision it holds them in: LN(x) rows (the quantizer casts to fp32), the output
+    channels of [Wqkv | W1] and of [Wo ; W2] (bf16 weights), and the rows of
+    [attn | GeLU(h)] after rounding to bf16 (how that intermediate is stored). Everything
+    else stays float64.
     """
     lib = lib or load()
     B, S, H = dims.batch, dims.seq, dims.hidden
@@ -260,11 +292,20 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
     sel = np.concatenate(sel) if sel else np.zeros(0, dtype=np.int64)
     xn_q = xn_cone[sel]
 
+    w1 = params["w1"]
+    if fp8:
+        # one scale per output channel of [Wqkv | W1] and per row of LN(x)
+        w1cat = np.concatenate([_f64(wqkv), _f64(w1)], axis=1)
+        w1cat = quantize_e4m3_rows(w1cat.T, threads, lib)[2].T
+        wqkv, w1 = w1cat[:, :3 * H], w1cat[:, 3 * H:]
+        xn_cone = quantize_e4m3_rows(xn_cone, threads, lib)[2]
+        xn_q = xn_cone[sel]
+
     # 2. four separate projections
     q = linear(xn_q, wqkv[:, 0:H], bq, threads, lib)
     k = linear(xn_cone, wqkv[:, H:2 * H], bk, threads, lib)
     v = linear(xn_cone, wqkv[:, 2 * H:3 * H], bv, threads, lib)
-    h = linear(xn_q, params["w1"], _param(params, "b1"), threads, lib)
+    h = linear(xn_q, w1, _param(params, "b1"), threads, lib)
 
     # 3. sliding-window attention, per sequence
     attn = np.empty_like(q)
@@ -278,8 +319,19 @@ def block_forward(dims: Dims, x, params: dict, rows: dict | None = None, threads
 
     # 4. the two output projections
     g = _mlp_act(dims, h, threads, lib)
-    mlp = linear(g, params["w2"], _param(params, "b2"), threads, lib)
-    att = linear(attn, params["wo"], _param(params, "b_o"), threads, lib)
+    wo, w2 = params["wo"], params["w2"]
+    if fp8:
+        # one scale per row of [attn | act(h)] (stored as bf16) and per output channel of
+        # [Wo ; W2]
+        act = quantize_e4m3_rows(round_bf16(np.concatenate([attn, g], axis=1)), threads, lib)[2]
+        attn_in, g_in = act[:, :H], act[:, H:]
+        w2cat = quantize_e4m3_rows(np.concatenate([_f64(wo), _f64(w2)], axis=0).T, threads,
+                                   lib)[2].T
+        wo, w2 = w2cat[:H], w2cat[H:]
+    else:
+        attn_in, g_in = attn, g
+    mlp = linear(g_in, w2, _param(params, "b2"), threads, lib)
+    att = linear(attn_in, wo, _param(params, "b_o"), threads, lib)
 
     # 5. residual sum of the three terms of eq. (4)
     xq = _f64(np.concatenate([x[b][want[b]] for b in want]) if want else np.zeros((0, H)))

@@ -17,6 +17,10 @@ What pins what:
 * RMSNorm + SwiGLU (the fused kernels of section 1.3): closed forms (constant rows,
   sigmoid(ln 3) = 3/4), torch ``rms_norm`` / ``silu``, RMSNorm's scale invariance, and
   the variant block restated with torch routines;
+* FP8 E4M3 with per-row current scaling: the code table of the format definition, a
+  round trip of every code through an independent decoder, ties to even, torch's
+  ``float8_e4m3fn`` casts, the per-row scale invariants, and the FP8 block restated with
+  torch;
 * the serial block of eq. (3): restated with torch routines, equal to the parallel
   block when either branch's output weight is zero, and first-order in the attention
   term when compared with the parallel block.
@@ -520,6 +524,131 @@ def pin_block_swiglu_rows_mode(lib):
     return _close(part, np.concatenate([full[b][rows[b]] for b in (0, 1)]), 1e-13)
 
 
+# ----------------------------------------------------------------------------- FP8 E4M3
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of an E4M3 code from the format definition (sign, 4 exponent bits with bias 7,
+    3 mantissa bits; exponent field 0 is subnormal: m * 2^-9)."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0:
+        return sign * m * 2.0 ** -9
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def _q1(values, lib):
+    """Quantize values with a unit scale: each row gets 448 as its amax."""
+    v = np.asarray(values, dtype=np.float64)
+    x = np.stack([v, np.full_like(v, 448.0)], axis=1)
+    codes, scales, deq = O.quantize_e4m3_rows(x, lib=lib)
+    assert np.all(scales == 1.0)
+    return codes[:, 0], deq[:, 0]
+
+
+def pin_e4m3_table(lib):
+    table = {448.0: 0x7E, 1.0: 0x38, 0.5: 0x30, 2.0 ** -6: 0x08, 2.0 ** -9: 0x01,
+             7 * 2.0 ** -9: 0x07, 240.0: 0x77, 1.125: 0x39, -1.0: 0xB8, 0.0: 0x00, -2.0: 0xC0}
+    codes, _ = _q1(list(table), lib)
+    want = np.array(list(table.values()), dtype=np.uint8)
+    return bool(np.array_equal(codes, want)), f"codes {codes.tolist()} want {want.tolist()}"
+
+
+def pin_e4m3_roundtrip_all_codes(lib):
+    codes = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    vals = [e4m3_decode(c) for c in codes]
+    got, deq = _q1(vals, lib)
+    # -0 (0x80) decodes to -0.0 and keeps its sign
+    want = np.array(codes, dtype=np.uint8)
+    ok = bool(np.array_equal(got, want)) and bool(np.array_equal(deq, np.array(vals)))
+    return ok, f"{int(np.sum(got != want))} codes differ"
+
+
+def pin_e4m3_ties_to_even(lib):
+    # halfway cases: 1.0625 between 1.0 (m 0) and 1.125 (m 1) -> 1.0; 1.1875 -> 1.25 (m 2);
+    # 3 * 2^-10 between 2^-9 (m 1) and 2^-8 (m 2) -> 2^-8; 27 * 2^-5 -> 0.875 (m 6)
+    vals = [1.0625, 1.1875, 3 * 2.0 ** -10, 29 * 2.0 ** -5, -1.0625]
+    want = [1.0, 1.25, 2.0 ** -8, 0.875, -1.0]
+    _, deq = _q1(vals, lib)
+    return bool(np.array_equal(deq, np.array(want))), f"{deq.tolist()} want {want}"
+
+
+def pin_e4m3_library(lib):
+    v = _rng(220).normal(0, 60, 4000).clip(-448, 448)
+    v = np.concatenate([v, _rng(221).normal(0, 0.01, 1000)])
+    codes, _ = _q1(v, lib)
+    want = torch.from_numpy(v).to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+    want = want.numpy()
+    # torch keeps the sign of a negative value that rounds to zero (0x80); so does the oracle
+    return bool(np.array_equal(codes, want)), f"{int(np.sum(codes != want))} differ"
+
+
+def pin_e4m3_row_scaling(lib):
+    # each row's largest magnitude maps to +-448 exactly (scale amax / 448 in fp32), the
+    # dequantized value is within half an E4M3 step of the input, and all-zero rows stay 0
+    x = _rng(222).normal(0, 3, size=(6, 40))
+    x[3] = 0.0
+    codes, scales, deq = O.quantize_e4m3_rows(x, lib=lib)
+    amax = np.abs(x.astype(np.float32)).max(axis=1)
+    ok = bool(np.array_equal(scales, (amax / np.float32(448.0)).astype(np.float32)))
+    big = np.abs(np.array([[e4m3_decode(int(c)) for c in r] for r in codes])).max(axis=1)
+    ok &= bool(np.all(big[[0, 1, 2, 4, 5]] == 448.0)) and bool(np.all(codes[3] == 0))
+    rel = np.abs(deq - x) / np.maximum(np.maximum(np.abs(x), 2.0 ** -6 * scales[:, None]),
+                                       1e-300)
+    ok &= bool(np.all(rel <= 2.0 ** -4 + 1e-6))
+    return ok, f"max relative error {rel.max():.3e}"
+
+
+def torch_block_fp8(dims, x, p):
+    """The FP8 block restated with torch: float8_e4m3fn casts with per-row fp32 scales."""
+    B, S, H, nh, dh = dims.batch, dims.seq, dims.hidden, dims.heads, dims.head_dim
+    T64 = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+
+    def q(a):  # rows of a (float64 tensor) -> dequantized float64
+        a32 = a.to(torch.float32)
+        amax = a32.abs().amax(dim=1, keepdim=True)
+        inv = torch.where(amax > 0, torch.tensor(448.0, dtype=torch.float32) / amax,
+                          torch.zeros_like(amax))
+        codes = (a32 * inv).to(torch.float8_e4m3fn)
+        return codes.to(torch.float64) * (amax / 448.0).to(torch.float64)
+
+    X = T64(x).reshape(B * S, H)
+    xn = q(F.layer_norm(X, (H,), T64(p["ln_gamma"]), T64(p["ln_beta"]), dims.ln_eps))
+    w1cat = q(torch.cat([T64(p["wqkv"]), T64(p["w1"])], dim=1).T).T
+    z = xn @ w1cat
+    qkv, h = z[:, :3 * H], z[:, 3 * H:]
+    q4, k4, v4 = (qkv[:, i * H:(i + 1) * H].reshape(B, S, nh, dh).transpose(1, 2) for i in range(3))
+    a = F.scaled_dot_product_attention(q4, k4, v4, attn_mask=band_mask(S, dims.window))
+    a = a.transpose(1, 2).reshape(B * S, H)
+    act = torch.cat([a, F.gelu(h, approximate="none")], dim=1)
+    act = q(act.to(torch.bfloat16).to(torch.float64))
+    w2cat = q(torch.cat([T64(p["wo"]), T64(p["w2"])], dim=0).T).T
+    return (X + act @ w2cat).reshape(B, S, H).numpy()
+
+
+def pin_block_fp8_library(lib):
+    ok, detail = True, []
+    for w in (2, 9):
+        dims = O.Dims(2, 12, 16, 4, 4, 32, w)
+        p = tiny_params(16, 4, 32, seed=230 + w, biases=False)
+        x = _rng(240 + w).normal(size=(2, 12, 16))
+        o, d = _close(O.block_forward(dims, x, p, lib=lib, fp8=True), torch_block_fp8(dims, x, p),
+                      1e-9)
+        ok &= o
+        detail.append(f"w={w}: {d}")
+    return ok, "; ".join(detail)
+
+
+def pin_block_fp8_rows_mode(lib):
+    dims = O.Dims(2, 30, 16, 4, 4, 32, 6)
+    p = tiny_params(16, 4, 32, seed=250)
+    x = _rng(251).normal(size=(2, 30, 16))
+    full = O.block_forward(dims, x, p, lib=lib, fp8=True)
+    rows = {0: [0, 29], 1: [4, 5, 17]}
+    part = O.block_forward(dims, x, p, rows=rows, lib=lib, fp8=True)
+    return _close(part, np.concatenate([full[b][rows[b]] for b in (0, 1)]), 1e-13)
+
+
 ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_layernorm_library,
             pin_layernorm_stats, pin_linear_library, pin_attention_window1_is_v,
             pin_attention_window2_closed_form, pin_attention_full_causal,
@@ -529,4 +658,7 @@ ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_laye
             pin_block_rows_mode, pin_serial_library, pin_serial_reduces_to_parallel,
             pin_serial_first_order, pin_serial_rows_mode, pin_rmsnorm_closed_form,
             pin_rmsnorm_library, pin_rmsnorm_scale_invariance, pin_swiglu_closed_form,
-            pin_swiglu_library, pin_block_swiglu_library, pin_block_swiglu_rows_mode]
+            pin_swiglu_library, pin_block_swiglu_library, pin_block_swiglu_rows_mode,
+            pin_e4m3_table, pin_e4m3_roundtrip_all_codes, pin_e4m3_ties_to_even,
+            pin_e4m3_library, pin_e4m3_row_scaling, pin_block_fp8_library,
+            pin_block_fp8_rows_mode]

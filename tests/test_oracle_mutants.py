@@ -33,6 +33,11 @@ MUTANTS = {
     "rms_no_gamma": ("o[c] = xr[c] * inv * gamma[c]", "o[c] = xr[c] * inv"),
     "silu_sign": ("(1.0 + std::exp(-gate[i]))", "(1.0 + std::exp(gate[i]))"),
     "swiglu_drops_up": ("std::exp(-gate[i])) * up[i]", "std::exp(-gate[i]))"),
+    "e4m3_ties_away": ("q = std::nearbyint(a / step) * step;", "q = std::round(a / step) * step;"),
+    "e4m3_subnormal_step": ("std::nearbyint(a * 512.0)", "std::nearbyint(a * 256.0)"),
+    "e4m3_bias_8": ("code = uint8_t(((E + 7) << 3) | mant);", "code = uint8_t(((E + 8) << 3) | mant);"),
+    "e4m3_two_mantissa_bits": ("std::ldexp(1.0, ex - 3)", "std::ldexp(1.0, ex - 2)"),
+    "e4m3_scale_inverted": ("const float s = amax / 448.0f;", "const float s = 448.0f / amax;"),
 }
 
 
