@@ -54,6 +54,9 @@ def parse():
                     help="instead of the contract line, time the parallel block (eq. (4)) and "
                          "the serial block (eq. (3)) on the same weights, one GPU, and print "
                          "one JSON line with both")
+    ap.add_argument("--operands", default="bf16", choices=["bf16", "fp16", "fp8"],
+                    help="operand type of the GEMMs (fp8: E4M3 with per-row / per-channel "
+                         "current scaling, not the reference precision)")
     ap.add_argument("--cpu-rows", type=int, default=192,
                     help="tokens of the oracle's CPU-baseline sample")
     return ap.parse_args()
@@ -223,6 +226,7 @@ def config_of(wl, args):
             "heads": wl.heads, "head_dim": wl.head_dim, "ffn": wl.ffn, "window": wl.window,
             "layers": wl.layers, "weight_std": wl.weight_std,
             "block": "RMSNorm + SwiGLU" if getattr(wl, "variant", 0) == 1 else "LayerNorm + GeLU",
+            "gemm_operands": getattr(args, "operands", "bf16"),
             "parallelism": f"replicas x{args.gpus} (no collective on the data path)",
             "l2": "inputs larger than L2 (weights alone exceed the 129 MB L2)"}
 
@@ -311,7 +315,9 @@ def main():
     # Inputs (seeded, synthetic, on the device) and one handle per layer.
     x, layers = inputs.make_stack(wl, seed=rank, device="cuda")
     dims = pb.make_dims(wl)
-    blocks = [pb.ParallelBlock(dims, p) for p in layers]
+    operands = {"bf16": pb.PB_OPERANDS_BF16, "fp16": pb.PB_OPERANDS_FP16,
+                "fp8": pb.PB_OPERANDS_FP8}[args.operands]
+    blocks = [pb.ParallelBlock(dims, p, operand_precision=operands) for p in layers]
     del layers
     torch.cuda.empty_cache()
     scratch = pb.new_scratch(dims)
@@ -391,12 +397,15 @@ def main():
     glu = getattr(wl, "variant", 0) == 1  # SwiGLU: the first GEMM also computes W_up
     g1_flops = 2 * wl.tokens * wl.hidden * (3 * wl.hidden + (2 if glu else 1) * wl.ffn)
     achieved = g1_flops / (g1_ms / 1e3) / 1e12
-    traffic = profiled_traffic(wl.name)
+    # FP8 operands: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+    ratio = 2.0 if args.operands == "fp8" else 1.0
+    traffic = profiled_traffic(wl.name) if args.operands == "bf16" else None
     roofline = {"kernel": "gemm_block_in (LN(x) [Wqkv | W1], GeLU epilogue)", "bound": "tensor",
-                "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
-                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "achieved": achieved, "peak": peaks["bf16_tflops"] * ratio, "unit": "TFLOP/s",
+                "frac": achieved / (peaks["bf16_tflops"] * ratio), "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)"
+                               + (" x 2 (nominal fp8 / bf16)" if ratio != 1.0 else ""),
+                "frac_of_sustained": achieved / (peaks["bf16_tflops_sustained"] * ratio),
                 "algorithmic_flops_per_launch": g1_flops, "ms_per_launch": g1_ms}
     step_ms = ms / args.steps
     kernels = {}
@@ -422,7 +431,8 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"bf16": "bf16", "fp16": "fp16", "fp8": "e4m3"}[args.operands],
             "data": "synthetic (seeded N(0,1) activations, N(0, std) weights)",
             "config": config_of(wl, args),
             "mfu": {"vs_spec_dense_bf16": value / world / SPEC_BF16_TFLOPS,
@@ -432,7 +442,8 @@ def main():
             "model_flops_per_step": model * world,
             "kernels": kernels,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * wl.layers * args.steps, "clocks": clk}
+            "gpu_launches": (5 if args.operands == "fp8" else 4) * wl.layers * args.steps,
+            "clocks": clk}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -110,6 +110,7 @@ typedef struct pb_weights {
  *   qk   [T, 2H]         [q | k], head-major columns (bf16)
  *   vt   [batch, heads, dh, seq_pad] v transposed per head, seq_pad = seq rounded up to 8
  *   act  [T, H + F]      [attention output (before Wo) | GeLU(h)]  (bf16 / fp16)
+ *   q8, qscale           the FP8 operands of PB_OPERANDS_FP8 (see the fields)
  *   io   [T, H]          bf16 staging of the host-buffer entry point
  *   res0, res1 [T, H]    fp32 residual stream between the layers of a stack
  *   sk                   stream-K partial tiles (fp32) and flags of the two GEMMs
@@ -123,6 +124,8 @@ typedef struct pb_scratch_layout {
   size_t res0;
   size_t res1;
   size_t sk;  /* stream-K partial tiles and flags of the GEMMs */
+  size_t q8;      /* PB_OPERANDS_FP8: [T, H + F] E4M3 codes of act (xn holds LN(x)'s codes) */
+  size_t qscale;  /* PB_OPERANDS_FP8: [2T] fp32 row scales of LN(x), then of act */
   size_t seq_pad;
   size_t total;
 } pb_scratch_layout;
@@ -132,10 +135,19 @@ typedef struct pb_scratch_layout {
  * "BF16 / FP16 / FP8"), which is the default. PB_OPERANDS_FP16 stores LN(x), the packed
  * weights, the attention output and GeLU(h) as fp16 instead: the same 16 bits and the
  * same tensor-core rate, 3 more mantissa bits, and a range limit of 65504 that the
- * kernels check (PB_ERR_RANGE). Attention (q, k, v, P) stays bf16 in both modes. */
+ * kernels check (PB_ERR_RANGE). Attention (q, k, v, P) stays bf16 in both modes.
+ * PB_OPERANDS_FP8 runs both GEMMs on FP8 E4M3 operands (the performance notes' FP8
+ * recipe: E4M3 for the forward pass, only the GEMMs in FP8, LayerNorm, softmax and the
+ * residual in bf16 / fp32) with current scaling per row: each row of LN(x) and of
+ * [attention output | GeLU(h)], and each output channel of the packed weights, is scaled
+ * by 448 / its largest magnitude; the GEMM epilogue multiplies the fp32 sum back by both
+ * scales. Needs H and H + F to be multiples of 128; pb_forward_serial does not support it.
+ * Not the reference precision: its results differ from the bf16 path by the E4M3 rounding
+ * (3 mantissa bits). */
 typedef enum pb_operand_precision {
   PB_OPERANDS_BF16 = 0,
-  PB_OPERANDS_FP16 = 1
+  PB_OPERANDS_FP16 = 1,
+  PB_OPERANDS_FP8 = 2
 } pb_operand_precision;
 
 typedef struct pb_options {
@@ -228,6 +240,15 @@ const char* pb_last_error_message(void);
 /* ------------------------------------------------------------------------------------
  * Single steps of the block, exported for testing and reuse. Same conventions.
  * ---------------------------------------------------------------------------------- */
+
+/* Per-row current scaling of a bf16 [rows, cols] matrix to FP8 E4M3, the quantizer of
+ * PB_OPERANDS_FP8 (performance notes, "BF16 / FP16 / FP8"), in fixed fp32 steps:
+ * amax = max |x[r,:]|, inv = 448 / amax (0 if amax = 0), scales[r] = amax / 448,
+ * codes[r,c] = E4M3(x[r,c] * inv) rounded to nearest even and saturated at +-448.
+ * x: device bf16 [rows, cols], codes: device [rows, cols] bytes, scales: device fp32
+ * [rows]; cols % 8 == 0, pointers 16-byte aligned. */
+pb_status pb_quantize_rows_e4m3(int64_t rows, int32_t cols, const void* x, void* codes,
+                                void* scales, void* stream);
 
 /* LayerNorm (the LN of eq. (4)): out[r,:] = (x[r,:] - mean) / sqrt(var + eps) * gamma
  * + beta, biased variance, fp32 statistics. x, out: [rows, H] bf16; gamma, beta: [H]

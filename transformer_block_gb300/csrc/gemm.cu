@@ -99,6 +99,18 @@ __device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]
 template <int KIND>
 __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col0, float (&v)[32]) {
   if (row >= ep.M) return;
+  if (ep.scale_a != nullptr) {  // FP8 operands: undo the row and channel scales
+    const float sa = ep.scale_a[row];
+    const float4* s4 = reinterpret_cast<const float4*>(ep.scale_b + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 sb = __ldg(s4 + q);
+      v[4 * q + 0] *= sa * sb.x;
+      v[4 * q + 1] *= sa * sb.y;
+      v[4 * q + 2] *= sa * sb.z;
+      v[4 * q + 3] *= sa * sb.w;
+    }
+  }
   if (KIND != kEpiStore && ep.bias != nullptr) {
     const float4* b4 = reinterpret_cast<const float4*>(ep.bias + col0);
 #pragma unroll
@@ -257,7 +269,7 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-template <int KIND, bool F16>
+template <int KIND, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int K, const EpiParams ep, const SkParams sk, int* status, uint64_t limit_ns) {
@@ -312,7 +324,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   Sched sc;
   sc.num_m = (ep.M + PM - 1) / PM;
   sc.num_n = (ep.N + BN - 1) / BN;
-  sc.num_kb = K / BK;
+  constexpr int BKE = OP == kOpE4m3 ? kGemmBK8 : BK;  // K elements per stage (128 bytes)
+  sc.num_kb = K / BKE;
   sc.cluster = int(blockIdx.x) >> 1;
   sc.clusters = int(gridDim.x) >> 1;
   sc.dp_tiles = sk.dp_tiles;
@@ -348,8 +361,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           // its arrival. The odd CTA reuses a stage only after the pair's MMAs read it, so
           // its copies always count toward the phase the MMA issuer waits for next.
           if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
-          tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, kb * BK, m0);
-          tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, kb * BK, n0);
+          tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, kb * BKE, m0);
+          tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, kb * BKE, n0);
           last_par[stage] = phase;
           used |= 1u << stage;
           if (++stage == STAGES) {
@@ -368,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_f32acc(PM, BN, F16);
+      const uint32_t idesc = idesc_f32acc(PM, BN, OP != kOpBf16);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -389,9 +402,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sa = smem_u32(smem + size_t(stage) * STAGE_BYTES);
           const uint64_t da = sdesc_kmajor_sw128(sa);
           const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
+          // four products of 32 bytes of K each: K = 16 (16-bit) or 32 (FP8) elements
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_f16kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb > u.kb0) || k > 0);
+          for (int k = 0; k < 4; ++k) {
+            if (OP == kOpE4m3)
+              mma_f8kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb > u.kb0) || k > 0);
+            else
+              mma_f16kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb > u.kb0) || k > 0);
+          }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
             stage = 0;
@@ -533,7 +551,7 @@ uint64_t next_epoch() {
   return e == 0 ? ++counter : e;
 }
 
-template <int KIND, bool F16>
+template <int KIND, int OP>
 cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
                         void* sk_scratch, cudaStream_t stream) {
@@ -550,12 +568,12 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   cfg.attrs = at;
   cfg.numAttrs = 1;
   if (max_clusters < 0) {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<KIND, F16>,
+    attr_err = cudaFuncSetAttribute(gemm_kernel<KIND, OP>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
     if (attr_err == cudaSuccess) {
       cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
       int n = 0;
-      attr_err = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, F16>, &cfg);
+      attr_err = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, OP>, &cfg);
       max_clusters = (attr_err == cudaSuccess && n > 0) ? n : 0;
     }
   }
@@ -563,7 +581,7 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
   const int tiles = ((M + PM - 1) / PM) * ((N + BN - 1) / BN);
   const int clusters = tiles < max_clusters ? tiles : max_clusters;
-  const int num_kb = K / BK;
+  const int num_kb = K / (OP == kOpE4m3 ? kGemmBK8 : BK);
   // Stream-K for the last waves when they would leave pairs idle: every full wave but one
   // runs whole tiles; the remaining (clusters + rem) tiles are split evenly along K.
   SkParams sk{};
@@ -585,7 +603,7 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   e.N = N;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, F16>, tmA, tmB, K, e, sk, status, limit_ns);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, OP>, tmA, tmB, K, e, sk, status, limit_ns);
 }
 
 }  // namespace
@@ -611,15 +629,23 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, int* status, cudaStream_t strea
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(EpiKind kind, bool ab_f16, const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_gemm(EpiKind kind, OpType op, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         int M, int N, int K, const EpiParams& ep, int num_sms, int* status,
                         uint64_t limit_ns, void* sk_scratch, cudaStream_t stream) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
-#define PB_GEMM_CASE(KIND_)                                                                  \
-  return ab_f16 ? launch_kind<KIND_, true>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,  \
-                                           sk_scratch, stream)                                \
-                : launch_kind<KIND_, false>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns, \
-                                            sk_scratch, stream)
+  if (K % (op == kOpE4m3 ? kGemmBK8 : kGemmBK) != 0) return cudaErrorInvalidValue;
+#define PB_GEMM_CASE(KIND_)                                                                    \
+  switch (op) {                                                                                \
+    case kOpF16:                                                                               \
+      return launch_kind<KIND_, kOpF16>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,      \
+                                        sk_scratch, stream);                                   \
+    case kOpE4m3:                                                                              \
+      return launch_kind<KIND_, kOpE4m3>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,     \
+                                         sk_scratch, stream);                                  \
+    default:                                                                                   \
+      return launch_kind<KIND_, kOpBf16>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,     \
+                                         sk_scratch, stream);                                  \
+  }
   switch (kind) {
     case kEpiStore:
       PB_GEMM_CASE(kEpiStore);

@@ -20,11 +20,16 @@ cudaError_t launch_layernorm(int64_t rows, int H, const void* x, bool x_f32,
 
 // ---------------------------------------------------------------- GEMM (gemm.cu)
 // D[M, N] = A[M, K] * B[N, K]^T with tcgen05 on CTA pairs; A and B come in through TMA
-// tensor maps (16-bit, 128-byte swizzle, boxes of 64 columns x kGemmBoxRows rows for both).
+// tensor maps (128-byte swizzle, boxes of 128 bytes of K x kGemmBoxRows rows for both:
+// 64 elements of a 16-bit operand, 128 of an FP8 one).
 constexpr int kGemmBM = 128;       // rows of A per CTA
 constexpr int kGemmBN = 256;       // columns of D per CTA pair (128 rows of B per CTA)
-constexpr int kGemmBK = 64;
+constexpr int kGemmBK = 64;        // K elements per stage, 16-bit operands
+constexpr int kGemmBK8 = 128;      // K elements per stage, FP8 operands
 constexpr int kGemmBoxRows = 128;
+
+// Operand types of the GEMM: both operands have the same one.
+enum OpType : int { kOpBf16 = 0, kOpF16 = 1, kOpE4m3 = 2 };
 
 enum EpiKind : int {
   kEpiStore = 0,     // C = bf16(D)
@@ -53,6 +58,10 @@ struct EpiParams {
   bool act_f16;        // act holds fp16 (else bf16)
   // kEpiBlockIn / kEpiResidual: fp32 bias of the N output columns, or null
   const float* bias;
+  // FP8 operands: D[m, n] is scale_a[m] * scale_b[n] times the accumulated sum (per-row
+  // scales of A and per-output-channel scales of B), applied before the bias; null = 1.
+  const float* scale_a;
+  const float* scale_b;
   // kEpiResidual
   const void* resid;  // [M, N], fp32 if resid_f32 else bf16
   void* y;            // [M, N], fp32 if y_f32 else bf16
@@ -69,9 +78,10 @@ constexpr size_t kSkFlagBytes = size_t(2) * 4 * 8;             // 2 CTAs x 4 war
 constexpr size_t kSkScratchBytes = size_t(kSkMaxClusters) * (kSkPartialBytes + kSkFlagBytes);
 
 size_t gemm_smem_bytes();
-// ab_f16: A and B are fp16 (else bf16). sk_scratch (kSkScratchBytes, 256-byte aligned) may
-// be null: then every tile is computed whole by one CTA pair.
-cudaError_t launch_gemm(EpiKind kind, bool ab_f16, const CUtensorMap& tmA, const CUtensorMap& tmB,
+// op: the type of A and B (K % 64 == 0, K % 128 == 0 for kOpE4m3). sk_scratch
+// (kSkScratchBytes, 256-byte aligned) may be null: then every tile is computed whole by one
+// CTA pair.
+cudaError_t launch_gemm(EpiKind kind, OpType op, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         int M, int N, int K, const EpiParams& ep, int num_sms, int* status,
                         uint64_t limit_ns, void* sk_scratch, cudaStream_t stream);
 
@@ -108,6 +118,32 @@ cudaError_t launch_bias_prep(const __nv_bfloat16* b_qkv, const __nv_bfloat16* b1
                              const __nv_bfloat16* b_o, const __nv_bfloat16* b2, int H, int F,
                              bool glu, float* bias1, float* bias2, float* bias_o, float* bias_2,
                              cudaStream_t stream);
+
+// ---------------------------------------------------------------- FP8 (quant.cu, pack.cu)
+// Per-row current scaling to E4M3 (fixed fp32 steps: amax, inv = 448 / amax, scale =
+// amax / 448, code = E4M3(x * inv) rounded to nearest even, saturating). x: bf16 [rows,
+// cols] with row stride ld_in; codes: [rows, cols] bytes with row stride ld_out; scales:
+// [rows] fp32. cols, ld_in, ld_out multiples of 8.
+cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* x, int64_t rows, int64_t cols,
+                                      int64_t ld_in, uint8_t* codes, int64_t ld_out,
+                                      float* scales, cudaStream_t stream);
+// amax[c] = max(amax[c], max_r |w[r, c]|) for a bf16 [rows, cols] matrix, row stride ld
+// (amax must start at 0 or hold an earlier partial result).
+cudaError_t launch_col_amax(const __nv_bfloat16* w, int64_t rows, int64_t cols, int64_t ld,
+                            float* amax, cudaStream_t stream);
+// As launch_transpose, writing the E4M3 code of each value scaled by 448 / amax of its
+// output row's source column (per-output-channel current scaling).
+cudaError_t launch_transpose_e4m3(const __nv_bfloat16* in, int64_t rows, int64_t cols,
+                                  int64_t ld_in, uint8_t* out, int64_t ld_out, int64_t glu_F,
+                                  const float* amax, cudaStream_t stream);
+// scales[c] = amax[source column of output row c] / 448.
+cudaError_t launch_amax_to_scales(const float* amax, int64_t n, int64_t glu_F, float* scales,
+                                  cudaStream_t stream);
+// LayerNorm (beta != null) or RMSNorm of bf16 / fp32 rows straight to E4M3 codes with
+// per-row current scaling: out [rows, H] bytes, scales [rows] fp32.
+cudaError_t launch_layernorm_e4m3(int64_t rows, int H, const void* x, bool x_f32,
+                                  const __nv_bfloat16* gamma, const __nv_bfloat16* beta,
+                                  float eps, uint8_t* out, float* scales, cudaStream_t stream);
 
 // ---------------------------------------------------------------- self-test (gemm.cu)
 cudaError_t launch_wait_probe(uint64_t limit_ns, int* status, cudaStream_t stream);

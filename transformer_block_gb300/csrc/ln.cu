@@ -10,13 +10,13 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace pb {
 namespace {
 
 constexpr int THREADS = 256;
 constexpr int MAXV = kLnMaxH / (8 * THREADS);  // 8 vectors of 8 elements per thread
-constexpr float kF16Max = 65504.f;
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -29,6 +29,19 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   for (int w = 0; w < THREADS / 32; ++w) s += red[w];
   __syncthreads();
   return s;
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float m = 0.f;
+#pragma unroll
+  for (int w = 0; w < THREADS / 32; ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
+  return m;
 }
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* row, int idx, float (&f)[8]) {
@@ -119,6 +132,68 @@ __global__ void __launch_bounds__(THREADS) layernorm_kernel(const TIn* __restric
   if (F16 && out_of_range && status != nullptr) atomicCAS(status, 0, kStatusRange);
 }
 
+// LayerNorm / RMSNorm straight to FP8 E4M3 (the FP8 GEMM operand): the normalised row is
+// computed in fp32 as above, its largest magnitude reduced across the CTA, and each value
+// written as E4M3(o * 448 / amax), the row's scale amax / 448 to scales[row] (per-row
+// current scaling, the steps of quant.cu).
+template <typename TIn, bool RMS>
+__global__ void __launch_bounds__(THREADS) layernorm_e4m3_kernel(
+    const TIn* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+    const __nv_bfloat16* __restrict__ beta, uint2* __restrict__ out, float* __restrict__ scales,
+    int H, float eps) {
+  __shared__ float red[THREADS / 32];
+  const int nv = H / 8;
+  const int64_t row = blockIdx.x;
+  const TIn* xr = x + row * H;
+  float v[MAXV][8];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nv) {
+      load8(xr, idx, v[i]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += v[i][e];
+    }
+  }
+  const float mean = RMS ? 0.f : block_sum(sum, red) / float(H);
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nv) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sq += (v[i][e] - mean) * (v[i][e] - mean);
+    }
+  }
+  const float rstd = rsqrtf(block_sum(sq, red) / float(H) + eps);
+  // the normalised values replace x in registers
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nv) {
+      float g[8], b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      load8(gamma, idx, g);
+      if (!RMS) load8(beta, idx, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[i][e] = (v[i][e] - mean) * rstd * g[e] + b[e];
+        amax = fmaxf(amax, fabsf(v[i][e]));
+      }
+    }
+  }
+  amax = block_max(amax, red);
+  const float inv = amax > 0.f ? 448.f / amax : 0.f;
+  if (threadIdx.x == 0) scales[row] = amax / 448.f;
+  uint2* orow = out + row * nv;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nv) orow[idx] = quant8_e4m3(v[i], inv);
+  }
+}
+
 template <typename TIn, bool F16>
 cudaError_t launch_t(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
                      const __nv_bfloat16* beta, float eps, void* out, int* status,
@@ -145,6 +220,31 @@ cudaError_t launch_layernorm(int64_t rows, int H, const void* x, bool x_f32,
   return out_f16
              ? launch_t<__nv_bfloat16, true>(rows, H, x, gamma, beta, eps, out, status, stream)
              : launch_t<__nv_bfloat16, false>(rows, H, x, gamma, beta, eps, out, status, stream);
+}
+
+cudaError_t launch_layernorm_e4m3(int64_t rows, int H, const void* x, bool x_f32,
+                                  const __nv_bfloat16* gamma, const __nv_bfloat16* beta,
+                                  float eps, uint8_t* out, float* scales, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  if (H <= 0 || H % 8 != 0 || H > kLnMaxH || rows > 0x7fffffff) return cudaErrorInvalidValue;
+  uint2* o = reinterpret_cast<uint2*>(out);
+  const unsigned g = unsigned(rows);
+  if (x_f32) {
+    if (beta == nullptr)
+      layernorm_e4m3_kernel<float, true><<<g, THREADS, 0, stream>>>(
+          static_cast<const float*>(x), gamma, beta, o, scales, H, eps);
+    else
+      layernorm_e4m3_kernel<float, false><<<g, THREADS, 0, stream>>>(
+          static_cast<const float*>(x), gamma, beta, o, scales, H, eps);
+  } else {
+    if (beta == nullptr)
+      layernorm_e4m3_kernel<__nv_bfloat16, true><<<g, THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(x), gamma, beta, o, scales, H, eps);
+    else
+      layernorm_e4m3_kernel<__nv_bfloat16, false><<<g, THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(x), gamma, beta, o, scales, H, eps);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace pb

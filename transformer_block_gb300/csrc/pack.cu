@@ -14,6 +14,7 @@
 #include <type_traits>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace pb {
 namespace {
@@ -29,12 +30,14 @@ __device__ __forceinline__ int64_t glu_source(int64_t c, int64_t glu_F) {
 }
 
 // out[c * ld_out + r] = in[r * ld_in + glu_source(c)], through a padded 32 x 32 shared-memory
-// tile so both the reads and the writes are coalesced; TOut is bf16 (a copy) or fp16 (a
-// conversion, exact inside the fp16 range; values beyond it are reported).
+// tile so both the reads and the writes are coalesced; TOut is bf16 (a copy), fp16 (a
+// conversion, exact inside the fp16 range; values beyond it are reported) or uint8_t: the
+// FP8 E4M3 code of the value times 448 / amax[glu_source(c)] (per-output-channel current
+// scaling, the same fp32 steps as the row quantizer of quant.cu).
 template <typename TOut>
 __global__ void transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t rows, int64_t cols,
                                  int64_t ld_in, TOut* __restrict__ out, int64_t ld_out,
-                                 int64_t glu_F, int* status) {
+                                 int64_t glu_F, const float* __restrict__ amax, int* status) {
   __shared__ float tile[TILE][TILE + 1];
   const int64_t r0 = int64_t(blockIdx.y) * TILE, c0 = int64_t(blockIdx.x) * TILE;
   for (int i = threadIdx.y; i < TILE; i += blockDim.y) {
@@ -48,7 +51,11 @@ __global__ void transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t r
     const int64_t c = c0 + i, r = r0 + threadIdx.x;
     if (r < rows && c < cols) {
       const float v = tile[threadIdx.x][i];
-      if (sizeof(TOut) == 2 && std::is_same<TOut, __half>::value) {
+      if (std::is_same<TOut, uint8_t>::value) {
+        const float a = amax[glu_source(c, glu_F)];
+        const float inv = a > 0.f ? 448.f / a : 0.f;
+        out[c * ld_out + r] = TOut(cvt_e4m3x2(v * inv, 0.f) & 0xFF);
+      } else if (sizeof(TOut) == 2 && std::is_same<TOut, __half>::value) {
         bad |= !(fabsf(v) <= 65504.f);
         out[c * ld_out + r] = TOut(__float2half_rn(v));
       } else {
@@ -95,10 +102,40 @@ cudaError_t launch_transpose(const __nv_bfloat16* in, int64_t rows, int64_t cols
   if (out_f16)
     transpose_kernel<__half><<<grid, block, 0, stream>>>(in, rows, cols, ld_in,
                                                           static_cast<__half*>(out), ld_out,
-                                                          glu_F, status);
+                                                          glu_F, nullptr, status);
   else
     transpose_kernel<__nv_bfloat16><<<grid, block, 0, stream>>>(
-        in, rows, cols, ld_in, static_cast<__nv_bfloat16*>(out), ld_out, glu_F, status);
+        in, rows, cols, ld_in, static_cast<__nv_bfloat16*>(out), ld_out, glu_F, nullptr,
+        status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_e4m3(const __nv_bfloat16* in, int64_t rows, int64_t cols,
+                                  int64_t ld_in, uint8_t* out, int64_t ld_out, int64_t glu_F,
+                                  const float* amax, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (glu_F != 0 && (cols != 2 * glu_F || glu_F % 16 != 0)) return cudaErrorInvalidValue;
+  const int64_t gx = (cols + TILE - 1) / TILE, gy = (rows + TILE - 1) / TILE;
+  if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidValue;
+  const dim3 grid{unsigned(gx), unsigned(gy), 1u}, block{unsigned(TILE), 8u, 1u};
+  transpose_kernel<uint8_t><<<grid, block, 0, stream>>>(in, rows, cols, ld_in, out, ld_out, glu_F,
+                                                         amax, nullptr);
+  return cudaGetLastError();
+}
+
+namespace {
+// scales[c] = amax[glu_source(c)] / 448 for the n output channels.
+__global__ void amax_to_scales_kernel(const float* amax, int64_t n, int64_t glu_F, float* scales) {
+  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < n;
+       c += int64_t(gridDim.x) * blockDim.x)
+    scales[c] = amax[glu_source(c, glu_F)] / 448.f;
+}
+}  // namespace
+
+cudaError_t launch_amax_to_scales(const float* amax, int64_t n, int64_t glu_F, float* scales,
+                                  cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  amax_to_scales_kernel<<<256, 256, 0, stream>>>(amax, n, glu_F, scales);
   return cudaGetLastError();
 }
 

@@ -28,9 +28,14 @@ struct pb_handle {
   uint64_t limit_ns;
   uint8_t* ws;
   int* status;             // device status word
-  bool f16;                // PB_OPERANDS_FP16
-  void* w1cat;             // [3H + F, H], bf16 or fp16
-  void* w2cat;             // [H, H + F], bf16 or fp16
+  bool f16;                // PB_OPERANDS_FP16: 16-bit intermediates and weights are fp16
+  bool fp8;                // PB_OPERANDS_FP8: the GEMMs take E4M3 operands
+  pb::OpType op16;         // type of the 16-bit intermediates (bf16 or fp16)
+  pb::OpType gop;          // operand type of the GEMMs
+  void* w1cat;             // [3H + F, H], bf16, fp16 or E4M3 codes
+  void* w2cat;             // [H, H + F], bf16, fp16 or E4M3 codes
+  float* w1scale;          // FP8: [3H + F] per-output-channel scales of W1cat
+  float* w2scale;          // FP8: [H] per-output-channel scales of W2cat
   float* bias1;            // [3H + F]
   float* bias2;            // [H] = b_o + b2
   float* bias_o;           // [H] = b_o (serial block)
@@ -111,7 +116,9 @@ int64_t w1_rows(const pb_dims& d) {
 }
 
 struct WsLayout {
-  size_t status, w1cat, w2cat, bias1, bias2, bias_o, bias_2, gamma, beta, total;
+  size_t status, w1cat, w2cat, bias1, bias2, bias_o, bias_2, gamma, beta;
+  size_t w1scale, w2scale, amax1, amax2;  // FP8 operands (reserved in every mode)
+  size_t total;
 };
 
 WsLayout ws_layout(const pb_dims& d) {
@@ -136,6 +143,14 @@ WsLayout ws_layout(const pb_dims& d) {
   off = align_up(off + H * 2, 1024);
   L.beta = off;
   off = align_up(off + H * 2, 1024);
+  L.w1scale = off;
+  off = align_up(off + size_t(w1_rows(d)) * 4, 1024);
+  L.w2scale = off;
+  off = align_up(off + H * 4, 1024);
+  L.amax1 = off;
+  off = align_up(off + size_t(w1_rows(d)) * 4, 1024);
+  L.amax2 = off;
+  off = align_up(off + H * 4, 1024);
   L.total = off;
   return L;
 }
@@ -162,6 +177,10 @@ pb_scratch_layout scratch_layout(const pb_dims& d) {
   off = align_up(off + T * H * 4, 1024);
   L.sk = off;
   off = align_up(off + pb::kSkScratchBytes, 1024);
+  L.q8 = off;
+  off = align_up(off + T * (H + F), 1024);
+  L.qscale = off;
+  off = align_up(off + 2 * T * 4, 1024);
   L.total = off;
   return L;
 }
@@ -191,10 +210,19 @@ pb_status get_encoder(EncodeTiledFn* out) {
   return PB_OK;
 }
 
-// 16-bit tensor (bf16, or fp16 when f16) of `rank` dims (dims[0] innermost), 128-byte
-// swizzle, zero fill outside.
+CUtensorMapDataType map_type(pb::OpType t) {
+  switch (t) {
+    case pb::kOpF16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case pb::kOpE4m3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;  // raw E4M3 bytes
+    default: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  }
+}
+
+// Tensor of `rank` dims (dims[0] innermost) of element type t, 128-byte swizzle, zero fill
+// outside.
 pb_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                   const uint64_t* strides_bytes, const uint32_t* box, bool f16 = false) {
+                   const uint64_t* strides_bytes, const uint32_t* box,
+                   pb::OpType t = pb::kOpBf16) {
   EncodeTiledFn enc;
   pb_status s = get_encoder(&enc);
   if (s != PB_OK) return s;
@@ -205,21 +233,22 @@ pb_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d
     bx[i] = box[i];
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                   cuuint32_t(rank), const_cast<void*>(base),
+  CUresult r = enc(m, map_type(t), cuuint32_t(rank), const_cast<void*>(base),
                    gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   return PB_OK;
 }
 
-// Row-major [rows, cols] 16-bit matrix read in boxes of 64 columns x box_rows rows.
+// Row-major [rows, cols] matrix of element type t read in boxes of 128 bytes of columns
+// (64 16-bit or 128 FP8 elements) x box_rows rows.
 pb_status make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                      uint64_t ld, uint32_t box_rows, bool f16 = false) {
+                      uint64_t ld, uint32_t box_rows, pb::OpType t = pb::kOpBf16) {
+  const uint64_t esz = t == pb::kOpE4m3 ? 1 : 2;
   const uint64_t dims[2] = {cols, rows};
-  const uint64_t strides[1] = {ld * 2};
-  const uint32_t box[2] = {64, box_rows};
-  return make_map(m, base, 2, dims, strides, box, f16);
+  const uint64_t strides[1] = {ld * esz};
+  const uint32_t box[2] = {uint32_t(128 / esz), box_rows};
+  return make_map(m, base, 2, dims, strides, box, t);
 }
 
 // Tensor maps of the attention step: q|k [B][S][2H] read as query tiles and as key tiles,
@@ -273,16 +302,23 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], st) : cudaSuccess; };
   PB_CUDA(mark(0), "cudaEventRecord");
 
-  // 1. the shared LayerNorm (RMSNorm for the SwiGLU variant: no beta)
+  // 1. the shared LayerNorm (RMSNorm for the SwiGLU variant: no beta); with FP8 operands
+  // it writes E4M3 codes of LN(x) and their per-row scales
   const bool glu = is_glu(d);
-  PB_CUDA(pb::launch_layernorm(T, H, x, x_f32, h->gamma, glu ? nullptr : h->beta, d.ln_eps, xn,
-                               h->f16, h->status, st),
-          "layernorm launch");
+  float* qscale = reinterpret_cast<float*>(scratch + L.qscale);
+  if (h->fp8)
+    PB_CUDA(pb::launch_layernorm_e4m3(T, H, x, x_f32, h->gamma, glu ? nullptr : h->beta,
+                                      d.ln_eps, static_cast<uint8_t*>(xn), qscale, st),
+            "layernorm launch");
+  else
+    PB_CUDA(pb::launch_layernorm(T, H, x, x_f32, h->gamma, glu ? nullptr : h->beta, d.ln_eps,
+                                 xn, h->f16, h->status, st),
+            "layernorm launch");
   PB_CUDA(mark(1), "cudaEventRecord");
 
   // 2. [q | k | v | h] = xn [Wqkv | W1], GeLU(h) in the epilogue
   CUtensorMap tm_xn, tm_act, tm_qk, tm_vt;
-  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, pb::kGemmBoxRows, h->f16);
+  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, pb::kGemmBoxRows, h->gop);
   if (s != PB_OK) return s;
   EpiParams e1{};
   e1.status = h->status;
@@ -298,7 +334,11 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   e1.act_f16 = h->f16;
   e1.bias = h->has_bias ? h->bias1 : nullptr;
   e1.glu = glu;
-  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, h->tm_w1cat, T, int(w1_rows(d)), H,
+  if (h->fp8) {
+    e1.scale_a = qscale;
+    e1.scale_b = h->w1scale;
+  }
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->gop, tm_xn, h->tm_w1cat, T, int(w1_rows(d)), H,
                           e1, h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
           "first GEMM launch");
   PB_CUDA(mark(2), "cudaEventRecord");
@@ -322,8 +362,17 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   PB_CUDA(pb::launch_swa(tm_qk, tm_k, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
   PB_CUDA(mark(3), "cudaEventRecord");
 
-  // 4. y = x + [attn | GeLU(h)] [Wo ; W2] (+ b_o + b2)
-  s = make_map_2d(&tm_act, act, T, H + F, H + F, pb::kGemmBoxRows, h->f16);
+  // 4. y = x + [attn | GeLU(h)] [Wo ; W2] (+ b_o + b2). With FP8 operands the rows of
+  // act are quantized first (per-row scales in qscale[T, 2T); timed with this step).
+  const void* a2 = act;
+  if (h->fp8) {
+    uint8_t* q8 = scratch + L.q8;
+    PB_CUDA(pb::launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(act), T, H + F,
+                                          H + F, q8, H + F, qscale + T, st),
+            "act quantization launch");
+    a2 = q8;
+  }
+  s = make_map_2d(&tm_act, a2, T, H + F, H + F, pb::kGemmBoxRows, h->gop);
   if (s != PB_OK) return s;
   EpiParams e2{};
   e2.status = h->status;
@@ -332,7 +381,11 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   e2.resid_f32 = x_f32;
   e2.y = y;
   e2.y_f32 = y_f32;
-  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->f16, tm_act, h->tm_w2cat, T, H, H + F, e2,
+  if (h->fp8) {
+    e2.scale_a = qscale + T;
+    e2.scale_b = h->w2scale;
+  }
+  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->gop, tm_act, h->tm_w2cat, T, H, H + F, e2,
                           h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
           "second GEMM launch");
   PB_CUDA(mark(4), "cudaEventRecord");
@@ -369,8 +422,8 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
           "layernorm launch");
   // 2. [q | k | v] = xn Wqkv (+ b_qkv): rows [0, 3H) of W1cat
   CUtensorMap tm_xn, tm_wqkv;
-  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, box, h->f16);
-  if (s == PB_OK) s = make_map_2d(&tm_wqkv, w1c, 3 * uint64_t(H), H, H, box, h->f16);
+  pb_status s = make_map_2d(&tm_xn, xn, T, H, H, box, h->op16);
+  if (s == PB_OK) s = make_map_2d(&tm_wqkv, w1c, 3 * uint64_t(H), H, H, box, h->op16);
   if (s != PB_OK) return s;
   EpiParams e1{};
   e1.status = h->status;
@@ -386,7 +439,7 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   e1.act_f16 = h->f16;
   e1.bias = h->has_bias ? h->bias1 : nullptr;
   e1.glu = glu;
-  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, tm_wqkv, T, 3 * H, H, e1, h->num_sms,
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->op16, tm_xn, tm_wqkv, T, 3 * H, H, e1, h->num_sms,
                           h->status, h->limit_ns, scratch + L.sk, st),
           "QKV GEMM launch");
   // 3. sliding-window attention -> act[:, 0:H]
@@ -408,8 +461,8 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   PB_CUDA(pb::launch_swa(tm_qk, tm_k, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
   // 4. h = x + attn Wo (+ b_o): columns [0, H) of W2cat, result in fp32
   CUtensorMap tm_attn, tm_wo;
-  s = make_map_2d(&tm_attn, act, T, H, H + F, box, h->f16);
-  if (s == PB_OK) s = make_map_2d(&tm_wo, w2c, H, H, H + F, box, h->f16);
+  s = make_map_2d(&tm_attn, act, T, H, H + F, box, h->op16);
+  if (s == PB_OK) s = make_map_2d(&tm_wo, w2c, H, H, H + F, box, h->op16);
   if (s != PB_OK) return s;
   EpiParams e2{};
   e2.status = h->status;
@@ -418,7 +471,7 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   e2.resid_f32 = false;
   e2.y = hres;
   e2.y_f32 = true;
-  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->f16, tm_attn, tm_wo, T, H, H, e2, h->num_sms,
+  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->op16, tm_attn, tm_wo, T, H, H, e2, h->num_sms,
                           h->status, h->limit_ns, scratch + L.sk, st),
           "attention projection GEMM launch");
   // 5. LN'(h) -> xn
@@ -429,18 +482,18 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   // ([3H, 3H + 2F) for SwiGLU), routed as the h columns of [q | k | v | h]
   const int n_h = int(w1_rows(d) - 3 * int64_t(H));
   CUtensorMap tm_w1;
-  s = make_map_2d(&tm_w1, w1c + 3 * size_t(H) * H * esz, n_h, H, H, box, h->f16);
+  s = make_map_2d(&tm_w1, w1c + 3 * size_t(H) * H * esz, n_h, H, H, box, h->op16);
   if (s != PB_OK) return s;
   EpiParams e3 = e1;
   e3.col_base = 3 * H;
   e3.bias = h->has_bias ? h->bias1 + 3 * size_t(H) : nullptr;
-  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->f16, tm_xn, tm_w1, T, n_h, H, e3, h->num_sms,
+  PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->op16, tm_xn, tm_w1, T, n_h, H, e3, h->num_sms,
                           h->status, h->limit_ns, scratch + L.sk, st),
           "MLP input GEMM launch");
   // 7. y = h + GeLU(.) W2 (+ b2): A = act[:, H:H+F], columns [H, H + F) of W2cat
   CUtensorMap tm_g, tm_w2;
-  s = make_map_2d(&tm_g, act + size_t(H) * esz, T, F, H + F, box, h->f16);
-  if (s == PB_OK) s = make_map_2d(&tm_w2, w2c + size_t(H) * esz, H, F, H + F, box, h->f16);
+  s = make_map_2d(&tm_g, act + size_t(H) * esz, T, F, H + F, box, h->op16);
+  if (s == PB_OK) s = make_map_2d(&tm_w2, w2c + size_t(H) * esz, H, F, H + F, box, h->op16);
   if (s != PB_OK) return s;
   EpiParams e4{};
   e4.status = h->status;
@@ -449,7 +502,7 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   e4.resid_f32 = true;
   e4.y = y;
   e4.y_f32 = false;
-  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->f16, tm_g, tm_w2, T, H, F, e4, h->num_sms,
+  PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->op16, tm_g, tm_w2, T, H, F, e4, h->num_sms,
                           h->status, h->limit_ns, scratch + L.sk, st),
           "MLP output GEMM launch");
   return PB_OK;
@@ -573,9 +626,15 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
       return fail(PB_ERR_INVALID_ARG, "a bias pointer is misaligned");
   pb_options opt{PB_OPERANDS_BF16, 0};
   if (options != nullptr) opt = *options;
-  if (opt.operand_precision != PB_OPERANDS_BF16 && opt.operand_precision != PB_OPERANDS_FP16)
+  if (opt.operand_precision != PB_OPERANDS_BF16 && opt.operand_precision != PB_OPERANDS_FP16 &&
+      opt.operand_precision != PB_OPERANDS_FP8)
     return fail(PB_ERR_INVALID_ARG, "operand_precision %d is not a pb_operand_precision",
                 opt.operand_precision);
+  // FP8 GEMMs step through K in 128-element stages: K = H (first GEMM) and H + F (second)
+  if (opt.operand_precision == PB_OPERANDS_FP8 &&
+      (dims->hidden % pb::kGemmBK8 != 0 || (dims->hidden + dims->ffn) % pb::kGemmBK8 != 0))
+    return fail(PB_ERR_UNSUPPORTED, "FP8 operands need hidden and hidden + ffn to be multiples of %d",
+                pb::kGemmBK8);
   const WsLayout L = ws_layout(*dims);
   if (workspace == nullptr || !aligned(workspace, 256))
     return fail(PB_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
@@ -594,10 +653,15 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
   h->num_sms = sms;
   h->limit_ns = opt.wait_limit_ns ? opt.wait_limit_ns : kDefaultLimitNs;
   h->f16 = opt.operand_precision == PB_OPERANDS_FP16;
+  h->fp8 = opt.operand_precision == PB_OPERANDS_FP8;
+  h->op16 = h->f16 ? pb::kOpF16 : pb::kOpBf16;
+  h->gop = h->fp8 ? pb::kOpE4m3 : h->op16;
   h->ws = static_cast<uint8_t*>(workspace);
   h->status = reinterpret_cast<int*>(h->ws + L.status);
   h->w1cat = h->ws + L.w1cat;
   h->w2cat = h->ws + L.w2cat;
+  h->w1scale = reinterpret_cast<float*>(h->ws + L.w1scale);
+  h->w2scale = reinterpret_cast<float*>(h->ws + L.w2scale);
   h->bias1 = reinterpret_cast<float*>(h->ws + L.bias1);
   h->bias2 = reinterpret_cast<float*>(h->ws + L.bias2);
   h->bias_o = reinterpret_cast<float*>(h->ws + L.bias_o);
@@ -626,17 +690,44 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
   const int64_t w1_cols = glu ? 2 * F : F;
   uint8_t* w1c = static_cast<uint8_t*>(h->w1cat);
   uint8_t* w2c = static_cast<uint8_t*>(h->w2cat);
-  PB_CUDA_H(pb::launch_transpose(bf(w->wqkv), H, 3 * H, 3 * H, w1c, H, h->f16, 0, h->status, st),
-            "pack Wqkv");
-  PB_CUDA_H(pb::launch_transpose(bf(w->w1), H, w1_cols, w1_cols, w1c + 3 * H * H * 2, H, h->f16,
-                                 glu ? F : 0, h->status, st),
-            "pack W1");
-  // W2cat columns [0, H) = Wo^T, columns [H, H + F) = W2^T
-  PB_CUDA_H(pb::launch_transpose(bf(w->wo), H, H, H, w2c, H + F, h->f16, 0, h->status, st),
-            "pack Wo");
-  PB_CUDA_H(pb::launch_transpose(bf(w->w2), F, H, H, w2c + H * 2, H + F, h->f16, 0, h->status,
-                                 st),
-            "pack W2");
+  if (h->fp8) {
+    // E4M3 codes with one scale per output channel (amax / 448): the channel's amax over
+    // the columns of Wqkv and W1 (source order), and over Wo's and W2's columns together
+    float* amax1 = reinterpret_cast<float*>(h->ws + L.amax1);
+    float* amax2 = reinterpret_cast<float*>(h->ws + L.amax2);
+    PB_CUDA_H(cudaMemsetAsync(amax1, 0, size_t(w1_rows(*dims)) * 4, st), "cudaMemsetAsync(amax)");
+    PB_CUDA_H(cudaMemsetAsync(amax2, 0, size_t(H) * 4, st), "cudaMemsetAsync(amax)");
+    PB_CUDA_H(pb::launch_col_amax(bf(w->wqkv), H, 3 * H, 3 * H, amax1, st), "amax of Wqkv");
+    PB_CUDA_H(pb::launch_col_amax(bf(w->w1), H, w1_cols, w1_cols, amax1 + 3 * H, st),
+              "amax of W1");
+    PB_CUDA_H(pb::launch_col_amax(bf(w->wo), H, H, H, amax2, st), "amax of Wo");
+    PB_CUDA_H(pb::launch_col_amax(bf(w->w2), F, H, H, amax2, st), "amax of W2");
+    PB_CUDA_H(pb::launch_transpose_e4m3(bf(w->wqkv), H, 3 * H, 3 * H, w1c, H, 0, amax1, st),
+              "pack Wqkv");
+    PB_CUDA_H(pb::launch_transpose_e4m3(bf(w->w1), H, w1_cols, w1_cols, w1c + 3 * H * H, H,
+                                        glu ? F : 0, amax1 + 3 * H, st),
+              "pack W1");
+    PB_CUDA_H(pb::launch_transpose_e4m3(bf(w->wo), H, H, H, w2c, H + F, 0, amax2, st), "pack Wo");
+    PB_CUDA_H(pb::launch_transpose_e4m3(bf(w->w2), F, H, H, w2c + H, H + F, 0, amax2, st),
+              "pack W2");
+    PB_CUDA_H(pb::launch_amax_to_scales(amax1, 3 * H, 0, h->w1scale, st), "W1cat scales");
+    PB_CUDA_H(pb::launch_amax_to_scales(amax1 + 3 * H, w1_cols, glu ? F : 0, h->w1scale + 3 * H,
+                                        st),
+              "W1cat scales");
+    PB_CUDA_H(pb::launch_amax_to_scales(amax2, H, 0, h->w2scale, st), "W2cat scales");
+  } else {
+    PB_CUDA_H(pb::launch_transpose(bf(w->wqkv), H, 3 * H, 3 * H, w1c, H, h->f16, 0, h->status, st),
+              "pack Wqkv");
+    PB_CUDA_H(pb::launch_transpose(bf(w->w1), H, w1_cols, w1_cols, w1c + 3 * H * H * 2, H, h->f16,
+                                   glu ? F : 0, h->status, st),
+              "pack W1");
+    // W2cat columns [0, H) = Wo^T, columns [H, H + F) = W2^T
+    PB_CUDA_H(pb::launch_transpose(bf(w->wo), H, H, H, w2c, H + F, h->f16, 0, h->status, st),
+              "pack Wo");
+    PB_CUDA_H(pb::launch_transpose(bf(w->w2), F, H, H, w2c + H * 2, H + F, h->f16, 0, h->status,
+                                   st),
+              "pack W2");
+  }
   PB_CUDA_H(pb::launch_bias_prep(bf(w->b_qkv), bf(w->b1), bf(w->b_o), bf(w->b2), int(H), int(F),
                                  glu, h->bias1, h->bias2, h->bias_o, h->bias_2, st),
             "bias prep");
@@ -646,8 +737,9 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* w, const pb_option
     PB_CUDA_H(cudaMemcpyAsync(h->beta, w->ln_beta, H * 2, cudaMemcpyDeviceToDevice, st),
               "copy beta");
 #undef PB_CUDA_H
-  s = make_map_2d(&h->tm_w1cat, h->w1cat, w1_rows(*dims), H, H, pb::kGemmBoxRows, h->f16);
-  if (s == PB_OK) s = make_map_2d(&h->tm_w2cat, h->w2cat, H, H + F, H + F, pb::kGemmBoxRows, h->f16);
+  s = make_map_2d(&h->tm_w1cat, h->w1cat, w1_rows(*dims), H, H, pb::kGemmBoxRows, h->gop);
+  if (s == PB_OK)
+    s = make_map_2d(&h->tm_w2cat, h->w2cat, H, H + F, H + F, pb::kGemmBoxRows, h->gop);
   if (s != PB_OK) return cleanup(s);
   *out = h;
   return PB_OK;
@@ -674,6 +766,7 @@ pb_status pb_forward_serial(pb_handle* h, const void* x, void* y, const void* ln
                             void* stream) {
   pb_status s = check_stack(&h, 1, scratch, scratch_bytes);
   if (s != PB_OK) return s;
+  if (h->fp8) return fail(PB_ERR_UNSUPPORTED, "pb_forward_serial does not take FP8 operands");
   if (x == nullptr || y == nullptr || !aligned(x, 16) || !aligned(y, 16))
     return fail(PB_ERR_INVALID_ARG, "x and y must be 16-byte aligned device pointers");
   if ((ln2_gamma == nullptr) != (ln2_beta == nullptr))
@@ -823,6 +916,23 @@ pb_status pb_layernorm(int64_t rows, int32_t H, const void* x, const void* gamma
   return PB_OK;
 }
 
+pb_status pb_quantize_rows_e4m3(int64_t rows, int32_t cols, const void* x, void* codes,
+                                void* scales, void* stream) {
+  if (rows < 0 || cols < 8 || cols % 8 != 0)
+    return fail(PB_ERR_UNSUPPORTED, "quantize needs rows >= 0 and cols %% 8 == 0, cols >= 8");
+  if (rows >= (int64_t(1) << 31)) return fail(PB_ERR_UNSUPPORTED, "rows >= 2^31");
+  const void* ps[3] = {x, codes, scales};
+  for (const void* p : ps)
+    if (p == nullptr || !aligned(p, 16))
+      return fail(PB_ERR_INVALID_ARG, "pointers must be 16-byte aligned device pointers");
+  PB_CUDA(pb::launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(x), rows, cols, cols,
+                                        static_cast<uint8_t*>(codes), cols,
+                                        static_cast<float*>(scales),
+                                        static_cast<cudaStream_t>(stream)),
+          "quantize launch");
+  return PB_OK;
+}
+
 pb_status pb_gemm_scratch_bytes(size_t* bytes) {
   if (bytes == nullptr) return fail(PB_ERR_INVALID_ARG, "bytes is NULL");
   *bytes = pb::kSkScratchBytes;
@@ -851,7 +961,7 @@ pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const voi
   EpiParams ep{};
   ep.c = static_cast<__nv_bfloat16*>(C);
   ep.ldc = N;
-  PB_CUDA(pb::launch_gemm(pb::kEpiStore, false, ta, tb, M, N, K, ep, sms, status, kDefaultLimitNs,
+  PB_CUDA(pb::launch_gemm(pb::kEpiStore, pb::kOpBf16, ta, tb, M, N, K, ep, sms, status, kDefaultLimitNs,
                           scratch, static_cast<cudaStream_t>(stream)),
           "gemm launch");
   return PB_OK;

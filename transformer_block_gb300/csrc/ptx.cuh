@@ -262,6 +262,19 @@ __device__ __forceinline__ void mma_f16kind_ss_pair(uint32_t d_tmem, uint64_t a_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// As mma_f16kind_ss_pair with FP8 operands (kind::f8f6f4, K = 32 per instruction, the same
+// 32 bytes of a 128-byte swizzled row). The instruction descriptor has the same layout; the
+// format code of E4M3 is 0, so idesc_f32acc(M, N, true) describes E4M3 x E4M3 -> f32.
+__device__ __forceinline__ void mma_f8kind_ss_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                   uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on the mbarrier at offset `bar` in every CTA of `cta_mask` when all pair
 // MMAs issued before by this thread have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
@@ -429,6 +442,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two fp32 values to two FP8 E4M3 codes, rounded to nearest even and saturated at +-448
+// (the .satfinite conversion); `lo` lands in the lower byte (lower address).
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Eight fp32 values times `inv` to eight E4M3 codes, in memory order.
+__device__ __forceinline__ uint2 quant8_e4m3(const float (&v)[8], float inv) {
+  uint2 u;
+  u.x = uint32_t(cvt_e4m3x2(v[0] * inv, v[1] * inv)) |
+        (uint32_t(cvt_e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+  u.y = uint32_t(cvt_e4m3x2(v[4] * inv, v[5] * inv)) |
+        (uint32_t(cvt_e4m3x2(v[6] * inv, v[7] * inv)) << 16);
+  return u;
 }
 
 constexpr float kF16Max = 65504.f;

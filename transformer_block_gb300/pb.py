@@ -21,7 +21,7 @@ PB_ERR_RANGE = 7
 STATUS_NAMES = {0: "PB_OK", 1: "PB_ERR_INVALID_ARG", 2: "PB_ERR_UNSUPPORTED",
                 3: "PB_ERR_WORKSPACE", 4: "PB_ERR_CUDA", 5: "PB_ERR_DEVICE_TIMEOUT",
                 6: "PB_ERR_BAD_HANDLE", 7: "PB_ERR_RANGE"}
-PB_OPERANDS_BF16, PB_OPERANDS_FP16 = 0, 1
+PB_OPERANDS_BF16, PB_OPERANDS_FP16, PB_OPERANDS_FP8 = 0, 1, 2
 
 
 class PbError(RuntimeError):
@@ -46,7 +46,8 @@ class pb_weights(ctypes.Structure):
 
 class pb_scratch_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("xn", "qk", "vt", "act", "io", "res0", "res1", "sk", "seq_pad", "total")]
+                ("xn", "qk", "vt", "act", "io", "res0", "res1", "sk", "q8", "qscale", "seq_pad",
+                 "total")]
 
 
 class pb_options(ctypes.Structure):
@@ -78,6 +79,7 @@ SIGNATURES = {
     "pb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pb_last_error_message": (ctypes.c_char_p, []),
     "pb_layernorm": (ctypes.c_int, [_I64, _I32, _P, _P, _P, ctypes.c_float, _P, _P]),
+    "pb_quantize_rows_e4m3": (ctypes.c_int, [_I64, _I32, _P, _P, _P, _P]),
     "pb_gemm_scratch_bytes": (ctypes.c_int, [ctypes.POINTER(_S)]),
     "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _S, _P, _P]),
     "pb_swa_attention": (ctypes.c_int, [_DP, _P, _P, _P, _I64, _P, _P]),
@@ -159,16 +161,20 @@ def new_scratch(dims: pb_dims, device="cuda") -> torch.Tensor:
 
 def scratch_view(scratch: torch.Tensor, dims: pb_dims, name: str,
                  dtype=torch.bfloat16) -> torch.Tensor:
-    """A view of one intermediate in the scratch (``xn, qk, vt, act, io, res0, res1``);
-    ``dtype`` is the element type it holds (fp16 for ``xn``/``act`` with fp16 operands,
-    fp32 for ``res0``/``res1``)."""
+    """A view of one intermediate in the scratch (``xn, qk, vt, act, io, res0, res1, q8,
+    qscale``); ``dtype`` is the element type it holds (fp16 for ``xn``/``act`` with fp16
+    operands, uint8 E4M3 codes for ``xn`` with FP8 operands; ``res0``/``res1``/``qscale``
+    are always fp32 and ``q8`` uint8)."""
     L = scratch_layout(dims)
     T, H, F = dims.batch * dims.seq, dims.hidden, dims.ffn
     shapes = {"xn": (T, H), "qk": (T, 2 * H), "act": (T, H + F), "io": (T, H),
               "res0": (T, H), "res1": (T, H),
-              "vt": (dims.batch, dims.heads, dims.head_dim, L.seq_pad)}
-    if name in ("res0", "res1"):
+              "vt": (dims.batch, dims.heads, dims.head_dim, L.seq_pad),
+              "q8": (T, H + F), "qscale": (2 * T,)}
+    if name in ("res0", "res1", "qscale"):
         dtype = torch.float32
+    elif name == "q8":
+        dtype = torch.uint8
     shape = shapes[name]
     n = 1
     for s in shape:
@@ -316,6 +322,17 @@ def gemm_static(a, b, out=None, status=None, stream=None):
     _check("pb_gemm_bf16_static", lib().pb_gemm_bf16_static(M, N, K, _ptr(a), _ptr(b), _ptr(out),
                                                             _ptr(status), _stream(stream)))
     return out
+
+
+def quantize_rows_e4m3(x: torch.Tensor, stream=None):
+    """Per-row current scaling of a bf16 [rows, cols] CUDA tensor to FP8 E4M3 codes
+    (``pb_quantize_rows_e4m3``): returns ``(codes uint8 [rows, cols], scales fp32 [rows])``."""
+    rows, cols = x.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check("pb_quantize_rows_e4m3", lib().pb_quantize_rows_e4m3(rows, cols, _ptr(x), _ptr(codes),
+                                                                _ptr(scales), _stream(stream)))
+    return codes, scales
 
 
 def swa_attention(dims: pb_dims, qk, vt, act, status=None, stream=None):
