@@ -257,6 +257,145 @@ void oracle_swa_attention(int64_t nq, const int64_t* q_pos, const double* q, int
   });
 }
 
+// ---------------------------------------------------------------------------- backward
+// The backward pass of the block (training: MFU counts the forward's 2 and the backward's
+// 4 FLOPs per weight and token, performance notes "MFU"). Each routine is the derivative
+// of the forward routine above, written from the chain rule.
+
+// LayerNorm / RMSNorm backward. With xhat = (x - mu) * rstd (RMSNorm: mu = 0,
+// rstd = 1 / sqrt(mean x^2 + eps)) and g = dout * gamma:
+//   dx[r,c] = rstd * (g[c] - mean_c g - xhat[c] * mean_c(g * xhat))   (RMSNorm: no mean_c g)
+//   dgamma[c] = sum_r dout[r,c] * xhat[r,c],   dbeta[c] = sum_r dout[r,c]
+// Rows are split over threads for dx; dgamma and dbeta are then summed per column, rows
+// in ascending order. dbeta may be NULL.
+void oracle_norm_backward(int64_t rows, int64_t H, const double* x, const double* gamma,
+                          const double* dout, double eps, int rms, double* dx, double* dgamma,
+                          double* dbeta, int threads) {
+  std::vector<double> mu(rows > 0 ? rows : 1), rstd(rows > 0 ? rows : 1);
+  for_row_ranges(rows, threads, [&](int64_t r0, int64_t r1) {
+    std::vector<double> xhat(H), g(H);
+    for (int64_t r = r0; r < r1; ++r) {
+      const double* xr = x + r * H;
+      double m = 0.0;
+      if (!rms) {
+        for (int64_t c = 0; c < H; ++c) m += xr[c];
+        m /= (double)H;
+      }
+      double sq = 0.0;
+      for (int64_t c = 0; c < H; ++c) sq += (xr[c] - m) * (xr[c] - m);
+      const double rs = 1.0 / std::sqrt(sq / (double)H + eps);
+      mu[r] = m;
+      rstd[r] = rs;
+      double mean_g = 0.0, mean_gx = 0.0;
+      for (int64_t c = 0; c < H; ++c) {
+        xhat[c] = (xr[c] - m) * rs;
+        g[c] = dout[r * H + c] * gamma[c];
+        mean_g += g[c];
+        mean_gx += g[c] * xhat[c];
+      }
+      mean_g /= (double)H;
+      mean_gx /= (double)H;
+      if (rms) mean_g = 0.0;
+      for (int64_t c = 0; c < H; ++c) dx[r * H + c] = rs * (g[c] - mean_g - xhat[c] * mean_gx);
+    }
+  });
+  for_row_ranges(H, threads, [&](int64_t c0, int64_t c1) {
+    for (int64_t c = c0; c < c1; ++c) {
+      double sg = 0.0, sb = 0.0;
+      for (int64_t r = 0; r < rows; ++r) {
+        const double d = dout[r * H + c];
+        sg += d * (x[r * H + c] - mu[r]) * rstd[r];
+        sb += d;
+      }
+      dgamma[c] = sg;
+      if (dbeta) dbeta[c] = sb;
+    }
+  });
+}
+
+// Exact GeLU backward: gelu'(z) = Phi(z) + z * phi(z), phi(z) = exp(-z^2 / 2) / sqrt(2 pi);
+// dz[i] = dout[i] * gelu'(z[i]).
+void oracle_gelu_backward(int64_t n, const double* z, const double* dout, double* dz,
+                          int threads) {
+  const double inv_sqrt2 = 0.70710678118654752440, inv_sqrt_2pi = 0.39894228040143267794;
+  for_row_ranges(n, threads, [=](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i) {
+      const double Phi = 0.5 * (1.0 + std::erf(z[i] * inv_sqrt2));
+      const double phi = std::exp(-0.5 * z[i] * z[i]) * inv_sqrt_2pi;
+      dz[i] = dout[i] * (Phi + z[i] * phi);
+    }
+  });
+}
+
+// SwiGLU backward for out = silu(gate) * up, silu(z) = z * sigma(z):
+//   dup = dout * silu(gate),   dgate = dout * up * sigma(gate) * (1 + gate * (1 - sigma(gate)))
+void oracle_swiglu_backward(int64_t n, const double* gate, const double* up, const double* dout,
+                            double* dgate, double* dup, int threads) {
+  for_row_ranges(n, threads, [=](int64_t b, int64_t e) {
+    for (int64_t i = b; i < e; ++i) {
+      const double sg = 1.0 / (1.0 + std::exp(-gate[i]));
+      dup[i] = dout[i] * gate[i] * sg;
+      dgate[i] = dout[i] * up[i] * sg * (1.0 + gate[i] * (1.0 - sg));
+    }
+  });
+}
+
+// Backward of oracle_swa_attention over ONE whole sequence of S tokens (positions 0..S-1),
+// from its definition. Per head and query i, with the visible keys W(i) = {j : 0 <= i - j
+// < w}, s_j = q_i . k_j / sqrt(dh), p = softmax(s) over W(i), o_i = sum_j p_j v_j:
+//   dv_j += p_j do_i
+//   dp_j  = do_i . v_j
+//   ds_j  = p_j (dp_j - sum_l p_l dp_l)
+//   dq_i  = sum_j ds_j k_j / sqrt(dh),     dk_j += ds_j q_i / sqrt(dh)
+// Heads are split over threads; within a head the queries are visited in ascending order.
+void oracle_swa_attention_backward(int64_t S, const double* q, const double* k, const double* v,
+                                   const double* dout, int64_t nh, int64_t dh, int64_t w,
+                                   double* dq, double* dk, double* dv, int threads) {
+  const int64_t H = nh * dh;
+  const double scale = 1.0 / std::sqrt((double)dh);
+  for (int64_t i = 0; i < S * H; ++i) dq[i] = dk[i] = dv[i] = 0.0;
+  for_row_ranges(nh, threads, [=](int64_t h0, int64_t h1) {
+    std::vector<double> p(S > 0 ? S : 1), dp(S > 0 ? S : 1);
+    for (int64_t head = h0; head < h1; ++head) {
+      const int64_t off = head * dh;
+      for (int64_t i = 0; i < S; ++i) {
+        const int64_t j0 = std::max<int64_t>(0, i - w + 1);
+        const double* qi = q + i * H + off;
+        const double* doi = dout + i * H + off;
+        double smax = -std::numeric_limits<double>::infinity();
+        for (int64_t j = j0; j <= i; ++j) {
+          double dot = 0.0;
+          for (int64_t d = 0; d < dh; ++d) dot += qi[d] * k[j * H + off + d];
+          p[j] = dot * scale;
+          smax = std::max(smax, p[j]);
+        }
+        double denom = 0.0;
+        for (int64_t j = j0; j <= i; ++j) {
+          p[j] = std::exp(p[j] - smax);
+          denom += p[j];
+        }
+        double pdp = 0.0;
+        for (int64_t j = j0; j <= i; ++j) {
+          p[j] /= denom;
+          double dot = 0.0;
+          for (int64_t d = 0; d < dh; ++d) dot += doi[d] * v[j * H + off + d];
+          dp[j] = dot;
+          pdp += p[j] * dp[j];
+        }
+        double* dqi = dq + i * H + off;
+        for (int64_t j = j0; j <= i; ++j) {
+          const double ds = p[j] * (dp[j] - pdp);
+          for (int64_t d = 0; d < dh; ++d) {
+            dqi[d] += ds * k[j * H + off + d] * scale;
+            dk[j * H + off + d] += ds * qi[d] * scale;
+            dv[j * H + off + d] += p[j] * doi[d];
+          }
+        }
+      }
+    }
+  });
+}
+
 // Elementwise sum of n-vectors: out = a + b + c (the three terms of eq. (4)).
 void oracle_add3(int64_t n, const double* a, const double* b, const double* c, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = a[i] + b[i] + c[i];

@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the parallel transformer block forward pass.
+"""fp64 CPU oracle for the parallel transformer block, forward and backward.
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py``; never by the product package. It shares no code with the
@@ -25,6 +25,12 @@ Two further block forms, on the same primitives:
   the standard forms are taken: ``x / sqrt(mean x^2 + eps) * gamma`` and
   ``silu(x W_gate) * (x W_up)``, ``w1 = [W_gate | W_up]``).
 * ``serial_block_forward``: the standard block of eq. (3), for comparison.
+* ``block_backward``: the gradients of eq. (4) for an upstream ``dy`` (training; the
+  performance notes count the backward as 4 of the 6 FLOPs per weight and token), by the
+  chain rule through the steps above in reverse, with the attention probabilities
+  recomputed from q and k (the pages' selective recomputation). Its primitives
+  (``oracle_norm_backward``, ``oracle_gelu_backward``, ``oracle_swiglu_backward``,
+  ``oracle_swa_attention_backward``) are the derivatives of the forward ones.
 * ``block_forward(fp8=True)``: both GEMMs on FP8 E4M3 operands with per-row current
   scaling (the performance notes' FP8 recipe), the quantizer's fp32 steps in
   ``oracle_quantize_e4m3_rows`` (E4M3 rounding written from the format definition).
@@ -80,8 +86,14 @@ def _bind(lib):
     lib.oracle_rmsnorm.argtypes = [i64, i64, d, d, ctypes.c_double, d, i32]
     lib.oracle_swiglu.argtypes = [i64, d, d, d, i32]
     lib.oracle_quantize_e4m3_rows.argtypes = [i64, i64, d, d, d, d, i32]
+    lib.oracle_norm_backward.argtypes = [i64, i64, d, d, d, ctypes.c_double, i32, d, d, d, i32]
+    lib.oracle_gelu_backward.argtypes = [i64, d, d, d, i32]
+    lib.oracle_swiglu_backward.argtypes = [i64, d, d, d, d, d, i32]
+    lib.oracle_swa_attention_backward.argtypes = [i64, d, d, d, d, i64, i64, i64, d, d, d, i32]
     for f in ("oracle_layernorm", "oracle_linear", "oracle_gelu", "oracle_swa_attention",
-              "oracle_add3", "oracle_rmsnorm", "oracle_swiglu", "oracle_quantize_e4m3_rows"):
+              "oracle_add3", "oracle_rmsnorm", "oracle_swiglu", "oracle_quantize_e4m3_rows",
+              "oracle_norm_backward", "oracle_gelu_backward", "oracle_swiglu_backward",
+              "oracle_swa_attention_backward"):
         getattr(lib, f).restype = None
     return lib
 
@@ -220,6 +232,47 @@ def swa_attention(q, q_pos, k, v, k_pos, heads, head_dim, window, threads=0, lib
     lib.oracle_swa_attention(q.shape[0], _ptr(qp), _ptr(q), k.shape[0], _ptr(kp), _ptr(k),
                              _ptr(v), heads, head_dim, window, _ptr(out), threads)
     return out
+
+
+def norm_backward(x, gamma, dout, eps, rms=False, threads=0, lib=None):
+    """LayerNorm (or RMSNorm) backward: returns ``(dx, dgamma, dbeta)`` (dbeta None for
+    RMSNorm)."""
+    lib = lib or load()
+    x, g, do = _f64(x), _f64(gamma), _f64(dout)
+    rows, H = x.shape
+    dx, dg = np.empty_like(x), np.empty(H)
+    db = None if rms else np.empty(H)
+    lib.oracle_norm_backward(rows, H, _ptr(x), _ptr(g), _ptr(do), float(eps), int(rms),
+                             _ptr(dx), _ptr(dg), None if db is None else _ptr(db), threads)
+    return dx, dg, db
+
+
+def gelu_backward(z, dout, threads=0, lib=None) -> np.ndarray:
+    lib = lib or load()
+    z, do = _f64(z), _f64(dout)
+    out = np.empty_like(z)
+    lib.oracle_gelu_backward(z.size, _ptr(z), _ptr(do), _ptr(out), threads)
+    return out
+
+
+def swiglu_backward(gate, up, dout, threads=0, lib=None):
+    """Returns ``(dgate, dup)`` for ``out = silu(gate) * up``."""
+    lib = lib or load()
+    gate, up, do = _f64(gate), _f64(up), _f64(dout)
+    dg, du = np.empty_like(gate), np.empty_like(up)
+    lib.oracle_swiglu_backward(gate.size, _ptr(gate), _ptr(up), _ptr(do), _ptr(dg), _ptr(du),
+                               threads)
+    return dg, du
+
+
+def swa_attention_backward(q, k, v, dout, heads, head_dim, window, threads=0, lib=None):
+    """Backward of the sliding-window attention of one whole sequence: ``(dq, dk, dv)``."""
+    lib = lib or load()
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    lib.oracle_swa_attention_backward(q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(do), heads,
+                                      head_dim, window, _ptr(dq), _ptr(dk), _ptr(dv), threads)
+    return dq, dk, dv
 
 
 # ----------------------------------------------------------------------------- the block
@@ -402,3 +455,87 @@ def stack_forward(dims: Dims, x, layers: list, prefix: int | None = None, thread
     for p in layers:
         x = block_forward(dims, x, p, threads=threads, lib=lib)
     return x
+
+
+# ----------------------------------------------------------------------------- backward
+
+
+def block_backward(dims: Dims, x, params: dict, dy, threads: int = 0, lib=None,
+                   keep_stages: bool = False):
+    """Gradients of the parallel block (eq. (4)) for an upstream gradient ``dy [B, S, H]``,
+    in float64, by the chain rule through the forward's steps in reverse:
+
+    1. ``y = x + attn Wo + b_o + act(h) W2 + b2``: ``d_attn = dy Wo^T``, ``d_act = dy W2^T``,
+       ``dWo = attn^T dy``, ``dW2 = act^T dy``, ``db_o = db2 = sum_t dy``.
+    2. the MLP activation: ``dh = d_act * gelu'(h)`` (SwiGLU: the gate and up parts).
+    3. the attention, per sequence: ``(dq, dk, dv)`` from its definition (the probabilities
+       are recomputed from q and k, as the pages' selective recomputation does).
+    4. ``[q | k | v | h] = xn [Wqkv | W1] + b``: ``dxn = dq Wq^T + dk Wk^T + dv Wv^T + dh W1^T``,
+       ``dWqkv = xn^T [dq | dk | dv]``, ``dW1 = xn^T dh``, biases the column sums.
+    5. the shared normalisation: ``dx = dy + LN'(x)^T dxn`` (both branches and the residual
+       meet here), ``dgamma``, ``dbeta``.
+
+    Returns a dict with ``dx [B, S, H]`` and one entry per parameter of ``params`` (the
+    same names and shapes; ``ln_beta`` is None for RMSNorm). ``keep_stages=True`` also
+    returns ``d_attn, d_act, dh, dq, dk, dv, dxn`` ([T, .] each).
+    """
+    lib = lib or load()
+    B, S, H = dims.batch, dims.seq, dims.hidden
+    nh, dh_, F, w = dims.heads, dims.head_dim, dims.ffn, dims.window
+    T = B * S
+    X = _f64(np.asarray(x).reshape(T, H))
+    dY = _f64(np.asarray(dy).reshape(T, H))
+    gamma, beta = _param(params, "ln_gamma"), _param(params, "ln_beta")
+    wqkv, w1 = _f64(params["wqkv"]), _f64(params["w1"])
+    wo, w2 = _f64(params["wo"]), _f64(params["w2"])
+    bqkv, b1 = _param(params, "b_qkv"), _param(params, "b1")
+    glu = dims.variant == 1
+
+    # forward, keeping what the backward reads
+    xn = _norm(dims, X, gamma, beta, threads, lib)
+    qkv = linear(xn, wqkv, bqkv, threads, lib)
+    q, k, v = qkv[:, :H], qkv[:, H:2 * H], qkv[:, 2 * H:]
+    h = linear(xn, w1, b1, threads, lib)
+    pos = np.arange(S, dtype=np.int64)
+    attn = np.concatenate([swa_attention(q[b * S:(b + 1) * S], pos, k[b * S:(b + 1) * S],
+                                         v[b * S:(b + 1) * S], pos, nh, dh_, w, threads, lib)
+                           for b in range(B)])
+    act = _mlp_act(dims, h, threads, lib)
+
+    # 1. the two output projections and the residual
+    d_attn = linear(dY, wo.T, None, threads, lib)
+    d_act = linear(dY, w2.T, None, threads, lib)
+    g = {"wo": linear(attn.T, dY, None, threads, lib), "w2": linear(act.T, dY, None, threads, lib)}
+    if params.get("b_o") is not None:
+        g["b_o"] = dY.sum(axis=0)
+    if params.get("b2") is not None:
+        g["b2"] = dY.sum(axis=0)
+    # 2. the MLP activation
+    if glu:
+        dgate, dup = swiglu_backward(h[:, :F], h[:, F:], d_act, threads, lib)
+        dh = np.concatenate([dgate, dup], axis=1)
+    else:
+        dh = gelu_backward(h, d_act, threads, lib)
+    # 3. the attention, per sequence
+    dq, dk, dv = (np.empty((T, H)) for _ in range(3))
+    for b in range(B):
+        r = slice(b * S, (b + 1) * S)
+        dq[r], dk[r], dv[r] = swa_attention_backward(q[r], k[r], v[r], d_attn[r], nh, dh_, w,
+                                                     threads, lib)
+    dqkv = np.concatenate([dq, dk, dv], axis=1)
+    # 4. the input projections
+    g["wqkv"] = linear(xn.T, dqkv, None, threads, lib)
+    g["w1"] = linear(xn.T, dh, None, threads, lib)
+    if bqkv is not None:
+        g["b_qkv"] = dqkv.sum(axis=0)
+    if b1 is not None:
+        g["b1"] = dh.sum(axis=0)
+    dxn = linear(dqkv, wqkv.T, None, threads, lib) + linear(dh, w1.T, None, threads, lib)
+    # 5. the shared normalisation and the residual
+    dx_norm, g["ln_gamma"], dbeta = norm_backward(X, gamma, dxn, dims.ln_eps, glu, threads, lib)
+    g["ln_beta"] = None if glu else dbeta
+    g["dx"] = (dY + dx_norm).reshape(B, S, H)
+    if keep_stages:
+        g["stages"] = {"d_attn": d_attn, "d_act": d_act, "dh": dh, "dq": dq, "dk": dk, "dv": dv,
+                       "dxn": dxn}
+    return g

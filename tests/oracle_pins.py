@@ -23,7 +23,12 @@ What pins what:
   torch;
 * the serial block of eq. (3): restated with torch routines, equal to the parallel
   block when either branch's output weight is zero, and first-order in the attention
-  term when compared with the parallel block.
+  term when compared with the parallel block;
+* the backward pass: central finite differences of the pinned forward at random entries
+  of x and of every parameter (both block variants), torch autograd through the torch
+  restatements, closed forms of gelu' and silu' (normal table, sigmoid(ln 3) = 3/4), the
+  normalisation's invariants (dx orthogonal to ones and to xhat) and softmax's (each
+  head's key gradients sum to zero; window 1 passes dout to dv and nothing to q, k).
 """
 
 from __future__ import annotations
@@ -649,6 +654,170 @@ def pin_block_fp8_rows_mode(lib):
     return _close(part, np.concatenate([full[b][rows[b]] for b in (0, 1)]), 1e-13)
 
 
+# ----------------------------------------------------------------------------- backward
+# The block's backward pass (training; performance notes "MFU": the backward is 4 of the 6
+# FLOPs per weight and token). Pinned by central finite differences of the pinned forward,
+# by torch autograd through the torch restatements above, by closed forms of the
+# activation derivatives and by invariants of the normalisation and of softmax.
+
+PHI_1 = 0.24197072451914337  # standard normal density at 1, from a printed normal table
+
+
+def pin_gelu_backward_closed_form(lib):
+    z = np.array([0.0, 1.0, -1.0])
+    want = np.array([0.5, NORMAL_TABLE[1.0] + PHI_1, NORMAL_TABLE[-1.0] - PHI_1])
+    return _close(O.gelu_backward(z, np.ones(3), lib=lib), want, 1e-14)
+
+
+def pin_swiglu_backward_closed_form(lib):
+    # sigmoid(ln 3) = 3/4: silu(ln 3) = 3 ln3 / 4, silu'(ln 3) = 3/4 (1 + ln3 / 4)
+    g, u, d = np.array([math.log(3.0)]), np.array([2.0]), np.array([-1.5])
+    dg, du = O.swiglu_backward(g, u, d, lib=lib)
+    want_du = -1.5 * 0.75 * math.log(3.0)
+    want_dg = -1.5 * 2.0 * 0.75 * (1.0 + math.log(3.0) / 4.0)
+    return _close([dg[0], du[0]], [want_dg, want_du], 1e-14)
+
+
+def pin_norm_backward_invariants(lib):
+    # LayerNorm's output ignores a shift and a scale of its input row, so dx is orthogonal
+    # to the all-ones row and to xhat; RMSNorm's only to xhat (a scale). Also against torch.
+    x = _rng(300).normal(1.0, 2.0, size=(5, 24))
+    gam, do = 1 + 0.2 * _rng(301).normal(size=24), _rng(302).normal(size=(5, 24))
+    # (exact only without eps, which breaks the scale invariance by eps / var)
+    ok, det = True, []
+    for rms in (False, True):
+        dx = O.norm_backward(x, gam, do, 0.0, rms, lib=lib)[0]
+        mu = 0.0 if rms else x.mean(axis=1, keepdims=True)
+        xhat = (x - mu) / np.sqrt(((x - mu) ** 2).mean(axis=1, keepdims=True))
+        ok &= bool(np.all(np.abs((dx * xhat).sum(axis=1)) < 1e-12))
+        if not rms:
+            ok &= bool(np.all(np.abs(dx.sum(axis=1)) < 1e-12))
+        dx, dg, db = O.norm_backward(x, gam, do, 1e-5, rms, lib=lib)
+        X = torch.tensor(x, requires_grad=True)
+        G = torch.tensor(gam, requires_grad=True)
+        out = F.rms_norm(X, (24,), G, 1e-5) if rms else F.layer_norm(X, (24,), G, None, 1e-5)
+        tx, tg = torch.autograd.grad((out * torch.tensor(do)).sum(), (X, G))
+        o1, d1 = _close(dx, tx.numpy(), 1e-12)
+        o2, d2 = _close(dg, tg.numpy(), 1e-12)
+        ok &= o1 and o2
+        if not rms:
+            ok &= _close(db, do.sum(axis=0), 1e-12)[0]
+        det.append(f"rms={rms}: {d1}, {d2}")
+    return ok, "; ".join(det)
+
+
+def pin_attention_backward_invariants(lib):
+    # softmax ignores a shift of its scores, so per query sum_j ds_j = 0 and the keys'
+    # gradients of one head sum to zero; window 1 attends to itself only: dq = dk = 0 and
+    # dv = dout; and against torch autograd through sdpa with the band mask.
+    S, nh, dh = 11, 2, 4
+    q, k, v = _qkv(310, S, nh, dh)
+    do = _rng(311).normal(size=(S, nh * dh))
+    ok, det = True, []
+    dq, dk, dv = O.swa_attention_backward(q, k, v, do, nh, dh, 1, lib=lib)
+    ok &= bool(np.all(dq == 0) and np.all(dk == 0)) and _close(dv, do, 0.0)[0]
+    for w in (2, 4, 11):
+        dq, dk, dv = O.swa_attention_backward(q, k, v, do, nh, dh, w, lib=lib)
+        ok &= bool(np.all(np.abs(dk.sum(axis=0)) < 1e-12))
+        Q, K, V = (torch.tensor(a.reshape(S, nh, dh).transpose(1, 0, 2), requires_grad=True)
+                   for a in (q, k, v))
+        o = F.scaled_dot_product_attention(Q, K, V, attn_mask=band_mask(S, w))
+        D = torch.tensor(do.reshape(S, nh, dh).transpose(1, 0, 2))
+        tq, tk, tv = (t.transpose(0, 1).reshape(S, nh * dh).numpy()
+                      for t in torch.autograd.grad((o * D).sum(), (Q, K, V)))
+        for a, b in ((dq, tq), (dk, tk), (dv, tv)):
+            o1, d1 = _close(a, b, 1e-12)
+            ok &= o1
+        det.append(f"w={w}: {d1}")
+    return ok, "; ".join(det)
+
+
+GRAD_NAMES = ["ln_gamma", "ln_beta", "wqkv", "w1", "wo", "w2", "b_qkv", "b1", "b_o", "b2"]
+
+
+def _grad_names(dims, p):
+    """Parameters with a gradient: RMSNorm has no beta."""
+    return [n for n in GRAD_NAMES
+            if p.get(n) is not None and not (dims.variant == 1 and n == "ln_beta")]
+
+
+def _bwd_case(variant, seed):
+    dims = O.Dims(2, 9, 8, 2, 4, 16, 4, variant=variant)
+    p = (swiglu_params if variant else tiny_params)(8, 2, 16, seed=seed)
+    x = _rng(seed + 1).normal(size=(2, 9, 8))
+    dy = _rng(seed + 2).normal(size=(2, 9, 8))
+    return dims, p, x, dy
+
+
+def pin_backward_finite_differences(lib, mod=O):
+    # central differences of L = sum(y * dy) through the pinned forward, at random entries
+    # of x and of every parameter
+    ok, det = True, []
+    for variant in (0, 1):
+        dims, p, x, dy = _bwd_case(variant, 320 + variant)
+        g = mod.block_backward(dims, x, p, dy, lib=lib)
+        L = lambda: float((O.block_forward(dims, x, p, lib=lib) * dy).sum())
+        r, eps, worst = _rng(330 + variant), 1e-6, 0.0
+        for name in ["x"] + _grad_names(dims, p):
+            a = x if name == "x" else p[name]
+            want = g["dx"] if name == "x" else g[name]
+            for _ in range(3):
+                idx = tuple(int(r.integers(0, n)) for n in a.shape)
+                old = a[idx]
+                a[idx] = old + eps
+                lp = L()
+                a[idx] = old - eps
+                lm = L()
+                a[idx] = old
+                err = abs((lp - lm) / (2 * eps) - want[idx]) / max(1.0, abs(want[idx]))
+                worst = max(worst, err)
+        ok &= worst < 1e-6
+        det.append(f"variant {variant}: worst relative {worst:.2e}")
+    return ok, "; ".join(det)
+
+
+def pin_backward_autograd(lib, mod=O):
+    # every gradient against torch autograd through torch_block / torch_block_swiglu
+    ok, det = True, []
+    for variant in (0, 1):
+        dims, p, x, dy = _bwd_case(variant, 340 + variant)
+        g = mod.block_backward(dims, x, p, dy, lib=lib)
+        names = _grad_names(dims, p)
+        leaves = {n: torch.tensor(np.asarray(p[n], dtype=np.float64), requires_grad=True)
+                  for n in names}
+        X = torch.tensor(x, requires_grad=True)
+        y = _torch_block_autograd(dims, X, leaves)
+        grads = torch.autograd.grad((y * torch.tensor(dy)).sum(), [X] + [leaves[n] for n in names])
+        worst = 0.0
+        for n, t in zip(["dx"] + names, grads):
+            a = g[n] if n != "dx" else g["dx"]
+            worst = max(worst, float(np.max(np.abs(np.asarray(a) - t.numpy()))))
+        ok &= worst < 1e-10
+        det.append(f"variant {variant}: max|diff| {worst:.2e}")
+    return ok, "; ".join(det)
+
+
+def _torch_block_autograd(dims, X, p):
+    """The block of torch_block / torch_block_swiglu on torch leaves (for autograd)."""
+    B, S, H, nh, dh, F_ = dims.batch, dims.seq, dims.hidden, dims.heads, dims.head_dim, dims.ffn
+    if dims.variant == 1:
+        xn = F.rms_norm(X, (H,), p["ln_gamma"], dims.ln_eps)
+    else:
+        xn = F.layer_norm(X, (H,), p["ln_gamma"], p["ln_beta"], dims.ln_eps)
+    qkv = xn @ p["wqkv"] + p["b_qkv"]
+    q, k, v = (qkv[..., i * H:(i + 1) * H].reshape(B, S, nh, dh).transpose(1, 2) for i in range(3))
+    a = F.scaled_dot_product_attention(q, k, v, attn_mask=band_mask(S, dims.window))
+    a = a.transpose(1, 2).reshape(B, S, H) @ p["wo"] + p["b_o"]
+    z = xn @ p["w1"] + p["b1"]
+    act = F.silu(z[..., :F_]) * z[..., F_:] if dims.variant == 1 else F.gelu(z, approximate="none")
+    return X + act @ p["w2"] + p["b2"] + a
+
+
+BACKWARD_PINS = [pin_gelu_backward_closed_form, pin_swiglu_backward_closed_form,
+                 pin_norm_backward_invariants, pin_attention_backward_invariants,
+                 pin_backward_finite_differences, pin_backward_autograd]
+
+
 ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_layernorm_library,
             pin_layernorm_stats, pin_linear_library, pin_attention_window1_is_v,
             pin_attention_window2_closed_form, pin_attention_full_causal,
@@ -661,4 +830,5 @@ ALL_PINS = [pin_gelu_table, pin_gelu_library, pin_layernorm_two_vector, pin_laye
             pin_swiglu_library, pin_block_swiglu_library, pin_block_swiglu_rows_mode,
             pin_e4m3_table, pin_e4m3_roundtrip_all_codes, pin_e4m3_ties_to_even,
             pin_e4m3_library, pin_e4m3_row_scaling, pin_block_fp8_library,
-            pin_block_fp8_rows_mode]
+            pin_block_fp8_rows_mode,
+            *BACKWARD_PINS]
