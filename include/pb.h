@@ -269,6 +269,16 @@ pb_status pb_gemm_scratch_bytes(size_t* bytes);
 pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const void* B, void* C,
                        void* scratch, size_t scratch_bytes, int* status, void* stream);
 
+/* pb_gemm_bf16 with either operand stored MN-major, the layouts of the backward pass's
+ * GEMMs (activations stored token-major are MN-major when the contraction runs over
+ * tokens): a_mn = 0: A is [M, K] (K contiguous), a_mn = 1: A is [K, M] (M contiguous);
+ * b_mn = 0: B is [N, K], b_mn = 1: B is [K, N]. C[m, n] = sum_k A(m, k) B(n, k), bf16.
+ * N % 32 == 0; a K-major operand needs K % 8 == 0, an MN-major one M (or N) % 8 == 0;
+ * a ragged last block of K is zero filled. Otherwise as pb_gemm_bf16. */
+pb_status pb_gemm_bf16_layout(int32_t M, int32_t N, int32_t K, const void* A, int32_t a_mn,
+                              const void* B, int32_t b_mn, void* C, void* scratch,
+                              size_t scratch_bytes, int* status, void* stream);
+
 /* pb_gemm_bf16 for callers that cannot allocate device memory: those capturing a CUDA
  * graph (cudaMalloc is not allowed during capture), plugins whose device memory belongs
  * to a host engine's allocator, and paths where an allocation could block. The pages have

@@ -47,6 +47,46 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
 }
 
+// d gelu / dz = Phi(z) + z phi(z), phi the standard normal density.
+__device__ __forceinline__ float gelu_erf_grad(float z) {
+  return 0.5f * (1.0f + erff(z * 0.70710678118654752f)) +
+         z * __expf(-0.5f * z * z) * 0.39894228040143268f;
+}
+
+template <int N>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16* src, float (&v)[N]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < N / 8; ++q) {
+    const uint4 u = s4[q];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      v[8 * q + 2 * e] = f.x;
+      v[8 * q + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+// n fp32 values to dst (16-byte aligned), added to what is there when accumulate.
+template <int N>
+__device__ __forceinline__ void store_f32(float* dst, const float* v, bool accumulate) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < N / 4; ++q) {
+    float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    if (accumulate) {
+      const float4 a = d[q];
+      o.x += a.x;
+      o.y += a.y;
+      o.z += a.z;
+      o.w += a.w;
+    }
+    d[q] = o;
+  }
+}
+
 template <bool F16>
 __device__ __forceinline__ void store_row32(void* dst, const float (&v)[32]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -137,35 +177,90 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
           ep.vt + (int64_t(b * ep.nh + head) * ep.dh + d0) * ep.seq_pad + s;
 #pragma unroll
       for (int i = 0; i < 32; ++i) dst[int64_t(i) * ep.seq_pad] = __float2bfloat16_rn(v[i]);
-    } else if (ep.glu) {
-      // [gate | up] of 16 MLP features -> silu(gate) * up, next to the attention output
-      // in the second GEMM's A operand
-      float o[16];
+    } else {
+      if (ep.hpre != nullptr)  // training forward: keep h for the backward
+        store_row32<false>(ep.hpre + int64_t(row) * (ep.N + ep.col_base - 3 * H) + (cc - 3 * H),
+                           v);
+      if (ep.glu) {
+        // [gate | up] of 16 MLP features -> silu(gate) * up, next to the attention output
+        // in the second GEMM's A operand
+        float o[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = v[i] / (1.0f + __expf(-v[i])) * v[16 + i];
-      const int64_t off = int64_t(row) * (H + ep.F) + H + (cc - 3 * H) / 2;
-      if (ep.act_f16) {
-        bool bad = false;
+        for (int i = 0; i < 16; ++i) o[i] = v[i] / (1.0f + __expf(-v[i])) * v[16 + i];
+        const int64_t off = int64_t(row) * (H + ep.F) + H + (cc - 3 * H) / 2;
+        if (ep.act_f16) {
+          bool bad = false;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) bad |= !(fabsf(o[i]) <= kF16Max);
-        if (bad) report_range(ep.status);
-        store_row16<true>(static_cast<__half*>(ep.act) + off, o);
-      } else {
-        store_row16<false>(static_cast<__nv_bfloat16*>(ep.act) + off, o);
+          for (int i = 0; i < 16; ++i) bad |= !(fabsf(o[i]) <= kF16Max);
+          if (bad) report_range(ep.status);
+          store_row16<true>(static_cast<__half*>(ep.act) + off, o);
+        } else {
+          store_row16<false>(static_cast<__nv_bfloat16*>(ep.act) + off, o);
+        }
+      } else {  // h -> GeLU(h), next to the attention output in the second GEMM's A operand
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+        const int64_t off = int64_t(row) * (H + ep.F) + H + (cc - 3 * H);
+        if (ep.act_f16) {
+          bool bad = false;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) bad |= !(fabsf(v[i]) <= kF16Max);
+          if (bad) report_range(ep.status);
+          store_row32<true>(static_cast<__half*>(ep.act) + off, v);
+        } else {
+          store_row32<false>(static_cast<__nv_bfloat16*>(ep.act) + off, v);
+        }
       }
-    } else {  // h -> GeLU(h), next to the attention output in the second GEMM's A operand
+    }
+  } else if (KIND == kEpiBwdAct) {
+    const int H = ep.H;
+    if (col0 < H) {  // d_attn = dy Wo^T
+      store_row32<false>(ep.d_attn + int64_t(row) * H + col0, v);
+      return;
+    }
+    const int f0 = col0 - H;  // MLP feature of the first column
+    const __nv_bfloat16* hp = ep.hpre + int64_t(row) * (ep.glu ? 2 * ep.F : ep.F);
+    __nv_bfloat16* dz = ep.dz + int64_t(row) * ep.ldz + 3 * H;
+    if (!ep.glu) {
+      float h[32];
+      load_bf16<32>(hp + f0, h);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-      const int64_t off = int64_t(row) * (H + ep.F) + H + (cc - 3 * H);
-      if (ep.act_f16) {
-        bool bad = false;
+      for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
+      store_row32<false>(dz + f0, v);
+    } else {
+      // features f0 .. f0 + 31 are the interleave groups f0 / 16 and f0 / 16 + 1: W1cat
+      // columns [2 f0, 2 f0 + 64), 16 gate then 16 up values each
 #pragma unroll
-        for (int i = 0; i < 32; ++i) bad |= !(fabsf(v[i]) <= kF16Max);
-        if (bad) report_range(ep.status);
-        store_row32<true>(static_cast<__half*>(ep.act) + off, v);
-      } else {
-        store_row32<false>(static_cast<__nv_bfloat16*>(ep.act) + off, v);
+      for (int half = 0; half < 2; ++half) {
+        const int c = 2 * f0 + 32 * half;
+        float g[16], u[16], dg[16], du[16];
+        load_bf16<16>(hp + c, g);
+        load_bf16<16>(hp + c + 16, u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d = v[16 * half + i];
+          const float sg = 1.0f / (1.0f + __expf(-g[i]));
+          du[i] = d * g[i] * sg;
+          dg[i] = d * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+        }
+        store_row16<false>(dz + c, dg);
+        store_row16<false>(dz + c + 16, du);
       }
+    }
+  } else if (KIND == kEpiGrad) {
+    if (row >= ep.split_row) {
+      store_f32<32>(ep.g1 + int64_t(row - ep.split_row) * ep.ld1 + col0, v, ep.accumulate);
+    } else if (col0 >= ep.split_col) {
+      const int c = col0 - ep.split_col;
+      float* base = ep.g1 + int64_t(row) * ep.ld1;
+      if (ep.glu) {  // undo the W1cat interleave: 16 gate then 16 up features
+        store_f32<16>(base + c / 2, v, ep.accumulate);
+        store_f32<16>(base + ep.F + c / 2, v + 16, ep.accumulate);
+      } else {
+        store_f32<32>(base + c, v, ep.accumulate);
+      }
+    } else {
+      store_f32<32>(ep.g0 + int64_t(row) * ep.ld0 + col0, v, ep.accumulate);
     }
   } else {  // kEpiResidual: y = D + bias + x
     const int64_t off = int64_t(row) * ep.N + col0;
@@ -269,7 +364,7 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-template <int KIND, int OP>
+template <int KIND, int OP, int LAYOUT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int K, const EpiParams ep, const SkParams sk, int* status, uint64_t limit_ns) {
@@ -325,7 +420,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   sc.num_m = (ep.M + PM - 1) / PM;
   sc.num_n = (ep.N + BN - 1) / BN;
   constexpr int BKE = OP == kOpE4m3 ? kGemmBK8 : BK;  // K elements per stage (128 bytes)
-  sc.num_kb = K / BKE;
+  constexpr bool AMN = (LAYOUT & kMK) != 0, BMN = (LAYOUT & kKM) != 0;
+  static_assert(!(AMN || BMN) || OP != kOpE4m3, "MN-major operands are 16-bit");
+  sc.num_kb = (K + BKE - 1) / BKE;  // a ragged last block is zero filled by TMA
   sc.cluster = int(blockIdx.x) >> 1;
   sc.clusters = int(gridDim.x) >> 1;
   sc.dp_tiles = sk.dp_tiles;
@@ -361,8 +458,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           // its arrival. The odd CTA reuses a stage only after the pair's MMAs read it, so
           // its copies always count toward the phase the MMA issuer waits for next.
           if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
-          tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, kb * BKE, m0);
-          tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, kb * BKE, n0);
+          // K-major: one box of 128 rows x 64 K; MN-major: two boxes of 64 K-rows x 64
+          // elements of M (or N), 8 KB apart
+          if (AMN) {
+            tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, m0, kb * BKE);
+            tma_load_2d_pair(sa + A_BYTES / 2, &tmA, full_pair0 + 8 * stage, m0 + 64, kb * BKE);
+          } else {
+            tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, kb * BKE, m0);
+          }
+          if (BMN) {
+            tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, n0, kb * BKE);
+            tma_load_2d_pair(sa + A_BYTES + B_BYTES / 2, &tmB, full_pair0 + 8 * stage, n0 + 64,
+                             kb * BKE);
+          } else {
+            tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, kb * BKE, n0);
+          }
           last_par[stage] = phase;
           used |= 1u << stage;
           if (++stage == STAGES) {
@@ -381,7 +491,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_f32acc(PM, BN, OP != kOpBf16);
+      const uint32_t idesc = idesc_f32acc(PM, BN, OP != kOpBf16, AMN, BMN);
+      // descriptor start-address step of one MMA (K = 16 or 32 elements, 32 bytes):
+      // along a swizzled row (K-major) or two 1024-byte atoms on (MN-major), in 16 B units
+      constexpr uint64_t kStepA = AMN ? 128 : 2, kStepB = BMN ? 128 : 2;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -400,15 +513,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + size_t(stage) * STAGE_BYTES);
-          const uint64_t da = sdesc_kmajor_sw128(sa);
-          const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
+          const uint64_t da =
+              AMN ? sdesc_mnmajor_sw128(sa, A_BYTES / 2) : sdesc_kmajor_sw128(sa);
+          const uint64_t db = BMN ? sdesc_mnmajor_sw128(sa + A_BYTES, B_BYTES / 2)
+                                  : sdesc_kmajor_sw128(sa + A_BYTES);
           // four products of 32 bytes of K each: K = 16 (16-bit) or 32 (FP8) elements
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (OP == kOpE4m3)
-              mma_f8kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb > u.kb0) || k > 0);
+              mma_f8kind_ss_pair(d_tmem, da + kStepA * k, db + kStepB * k, idesc,
+                                 (kb > u.kb0) || k > 0);
             else
-              mma_f16kind_ss_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb > u.kb0) || k > 0);
+              mma_f16kind_ss_pair(d_tmem, da + kStepA * k, db + kStepB * k, idesc,
+                                  (kb > u.kb0) || k > 0);
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
@@ -551,7 +668,7 @@ uint64_t next_epoch() {
   return e == 0 ? ++counter : e;
 }
 
-template <int KIND, int OP>
+template <int KIND, int OP, int LAYOUT = kKK>
 cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
                         void* sk_scratch, cudaStream_t stream) {
@@ -568,12 +685,12 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   cfg.attrs = at;
   cfg.numAttrs = 1;
   if (max_clusters < 0) {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<KIND, OP>,
+    attr_err = cudaFuncSetAttribute(gemm_kernel<KIND, OP, LAYOUT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
     if (attr_err == cudaSuccess) {
       cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
       int n = 0;
-      attr_err = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, OP>, &cfg);
+      attr_err = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, OP, LAYOUT>, &cfg);
       max_clusters = (attr_err == cudaSuccess && n > 0) ? n : 0;
     }
   }
@@ -581,7 +698,8 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
   const int tiles = ((M + PM - 1) / PM) * ((N + BN - 1) / BN);
   const int clusters = tiles < max_clusters ? tiles : max_clusters;
-  const int num_kb = K / (OP == kOpE4m3 ? kGemmBK8 : BK);
+  const int bke = OP == kOpE4m3 ? kGemmBK8 : BK;
+  const int num_kb = (K + bke - 1) / bke;
   // Stream-K for the last waves when they would leave pairs idle: every full wave but one
   // runs whole tiles; the remaining (clusters + rem) tiles are split evenly along K.
   SkParams sk{};
@@ -603,7 +721,7 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   e.N = N;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, OP>, tmA, tmB, K, e, sk, status, limit_ns);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, OP, LAYOUT>, tmA, tmB, K, e, sk, status, limit_ns);
 }
 
 }  // namespace
@@ -653,8 +771,36 @@ cudaError_t launch_gemm(EpiKind kind, OpType op, const CUtensorMap& tmA, const C
       PB_GEMM_CASE(kEpiBlockIn);
     case kEpiResidual:
       PB_GEMM_CASE(kEpiResidual);
+    default:
+      break;
   }
 #undef PB_GEMM_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_layout(EpiKind kind, GemmLayout layout, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, int M, int N, int K, const EpiParams& ep,
+                               int num_sms, int* status, uint64_t limit_ns, void* sk_scratch,
+                               cudaStream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  // a K-major operand's rows are K elements: TMA wants a 16-byte multiple
+  if (layout != kMM && K % 8 != 0) return cudaErrorInvalidValue;
+#define PB_GEMM_LAYOUT(KIND_, LAYOUT_)                                                        return launch_kind<KIND_, kOpBf16, LAYOUT_>(tmA, tmB, M, N, K, ep, num_sms, status,                                                     limit_ns, sk_scratch, stream)
+  if (kind == kEpiStore) {
+    switch (layout) {
+      case kKK: PB_GEMM_LAYOUT(kEpiStore, kKK);
+      case kMK: PB_GEMM_LAYOUT(kEpiStore, kMK);
+      case kKM: PB_GEMM_LAYOUT(kEpiStore, kKM);
+      case kMM: PB_GEMM_LAYOUT(kEpiStore, kMM);
+    }
+  } else if (kind == kEpiBwdAct && layout == kKM) {
+    PB_GEMM_LAYOUT(kEpiBwdAct, kKM);
+  } else if (kind == kEpiGrad && layout == kKM) {
+    PB_GEMM_LAYOUT(kEpiGrad, kKM);
+  } else if (kind == kEpiGrad && layout == kMM) {
+    PB_GEMM_LAYOUT(kEpiGrad, kMM);
+  }
+#undef PB_GEMM_LAYOUT
   return cudaErrorInvalidValue;
 }
 

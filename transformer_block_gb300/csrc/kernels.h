@@ -35,7 +35,13 @@ enum EpiKind : int {
   kEpiStore = 0,     // C = bf16(D)
   kEpiBlockIn = 1,   // D = xn [Wqkv | W1]: route q|k, v (transposed per head), GeLU(h)
   kEpiResidual = 2,  // y = bf16(D + bias + x)
+  kEpiBwdAct = 3,    // D = dy [Wo ; W2]^T: d_attn (bf16), and dh = D * act'(h) into dz
+  kEpiGrad = 4,      // fp32 gradient store (or accumulate), split by rows or columns
 };
+
+// Operand layouts: bit 0 set = A is MN-major (stored [K, M], M contiguous), bit 1 = B is
+// MN-major ([K, N]). K-major operands are [M, K] / [N, K], K contiguous.
+enum GemmLayout : int { kKK = 0, kMK = 1, kKM = 2, kMM = 3 };
 
 struct EpiParams {
   int M, N;
@@ -67,6 +73,25 @@ struct EpiParams {
   void* y;            // [M, N], fp32 if y_f32 else bf16
   bool resid_f32;
   bool y_f32;
+  // kEpiBlockIn: when set, the pre-activation h (after its bias) is also stored here,
+  // [T, N - 3H] bf16 in W1cat row order (training forward). kEpiBwdAct reads it back.
+  __nv_bfloat16* hpre;
+  // kEpiBwdAct (N = H + F): columns [0, H) are d_attn = dy Wo^T -> d_attn [T, H] bf16;
+  // column H + f is d act_f = dy W2^T -> dh = d act_f * gelu'(h_f) at dz column 3H + f
+  // (SwiGLU: d gate and d up at the W1cat-order columns of feature f), dz row stride ldz.
+  __nv_bfloat16* d_attn;
+  __nv_bfloat16* dz;
+  int64_t ldz;
+  // kEpiGrad: D[m, n] -> g0[m * ld0 + n] while m < split_row and n < split_col; rows from
+  // split_row on -> g1[(m - split_row) * ld1 + n]; columns from split_col on ->
+  // g1[m * ld1 + (n - split_col)], with glu the W1cat interleave undone (column
+  // split_col + 32t + i is gate feature 16t + i for i < 16, else up feature F + 16t + i - 16).
+  // accumulate: add to what is there (fp32 gradient accumulation).
+  float* g0;
+  float* g1;
+  int64_t ld0, ld1;
+  int split_row, split_col;
+  bool accumulate;
 };
 
 // Stream-K work space: the tiles of the last waves are split along K across all CTA
@@ -84,6 +109,13 @@ size_t gemm_smem_bytes();
 cudaError_t launch_gemm(EpiKind kind, OpType op, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         int M, int N, int K, const EpiParams& ep, int num_sms, int* status,
                         uint64_t limit_ns, void* sk_scratch, cudaStream_t stream);
+// bf16 operands in the given layout. An MN-major operand's tensor map is [K rows, M (or N)
+// columns] in boxes of 64 x 64; K need not be a multiple of 64 (the last block is zero
+// filled). Kinds: kEpiStore (any layout), kEpiBwdAct and kEpiGrad (kKM, kMM).
+cudaError_t launch_gemm_layout(EpiKind kind, GemmLayout layout, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, int M, int N, int K, const EpiParams& ep,
+                               int num_sms, int* status, uint64_t limit_ns, void* sk_scratch,
+                               cudaStream_t stream);
 
 // ---------------------------------------------------------------- attention (swa.cu)
 struct SwaParams {

@@ -967,6 +967,42 @@ pb_status pb_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, const voi
   return PB_OK;
 }
 
+pb_status pb_gemm_bf16_layout(int32_t M, int32_t N, int32_t K, const void* A, int32_t a_mn,
+                              const void* B, int32_t b_mn, void* C, void* scratch,
+                              size_t scratch_bytes, int* status, void* stream) {
+  if (M < 1 || N < 1 || K < 1) return fail(PB_ERR_INVALID_ARG, "M, N, K must be >= 1");
+  if (N % 32 != 0) return fail(PB_ERR_UNSUPPORTED, "gemm needs N %% 32 == 0");
+  if ((!a_mn || !b_mn) && K % 8 != 0)
+    return fail(PB_ERR_UNSUPPORTED, "a K-major operand needs K %% 8 == 0");
+  if ((a_mn && M % 8 != 0) || (b_mn && N % 8 != 0))
+    return fail(PB_ERR_UNSUPPORTED, "an MN-major operand needs M (or N) %% 8 == 0");
+  if (A == nullptr || B == nullptr || C == nullptr || !aligned(A, 16) || !aligned(B, 16) ||
+      !aligned(C, 16))
+    return fail(PB_ERR_INVALID_ARG, "A, B, C must be 16-byte aligned device pointers");
+  if (scratch != nullptr && (!aligned(scratch, 256) || scratch_bytes < pb::kSkScratchBytes))
+    return fail(PB_ERR_WORKSPACE, "scratch must be NULL or 256-byte aligned with >= %zu bytes",
+                pb::kSkScratchBytes);
+  int dev = -1, sms = 0;
+  PB_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  PB_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+          "cudaDeviceGetAttribute");
+  CUtensorMap ta, tb;
+  pb_status s = a_mn ? make_map_2d(&ta, A, uint64_t(K), uint64_t(M), uint64_t(M), 64)
+                     : make_map_2d(&ta, A, uint64_t(M), uint64_t(K), uint64_t(K), pb::kGemmBoxRows);
+  if (s == PB_OK)
+    s = b_mn ? make_map_2d(&tb, B, uint64_t(K), uint64_t(N), uint64_t(N), 64)
+             : make_map_2d(&tb, B, uint64_t(N), uint64_t(K), uint64_t(K), pb::kGemmBoxRows);
+  if (s != PB_OK) return s;
+  EpiParams ep{};
+  ep.c = static_cast<__nv_bfloat16*>(C);
+  ep.ldc = N;
+  const pb::GemmLayout layout = pb::GemmLayout((a_mn ? pb::kMK : 0) | (b_mn ? pb::kKM : 0));
+  PB_CUDA(pb::launch_gemm_layout(pb::kEpiStore, layout, ta, tb, M, N, K, ep, sms, status,
+                                 kDefaultLimitNs, scratch, static_cast<cudaStream_t>(stream)),
+          "gemm launch");
+  return PB_OK;
+}
+
 pb_status pb_swa_attention(const pb_dims* dims, const void* qk, const void* vt, void* act,
                            int64_t act_ld, int* status, void* stream) {
   pb_status s = check_dims(dims);

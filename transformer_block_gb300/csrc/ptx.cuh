@@ -315,12 +315,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Instruction descriptor of kind::f16: A and B both bf16 (or both fp16 when f16), both
-// K-major, fp32 D, M x N.
-__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool f16 = false) {
+// Instruction descriptor of kind::f16: A and B both bf16 (or both fp16 when f16), each
+// K-major unless a_mn / b_mn, fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool f16 = false,
+                                                   bool a_mn = false, bool b_mn = false) {
   return (1u << 4)                                   // D format: f32
          | ((f16 ? 0u : 1u) << 7)                    // A format: f16 = 0, bf16 = 1
          | ((f16 ? 0u : 1u) << 10)                   // B format
+         | ((a_mn ? 1u : 0u) << 15)                  // A is MN-major
+         | ((b_mn ? 1u : 0u) << 16)                  // B is MN-major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
@@ -338,6 +341,19 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
          | (64ull << 32)                                 // stride byte offset: 1024 B
          | (1ull << 46)                                  // descriptor version
          | (2ull << 61);                                 // 128-byte swizzle
+}
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte-swizzled layout a TMA
+// box of 64 16-bit elements (128 bytes) of M or N x r rows of K writes: swizzle atoms of
+// 8 K-rows x 128 bytes, consecutive along K (1024 bytes apart: the stride dimension
+// offset), and the next 64 elements of M or N `mn_block_bytes` further on (the leading
+// dimension offset). One MMA of K = 16 reads two atoms; the next starts 2048 bytes on.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)       // start address
+         | (static_cast<uint64_t>(mn_block_bytes >> 4) << 16)  // leading byte offset
+         | (64ull << 32)                                      // stride byte offset: 1024 B
+         | (1ull << 46)                                       // descriptor version
+         | (2ull << 61);                                      // 128-byte swizzle
 }
 
 // 32 lanes x 32 consecutive 32-bit columns of tensor memory -> 32 registers per thread

@@ -82,6 +82,8 @@ SIGNATURES = {
     "pb_quantize_rows_e4m3": (ctypes.c_int, [_I64, _I32, _P, _P, _P, _P]),
     "pb_gemm_scratch_bytes": (ctypes.c_int, [ctypes.POINTER(_S)]),
     "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _S, _P, _P]),
+    "pb_gemm_bf16_layout": (ctypes.c_int, [_I32, _I32, _I32, _P, _I32, _P, _I32, _P, _P, _S, _P,
+                                           _P]),
     "pb_swa_attention": (ctypes.c_int, [_DP, _P, _P, _P, _I64, _P, _P]),
     "pb_wait_probe": (ctypes.c_int, [_U64, _P, _P]),
     "pb_gemm_bf16_static": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
@@ -309,6 +311,21 @@ def gemm(a, b, out=None, scratch=None, status=None, stream=None):
     nbytes = 0 if scratch is None else scratch.numel()
     _check("pb_gemm_bf16", lib().pb_gemm_bf16(M, N, K, _ptr(a), _ptr(b), _ptr(out), _ptr(scratch),
                                               nbytes, _ptr(status), _stream(stream)))
+    return out
+
+
+def gemm_layout(a, b, a_mn=False, b_mn=False, out=None, scratch=None, status=None,
+                stream=None):
+    """``C[m, n] = sum_k A(m, k) B(n, k)`` -> bf16 ``[M, N]`` with ``a`` stored ``[M, K]``
+    (or ``[K, M]`` when ``a_mn``) and ``b`` stored ``[N, K]`` (or ``[K, N]`` when ``b_mn``)."""
+    M, K = (a.shape[1], a.shape[0]) if a_mn else a.shape
+    N = b.shape[1] if b_mn else b.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    nbytes = 0 if scratch is None else scratch.numel()
+    _check("pb_gemm_bf16_layout",
+           lib().pb_gemm_bf16_layout(M, N, K, _ptr(a), int(a_mn), _ptr(b), int(b_mn), _ptr(out),
+                                     _ptr(scratch), nbytes, _ptr(status), _stream(stream)))
     return out
 
 
