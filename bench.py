@@ -54,6 +54,9 @@ def parse():
                     help="instead of the contract line, time the parallel block (eq. (4)) and "
                          "the serial block (eq. (3)) on the same weights, one GPU, and print "
                          "one JSON line with both")
+    ap.add_argument("--train", action="store_true",
+                    help="instead of the contract line, time one training step of a single "
+                         "block (pb_forward_train + pb_backward) and print one JSON line")
     ap.add_argument("--operands", default="bf16", choices=["bf16", "fp16", "fp8"],
                     help="operand type of the GEMMs (fp8: E4M3 with per-row / per-channel "
                          "current scaling, not the reference precision)")
@@ -286,6 +289,66 @@ def run_ab_serial(args, wl) -> int:
     return 0
 
 
+def run_train(args, wl) -> int:
+    """One training step of one block: pb_forward_train then pb_backward, same weights and
+    inputs every step, upstream gradient seeded N(0, 1). Model FLOPs of the step are three
+    times the forward's (the performance notes' 6ND: forward 2, backward 4 per weight and
+    token; the attention backward counted as twice its forward, the recomputed scores not
+    counted). Forward and backward are timed apart with CUDA events on the stream."""
+    import torch
+
+    from transformer_block_gb300 import flops, inputs, pb
+
+    if wl.layers != 1:
+        raise SystemExit("--train times one block: pick a single-layer workload")
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    x, params = inputs.make_layer(wl, 0, device="cuda")
+    dims = pb.make_dims(wl)
+    block = pb.ParallelBlock(dims, params)
+    del params
+    torch.cuda.empty_cache()
+    scratch = pb.new_train_scratch(dims)
+    y = torch.empty_like(x)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    dy = torch.randn(x.shape, generator=g, device="cuda").to(torch.bfloat16)
+    grads = None
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        block.forward_train(x, scratch, y=y)
+        grads = block.backward(x, dy, scratch, grads=grads)
+    torch.cuda.synchronize()
+    if block.status() != pb.PB_OK:
+        raise RuntimeError("device status word reports an error after warm-up")
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        block.forward_train(x, scratch, y=y)
+        ev[2 * i + 1].record(stream)
+        grads = block.backward(x, dy, scratch, grads=grads)
+        ev[2 * i + 2].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if block.status() != pb.PB_OK:
+        raise RuntimeError("device status word reports an error in the timed region")
+    fwd = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)) / args.steps
+    bwd = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps)) / args.steps
+    model = flops.model_flops(wl)
+    line = {"metric": "parallel-block training step (fwd + bwd) TFLOP/s, 1 GPU",
+            "value": 3 * model / ((fwd + bwd) * 1e-3) / 1e12, "unit": UNIT,
+            "higher_is_better": True, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": fwd + bwd, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl, args),
+            "forward": {"ms": fwd, "tflops": model / (fwd * 1e-3) / 1e12},
+            "backward": {"ms": bwd, "tflops": 2 * model / (bwd * 1e-3) / 1e12},
+            "mfu_vs_spec_dense_bf16": 3 * model / ((fwd + bwd) * 1e-3) / 1e12 / SPEC_BF16_TFLOPS,
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     from transformer_block_gb300 import BENCH_WORKLOAD, WORKLOADS
@@ -295,6 +358,8 @@ def main():
         return run_reference(args, wl)
     if args.ab_serial:
         return run_ab_serial(args, wl)
+    if args.train:
+        return run_train(args, wl)
 
     import torch
     import torch.distributed as dist

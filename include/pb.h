@@ -114,7 +114,19 @@ typedef struct pb_weights {
  *   io   [T, H]          bf16 staging of the host-buffer entry point
  *   res0, res1 [T, H]    fp32 residual stream between the layers of a stack
  *   sk                   stream-K partial tiles (fp32) and flags of the two GEMMs
- * T = batch * seq. */
+ * T = batch * seq, F' = F (GeLU) or 2F (SwiGLU).
+ * A training scratch (pb_forward_train / pb_backward, train_total bytes) has the same
+ * regions up to `total`, then:
+ *   hpre   [T, F']       h before the activation (bf16; SwiGLU: W1cat's interleaved order)
+ *   lse    [batch, heads, seq]  fp32 log2-sum-exp of each attention row's scores x
+ *                        log2(e) / sqrt(dh)
+ *   d_attn [T, H]        dL/d(attention output) (bf16)
+ *   delta  [batch, heads, seq]  fp32 dO . O per row
+ *   dq_acc [T, H]        fp32 dq accumulator
+ *   dz     [T, 3H + F']  [dq | dk | dv | dh], dL/d[q | k | v | h] (bf16, W1cat order)
+ *   dxn    [T, H]        fp32 dL/dLN(x)
+ *   stats  [T]           fp32 (mean, rstd) per row
+ *   partials             fp32 partial column sums of the parameter gradients */
 typedef struct pb_scratch_layout {
   size_t xn;
   size_t qk;
@@ -128,6 +140,16 @@ typedef struct pb_scratch_layout {
   size_t qscale;  /* PB_OPERANDS_FP8: [2T] fp32 row scales of LN(x), then of act */
   size_t seq_pad;
   size_t total;
+  size_t hpre;
+  size_t lse;
+  size_t d_attn;
+  size_t delta;
+  size_t dq_acc;
+  size_t dz;
+  size_t dxn;
+  size_t stats;
+  size_t partials;
+  size_t train_total;
 } pb_scratch_layout;
 
 /* Precision of the two GEMMs' operands. The pages' mixed-precision recipe computes in
@@ -182,6 +204,51 @@ pb_status pb_create_ex(const pb_dims* dims, const pb_weights* weights, const pb_
  * call that may run concurrently. */
 pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t scratch_bytes,
                      void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Training: the block's backward pass (the pages' subject is training: MFU counts the
+ * forward's 2 and the backward's 4 FLOPs per weight and token, performance notes "MFU").
+ * pb_forward_train is pb_forward that also keeps, in a training scratch, what the
+ * backward reads: h before its activation and each attention row's log-sum-exp. The
+ * attention probabilities are not kept; pb_backward recomputes them (the selective
+ * recomputation of the MegaScale reading notes, section 1.3). Supported: bf16 operands
+ * (PB_OPERANDS_BF16) and head_dim 128; otherwise PB_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------------------- */
+
+/* Bytes of the training scratch of pb_forward_train / pb_backward (train_total). */
+pb_status pb_train_scratch_bytes(const pb_dims* dims, size_t* bytes);
+
+/* pb_forward, keeping hpre and lse in `scratch` (>= pb_train_scratch_bytes) for a
+ * following pb_backward on the same handle, x and scratch. */
+pb_status pb_forward_train(pb_handle* h, const void* x, void* y, void* scratch,
+                           size_t scratch_bytes, void* stream);
+
+/* Gradients of the block, all device pointers: dx bf16 [T, H] (dL/dx, the residual path
+ * included); every parameter gradient fp32 in the layout of its pb_weights entry
+ * (dwqkv [H, 3H], dw1 [H, F'] = [gate | up] for SwiGLU, dwo [H, H], dw2 [F, H], biases
+ * [3H], [F'], [H], [H], dgamma and dbeta [H]). NULL skips a bias gradient or dbeta. */
+typedef struct pb_grads {
+  void* dx;
+  float* dgamma;
+  float* dbeta;
+  float* dwqkv;
+  float* dw1;
+  float* dwo;
+  float* dw2;
+  float* db_qkv;
+  float* db1;
+  float* db_o;
+  float* db2;
+} pb_grads;
+
+/* The backward pass for upstream gradient dy (bf16 [T, H]) after pb_forward_train(h, x,
+ * ...) with the same scratch: d_attn and dh from one GEMM against W2cat, the attention
+ * backward (P recomputed from q, k and lse), dLN(x) from one GEMM against W1cat, the
+ * normalisation backward plus dy (dx), and the weight gradients as two GEMMs over the
+ * tokens ([dWo ; dW2] = act^T dy, [dWqkv | dW1] = LN(x)^T dz). accumulate != 0 adds the
+ * fp32 parameter gradients to what the buffers hold (dx is always overwritten). */
+pb_status pb_backward(pb_handle* h, const void* x, const void* dy, const pb_grads* grads,
+                      int32_t accumulate, void* scratch, size_t scratch_bytes, void* stream);
 
 /* The serial (standard) transformer block of eq. (3) (MegaScale reading notes, section 1.1,
  * "Parallel Transformer Block") on the handle's weights, for comparison with pb_forward:

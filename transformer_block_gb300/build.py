@@ -17,7 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpb.so")
-SOURCES = ["pb_api.cu", "ln.cu", "gemm.cu", "swa.cu", "pack.cu", "noalloc.cu", "quant.cu"]
+SOURCES = ["pb_api.cu", "ln.cu", "gemm.cu", "swa.cu", "pack.cu", "noalloc.cu", "quant.cu",
+           "swa_bwd.cu", "bwd_aux.cu"]
 HEADERS = ["kernels.h", "ptx.cuh", os.path.join("..", "..", "include", "pb.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]

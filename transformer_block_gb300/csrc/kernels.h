@@ -125,6 +125,8 @@ struct SwaParams {
   void* out;  // attention output, row (b*S + i), columns [head*dh, (head+1)*dh)
   int64_t out_ld;
   bool out_f16;  // write fp16 (else bf16)
+  float* lse;    // training forward: [B, nh, S] log2-sum-exp of each row's scores
+                 // (times log2(e) / sqrt(dh)), or null
 };
 constexpr int kSwaBQ = 128;  // query rows per tile (two tiles per CTA)
 constexpr int kSwaBKV = 128;  // keys per tile
@@ -133,6 +135,60 @@ constexpr int kSwaBKV = 128;  // keys per tile
 // keys x dh rows.
 cudaError_t launch_swa(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmVT,
                        const SwaParams& p, int* status, uint64_t limit_ns, cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention backward
+// (swa_bwd.cu). q | k and v^T as the forward left them, dO = d_attn [B][S][H] bf16, the
+// forward's lse and delta[b, head, i] = dO_i . O_i ([B, nh, S] fp32). Adds dq (unscaled)
+// into dq_acc [T, H] fp32 (zeroed by the caller) and writes dk (scaled by 1/sqrt(dh)) and
+// dv as bf16 into dz columns [H, 2H) and [2H, 3H) (row stride ldz). dh == 128.
+struct SwaBwdParams {
+  int B, S, H, nh, dh, window;
+  float scale_log2;  // log2(e) / sqrt(dh)
+  float scale;       // 1 / sqrt(dh)
+  const float* lse;
+  const float* delta;
+  float* dq_acc;
+  __nv_bfloat16* dz;
+  int64_t ldz;
+};
+// tmQ: q|k in boxes of 64 columns x 64 rows; tmK: the same in boxes of 64 x 128 rows;
+// tmVT: v^T in boxes of 64 keys x dh rows; tmDO: d_attn [B][S][H] in boxes of 64 x 64.
+cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmVT, const CUtensorMap& tmDO,
+                           const SwaBwdParams& p, int* status, uint64_t limit_ns,
+                           cudaStream_t stream);
+
+// ---------------------------------------------------------------- backward helpers
+// (bwd_aux.cu)
+// delta[(b * nh + head) * S + s] = sum_d dO[t, head*dh + d] * O[t, head*dh + d], t = b*S + s
+// (dO: [T, H] bf16; O: the attention output, row stride o_ld).
+cudaError_t launch_attn_delta(const __nv_bfloat16* dO, const __nv_bfloat16* O, int64_t o_ld,
+                              int B, int S, int nh, int dh, float* delta, cudaStream_t stream);
+// dz[t * ldz + c] = bf16(dq_acc[t * H + c] * scale), c < H.
+cudaError_t launch_dq_to_bf16(const float* dq_acc, int64_t T, int H, float scale,
+                              __nv_bfloat16* dz, int64_t ldz, cudaStream_t stream);
+// Normalisation backward, per row: dx = dy + rstd (g - mean g - xhat mean(g xhat)), g =
+// dxn * gamma, xhat = (x - mu) rstd (RMSNorm when rms: mu = 0, no mean g term); also the
+// row statistics (mu, rstd) for the parameter gradients. x, dy, dx bf16 [T, H]; dxn fp32.
+cudaError_t launch_norm_bwd(int64_t T, int H, const __nv_bfloat16* x,
+                            const __nv_bfloat16* gamma, const float* dxn,
+                            const __nv_bfloat16* dy, float eps, bool rms, __nv_bfloat16* dx,
+                            float2* stats, cudaStream_t stream);
+constexpr int kColBlocks = 32;  // row blocks of the column reductions
+// dgamma[c] (+)= sum_r dxn[r,c] xhat[r,c], dbeta[c] (+)= sum_r dxn[r,c] (dbeta may be null),
+// through partials [2][kColBlocks][H] fp32, rows summed in a fixed order.
+cudaError_t launch_norm_param_grads(int64_t T, int H, const __nv_bfloat16* x, const float* dxn,
+                                    const float2* stats, float* partials, float* dgamma,
+                                    float* dbeta, bool accumulate, cudaStream_t stream);
+// Column sums of a bf16 [rows, N] matrix (row stride ld), through partials
+// [kColBlocks][N] fp32, rows summed in a fixed order: column c < split goes to out0[c],
+// column c >= split to out1[c - split], or with glu_F > 0 to out1 at the SwiGLU
+// de-interleave of c - split (group t = (c - split) / 32, i = (c - split) % 32: gate
+// feature 16t + i for i < 16, else up feature glu_F + 16t + i - 16). A null out is skipped;
+// accumulate adds to it.
+cudaError_t launch_col_sums(const __nv_bfloat16* m, int64_t rows, int64_t N, int64_t ld,
+                            float* partials, float* out0, float* out1, int64_t split,
+                            int64_t glu_F, bool accumulate, cudaStream_t stream);
 
 // ---------------------------------------------------------------- packing (pack.cu)
 // out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols; with out_f16 the bf16

@@ -182,6 +182,29 @@ pb_scratch_layout scratch_layout(const pb_dims& d) {
   L.qscale = off;
   off = align_up(off + 2 * T * 4, 1024);
   L.total = off;
+  // training: what the backward reads from the forward, then its own intermediates
+  const size_t Fp = size_t(w1_rows(d)) - 3 * H;  // F, or 2F for SwiGLU
+  const size_t NZ = size_t(w1_rows(d));          // columns of dz = [dq | dk | dv | dh]
+  const size_t rows_lse = size_t(d.batch) * size_t(d.heads) * size_t(d.seq);
+  L.hpre = off;
+  off = align_up(off + T * Fp * 2, 1024);
+  L.lse = off;
+  off = align_up(off + rows_lse * 4, 1024);
+  L.d_attn = off;
+  off = align_up(off + T * H * 2, 1024);
+  L.delta = off;
+  off = align_up(off + rows_lse * 4, 1024);
+  L.dq_acc = off;
+  off = align_up(off + T * H * 4, 1024);
+  L.dz = off;
+  off = align_up(off + T * NZ * 2, 1024);
+  L.dxn = off;
+  off = align_up(off + T * H * 4, 1024);
+  L.stats = off;
+  off = align_up(off + T * 8, 1024);
+  L.partials = off;
+  off = align_up(off + size_t(pb::kColBlocks) * (NZ > 2 * H ? NZ : 2 * H) * 4, 1024);
+  L.train_total = off;
   return L;
 }
 
@@ -288,7 +311,7 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 // One block from x to y (each bf16, or fp32 inside a stack's residual stream),
 // intermediates in `scratch`.
 pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32,
-                    uint8_t* scratch, cudaStream_t st) {
+                    uint8_t* scratch, cudaStream_t st, bool train = false) {
   const pb_dims& d = h->d;
   const pb_scratch_layout L = scratch_layout(d);
   const int H = d.hidden, F = d.ffn, T = d.batch * d.seq;
@@ -338,6 +361,7 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
     e1.scale_a = qscale;
     e1.scale_b = h->w1scale;
   }
+  if (train) e1.hpre = reinterpret_cast<__nv_bfloat16*>(scratch + L.hpre);
   PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->gop, tm_xn, h->tm_w1cat, T, int(w1_rows(d)), H,
                           e1, h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
           "first GEMM launch");
@@ -359,6 +383,7 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   sp.out = act;
   sp.out_ld = H + F;
   sp.out_f16 = h->f16;
+  if (train) sp.lse = reinterpret_cast<float*>(scratch + L.lse);
   PB_CUDA(pb::launch_swa(tm_qk, tm_k, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
   PB_CUDA(mark(3), "cudaEventRecord");
 
@@ -505,6 +530,167 @@ pb_status run_serial(pb_handle* h, const void* x, void* y, const __nv_bfloat16* 
   PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->op16, tm_g, tm_w2, T, H, F, e4, h->num_sms,
                           h->status, h->limit_ns, scratch + L.sk, st),
           "MLP output GEMM launch");
+  return PB_OK;
+}
+
+// The block's backward pass (see pb_backward in pb.h) after run_block(..., train = true) on
+// the same scratch. Nine steps, each on the handle's stream:
+//   1. [d_attn | d act] = dy [Wo ; W2]^T (B = W2cat read MN-major), dh = d act * act'(h)
+//   2. delta = d_attn . O per row and head
+//   3. attention backward: dq (fp32 accumulator, then bf16), dk, dv into dz
+//   4. dLN(x) = dz W1cat (B = W1cat read MN-major), fp32
+//   5. dx = dy + norm'(x)^T dLN(x); dgamma, dbeta
+//   6. [dWo ; dW2] = act^T dy     (both operands MN-major: the contraction runs over tokens)
+//   7. [dWqkv | dW1] = LN(x)^T dz
+//   8. bias gradients: column sums of dy and dz
+pb_status run_backward(pb_handle* h, const void* x, const void* dy, const pb_grads& g,
+                       bool acc, uint8_t* scratch, cudaStream_t st) {
+  const pb_dims& d = h->d;
+  const pb_scratch_layout L = scratch_layout(d);
+  const int H = d.hidden, F = d.ffn, T = d.batch * d.seq;
+  const bool glu = is_glu(d);
+  const int NZ = int(w1_rows(d)), Fp = NZ - 3 * H;
+  auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(scratch + off); };
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(scratch + off); };
+  __nv_bfloat16 *d_attn = bf(L.d_attn), *dz = bf(L.dz);
+  const uint32_t box = pb::kGemmBoxRows;
+  const int big = 0x7fffffff;
+
+  // 1. d_attn, dh
+  CUtensorMap tm_dy, tm_w2t;
+  pb_status s = make_map_2d(&tm_dy, dy, T, H, H, box);
+  if (s == PB_OK) s = make_map_2d(&tm_w2t, h->w2cat, H, H + F, H + F, 64);
+  if (s != PB_OK) return s;
+  EpiParams e1{};
+  e1.status = h->status;
+  e1.H = H;
+  e1.F = F;
+  e1.glu = glu;
+  e1.hpre = bf(L.hpre);
+  e1.d_attn = d_attn;
+  e1.dz = dz;
+  e1.ldz = NZ;
+  PB_CUDA(pb::launch_gemm_layout(pb::kEpiBwdAct, pb::kKM, tm_dy, tm_w2t, T, H + F, H, e1,
+                                 h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
+          "backward GEMM (d_attn, dh) launch");
+  // 2. delta
+  PB_CUDA(pb::launch_attn_delta(d_attn, bf(L.act), H + F, d.batch, d.seq, d.heads, d.head_dim,
+                                f32(L.delta), st),
+          "delta launch");
+  // 3. attention backward
+  CUtensorMap tm_q, tm_k, tm_vt, tm_do;
+  {
+    const uint64_t qdims[3] = {2 * uint64_t(H), uint64_t(d.seq), uint64_t(d.batch)};
+    const uint64_t qstr[2] = {2 * uint64_t(H) * 2, 2 * uint64_t(H) * 2 * uint64_t(d.seq)};
+    const uint32_t qbox[3] = {64, 64, 1}, kbox[3] = {64, 128, 1};
+    const uint64_t odims[3] = {uint64_t(H), uint64_t(d.seq), uint64_t(d.batch)};
+    const uint64_t ostr[2] = {uint64_t(H) * 2, uint64_t(H) * 2 * uint64_t(d.seq)};
+    const uint64_t vdims[2] = {uint64_t(d.seq), uint64_t(d.batch) * H};
+    const uint64_t vstr[1] = {uint64_t(L.seq_pad) * 2};
+    const uint32_t vbox[2] = {64, uint32_t(d.head_dim)};
+    s = make_map(&tm_q, scratch + L.qk, 3, qdims, qstr, qbox);
+    if (s == PB_OK) s = make_map(&tm_k, scratch + L.qk, 3, qdims, qstr, kbox);
+    if (s == PB_OK) s = make_map(&tm_vt, scratch + L.vt, 2, vdims, vstr, vbox);
+    if (s == PB_OK) s = make_map(&tm_do, d_attn, 3, odims, ostr, qbox);
+    if (s != PB_OK) return s;
+  }
+  PB_CUDA(cudaMemsetAsync(f32(L.dq_acc), 0, size_t(T) * H * 4, st), "cudaMemsetAsync(dq)");
+  pb::SwaBwdParams sb{};
+  sb.B = d.batch;
+  sb.S = d.seq;
+  sb.H = H;
+  sb.nh = d.heads;
+  sb.dh = d.head_dim;
+  sb.window = d.window;
+  sb.scale = float(1.0 / std::sqrt(double(d.head_dim)));
+  sb.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d.head_dim)));
+  sb.lse = f32(L.lse);
+  sb.delta = f32(L.delta);
+  sb.dq_acc = f32(L.dq_acc);
+  sb.dz = dz;
+  sb.ldz = NZ;
+  PB_CUDA(pb::launch_swa_bwd(tm_q, tm_k, tm_vt, tm_do, sb, h->status, h->limit_ns, st),
+          "attention backward launch");
+  PB_CUDA(pb::launch_dq_to_bf16(f32(L.dq_acc), T, H, sb.scale, dz, NZ, st), "dq launch");
+  // 4. dLN(x) = dz W1cat
+  CUtensorMap tm_dz, tm_w1t;
+  s = make_map_2d(&tm_dz, dz, T, NZ, NZ, box);
+  if (s == PB_OK) s = make_map_2d(&tm_w1t, h->w1cat, NZ, H, H, 64);
+  if (s != PB_OK) return s;
+  EpiParams e4{};
+  e4.status = h->status;
+  e4.g0 = f32(L.dxn);
+  e4.ld0 = H;
+  e4.split_row = big;
+  e4.split_col = big;
+  PB_CUDA(pb::launch_gemm_layout(pb::kEpiGrad, pb::kKM, tm_dz, tm_w1t, T, H, NZ, e4, h->num_sms,
+                                 h->status, h->limit_ns, scratch + L.sk, st),
+          "backward GEMM (dLN(x)) launch");
+  // 5. the normalisation and the residual
+  auto* stats = reinterpret_cast<float2*>(scratch + L.stats);
+  PB_CUDA(pb::launch_norm_bwd(T, H, static_cast<const __nv_bfloat16*>(x), h->gamma, f32(L.dxn),
+                              static_cast<const __nv_bfloat16*>(dy), d.ln_eps, glu,
+                              static_cast<__nv_bfloat16*>(g.dx), stats, st),
+          "norm backward launch");
+  PB_CUDA(pb::launch_norm_param_grads(T, H, static_cast<const __nv_bfloat16*>(x), f32(L.dxn),
+                                      stats, f32(L.partials), g.dgamma,
+                                      glu ? nullptr : g.dbeta, acc, st),
+          "norm parameter gradients launch");
+  // 6. [dWo ; dW2] = act^T dy
+  CUtensorMap tm_act_t, tm_dy_t;
+  s = make_map_2d(&tm_act_t, scratch + L.act, T, H + F, H + F, 64);
+  if (s == PB_OK) s = make_map_2d(&tm_dy_t, dy, T, H, H, 64);
+  if (s != PB_OK) return s;
+  EpiParams e6{};
+  e6.status = h->status;
+  e6.g0 = g.dwo;
+  e6.ld0 = H;
+  e6.g1 = g.dw2;
+  e6.ld1 = H;
+  e6.split_row = H;
+  e6.split_col = big;
+  e6.accumulate = acc;
+  PB_CUDA(pb::launch_gemm_layout(pb::kEpiGrad, pb::kMM, tm_act_t, tm_dy_t, H + F, H, T, e6,
+                                 h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
+          "weight gradient GEMM (Wo, W2) launch");
+  // 7. [dWqkv | dW1] = LN(x)^T dz
+  CUtensorMap tm_xn_t, tm_dz_t;
+  s = make_map_2d(&tm_xn_t, scratch + L.xn, T, H, H, 64);
+  if (s == PB_OK) s = make_map_2d(&tm_dz_t, dz, T, NZ, NZ, 64);
+  if (s != PB_OK) return s;
+  EpiParams e7{};
+  e7.status = h->status;
+  e7.g0 = g.dwqkv;
+  e7.ld0 = 3 * H;
+  e7.g1 = g.dw1;
+  e7.ld1 = Fp;
+  e7.split_row = big;
+  e7.split_col = 3 * H;
+  e7.glu = glu;
+  e7.F = F;
+  e7.accumulate = acc;
+  PB_CUDA(pb::launch_gemm_layout(pb::kEpiGrad, pb::kMM, tm_xn_t, tm_dz_t, H, NZ, T, e7,
+                                 h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
+          "weight gradient GEMM (Wqkv, W1) launch");
+  // 8. biases
+  const auto* dyb = static_cast<const __nv_bfloat16*>(dy);
+  if (g.db_o != nullptr)
+    PB_CUDA(pb::launch_col_sums(dyb, T, H, H, f32(L.partials), g.db_o, nullptr, H, 0, acc, st),
+            "bias gradient launch");
+  if (g.db2 != nullptr)
+    PB_CUDA(pb::launch_col_sums(dyb, T, H, H, f32(L.partials), g.db2, nullptr, H, 0, acc, st),
+            "bias gradient launch");
+  if (g.db_qkv != nullptr || g.db1 != nullptr)
+    PB_CUDA(pb::launch_col_sums(dz, T, NZ, NZ, f32(L.partials), g.db_qkv, g.db1, 3 * H,
+                                glu ? F : 0, acc, st),
+            "bias gradient launch");
+  return PB_OK;
+}
+
+pb_status check_train(pb_handle* h) {
+  if (h->f16 || h->fp8)
+    return fail(PB_ERR_UNSUPPORTED, "training needs PB_OPERANDS_BF16 operands");
+  if (h->d.head_dim != 128) return fail(PB_ERR_UNSUPPORTED, "training needs head_dim 128");
   return PB_OK;
 }
 
@@ -759,6 +945,68 @@ pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t
     return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
   return run_block(h, x, false, y, false, static_cast<uint8_t*>(scratch),
                    static_cast<cudaStream_t>(stream));
+}
+
+pb_status pb_train_scratch_bytes(const pb_dims* dims, size_t* bytes) {
+  pb_status s = check_dims(dims);
+  if (s != PB_OK) return s;
+  if (bytes == nullptr) return fail(PB_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = scratch_layout(*dims).train_total;
+  return PB_OK;
+}
+
+pb_status pb_forward_train(pb_handle* h, const void* x, void* y, void* scratch,
+                           size_t scratch_bytes, void* stream) {
+  pb_status s = check_handle(h);
+  if (s != PB_OK) return s;
+  s = check_train(h);
+  if (s != PB_OK) return s;
+  const pb_scratch_layout L = scratch_layout(h->d);
+  if (scratch == nullptr || !aligned(scratch, 256))
+    return fail(PB_ERR_INVALID_ARG, "scratch must be a 256-byte aligned device pointer");
+  if (scratch_bytes < L.train_total)
+    return fail(PB_ERR_WORKSPACE, "training scratch has %zu bytes, %zu needed", scratch_bytes,
+                L.train_total);
+  if (x == nullptr || y == nullptr || !aligned(x, 16) || !aligned(y, 16))
+    return fail(PB_ERR_INVALID_ARG, "x and y must be 16-byte aligned device pointers");
+  const size_t n = size_t(h->d.batch) * h->d.seq * h->d.hidden * 2;
+  if (x == y) return fail(PB_ERR_INVALID_ARG, "the backward reads x: y must not be x");
+  if (overlap(x, n, y, n)) return fail(PB_ERR_INVALID_ARG, "x and y overlap");
+  if (overlap(x, n, scratch, L.train_total) || overlap(y, n, scratch, L.train_total))
+    return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
+  return run_block(h, x, false, y, false, static_cast<uint8_t*>(scratch),
+                   static_cast<cudaStream_t>(stream), true);
+}
+
+pb_status pb_backward(pb_handle* h, const void* x, const void* dy, const pb_grads* grads,
+                      int32_t accumulate, void* scratch, size_t scratch_bytes, void* stream) {
+  pb_status s = check_handle(h);
+  if (s != PB_OK) return s;
+  s = check_train(h);
+  if (s != PB_OK) return s;
+  const pb_scratch_layout L = scratch_layout(h->d);
+  if (scratch == nullptr || !aligned(scratch, 256))
+    return fail(PB_ERR_INVALID_ARG, "scratch must be a 256-byte aligned device pointer");
+  if (scratch_bytes < L.train_total)
+    return fail(PB_ERR_WORKSPACE, "training scratch has %zu bytes, %zu needed", scratch_bytes,
+                L.train_total);
+  if (grads == nullptr) return fail(PB_ERR_INVALID_ARG, "grads is NULL");
+  const void* need[7] = {x, dy, grads->dx, grads->dgamma, grads->dwqkv, grads->dw1, grads->dwo};
+  for (const void* p : need)
+    if (p == nullptr || !aligned(p, 16))
+      return fail(PB_ERR_INVALID_ARG,
+                  "x, dy, dx, dgamma and the weight gradients must be 16-byte aligned device "
+                  "pointers");
+  if (grads->dw2 == nullptr || !aligned(grads->dw2, 16))
+    return fail(PB_ERR_INVALID_ARG, "dw2 must be a 16-byte aligned device pointer");
+  const pb_dims& d = h->d;
+  const size_t n = size_t(d.batch) * d.seq * d.hidden * 2;
+  if (overlap(grads->dx, n, x, n) || overlap(grads->dx, n, dy, n))
+    return fail(PB_ERR_INVALID_ARG, "dx overlaps x or dy");
+  if (overlap(grads->dx, n, scratch, L.train_total) || overlap(dy, n, scratch, L.train_total))
+    return fail(PB_ERR_INVALID_ARG, "dx or dy overlaps the scratch buffer");
+  return run_backward(h, x, dy, *grads, accumulate != 0, static_cast<uint8_t*>(scratch),
+                      static_cast<cudaStream_t>(stream));
 }
 
 pb_status pb_forward_serial(pb_handle* h, const void* x, void* y, const void* ln2_gamma,

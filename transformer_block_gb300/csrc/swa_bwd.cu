@@ -1,0 +1,366 @@
+// swa_bwd.cu — backward of the sliding-window causal attention on the tensor cores, with
+// the probabilities recomputed from q, k and the forward's log-sum-exp instead of stored
+// (the selective recomputation of the MegaScale reading notes, section 1.3: the score
+// matrix is the expensive activation, recomputed in the backward pass).
+//
+// For one head of one sequence, with W(i) = {j : 0 <= i - j < w}, s_ij = q_i . k_j / sqrt(dh),
+// p_ij = 2^(s_ij log2(e) - L_i) (L_i the forward's log2-sum-exp of row i), do = dL/do:
+//   dv_j = sum_i p_ij do_i
+//   dp_ij = do_i . v_j,   ds_ij = p_ij (dp_ij - D_i),   D_i = do_i . o_i
+//   dq_i = sum_j ds_ij k_j / sqrt(dh),   dk_j = sum_i ds_ij q_i / sqrt(dh)
+// (D_i equals sum_j p_ij dp_ij because o_i = sum_j p_ij v_j.)
+//
+// One CTA per (128-key tile, head, sequence), the key tiles with the most queries first.
+// It keeps K and V of its keys in shared memory and dV, dK (fp32) in tensor memory, and
+// walks the 64-query steps that reach its keys (from its first key to the last query whose
+// window does):
+//   S^T  = K Q^T        (M = 128 keys, N = 64 queries)        tensor memory
+//   dP^T = V dO^T       (A = V, MN-major from v^T)            tensor memory
+//   softmax warps: P^T, dS^T (bf16) back into tensor memory over S^T and dP^T, and dS
+//                  into shared memory
+//   dV  += P^T dO,  dK += dS^T Q   (A from tensor memory, B = dO, Q read MN-major)
+//   dQ^T = K^T dS       (M = dh, N = 64 queries; both operands MN-major)
+// and a second group of warps adds dQ^T into an fp32 dq accumulator in global memory
+// (one coalesced reduction per query and head; other key tiles add theirs). The same
+// shared-memory tiles serve as K-major and as MN-major operands: a TMA box of 64 16-bit
+// elements per row is both.
+//   warp 0     TMA producer: K and V once, then Q and dO per step (2-stage ring)
+//   warp 1     tensor-memory owner and the MMA-issuing thread
+//   warps 2-5  recompute P and dS, one key per thread (its TMEM lane)
+//   warps 6-9  dQ reduction per step, then the dK and dV rows of the tile
+// Tensor memory: S^T [0, 64) | dP^T [64, 128) | dQ^T [128, 192) | dV [192, 320) |
+// dK [320, 448). The MMAs of one thread execute in issue order, so the next step's S^T
+// overwrites P^T only after dV has read it; a commit covers every earlier MMA.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace pb {
+namespace {
+
+constexpr int BKV = 128;  // keys per CTA
+constexpr int BQ = 64;    // queries per step
+constexpr int DH = 128;   // head dim
+constexpr int THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 192, T_DK = 320;
+constexpr int K_BOX = BKV * 64 * 2;   // 16 KB: 128 keys x 64 dims
+constexpr int K_BYTES = 2 * K_BOX;
+constexpr int V_HALF = DH * 64 * 2;   // 16 KB: dh rows x 64 keys (from v^T)
+constexpr int V_BYTES = 2 * V_HALF;
+constexpr int QD_BOX = BQ * 64 * 2;   // 8 KB: 64 queries x 64 dims
+constexpr int Q_BYTES = 2 * QD_BOX;
+constexpr int STAGE_BYTES = 2 * Q_BYTES;  // Q and dO
+constexpr int STAGES = 2;
+constexpr int DS_BYTES = BKV * BQ * 2;  // dS: 128 key rows x 64 queries
+constexpr int K_OFF = 0, V_OFF = K_BYTES, ST_OFF = V_OFF + V_BYTES;
+constexpr int DS_OFF = ST_OFF + STAGES * STAGE_BYTES;
+constexpr int BAR_OFF = DS_OFF + DS_BYTES;
+// kv_full, q_full[2], q_empty[2], s_full, p_full, mma_done, dq_free, drain
+constexpr int NUM_BARS = 10;
+constexpr size_t SMEM = size_t(BAR_OFF) + NUM_BARS * 8 + 16 + 1024;
+static_assert(SMEM <= 227 * 1024 && 2 * SMEM > 228 * 1024,
+              "one CTA per SM: it takes all tensor-memory columns");
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t u[64];
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(u));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+  tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(u));
+  tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+#pragma unroll
+  for (int e = 0; e < 64; ++e) v[e] = __uint_as_float(u[e]);
+}
+
+// The step's work: the key tile's first query step and the number of 64-query steps.
+__device__ __forceinline__ int num_steps(const SwaBwdParams& p, int j0) {
+  const int last = min(p.S - 1, j0 + BKV - 1 + p.window - 1);
+  return last / BQ - j0 / BQ + 1;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    swa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmVT,
+                   const __grid_constant__ CUtensorMap tmDO, const SwaBwdParams p, int* status,
+                   uint64_t limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  const uint32_t kv_full = smem_u32(bars + 0);
+  const uint32_t q_full0 = smem_u32(bars + 1);   // [2]
+  const uint32_t q_empty0 = smem_u32(bars + 3);  // [2]
+  const uint32_t s_full = smem_u32(bars + 5);
+  const uint32_t p_full = smem_u32(bars + 6);    // 4 softmax warps
+  const uint32_t mma_done = smem_u32(bars + 7);  // the step's dV, dK, dQ^T products
+  const uint32_t dq_free = smem_u32(bars + 8);   // 4 reduction warps read dQ^T out
+  const uint32_t drain_bar = smem_u32(bars + 9);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (cta_should_skip(status)) return;
+  // Work item: key tile (slowest: the tiles with the most queries come first), head, sequence.
+  const int per_tile = p.nh * p.B;
+  const int jt = int(blockIdx.x) / per_tile;
+  const int head = int(blockIdx.x) % p.nh;
+  const int b = (int(blockIdx.x) / p.nh) % p.B;
+  const int j0 = jt * BKV;
+  const int N = num_steps(p, j0);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(q_full0 + 8 * s, 1);
+      mbar_init(q_empty0 + 8 * s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(mma_done, 1);
+    mbar_init(dq_free, 4);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmVT);
+    tma_prefetch_desc(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, status, limit_ns};
+  const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
+  const uint32_t sK = smem_u32(smem + K_OFF), sV = smem_u32(smem + V_OFF);
+  const uint32_t sST = smem_u32(smem + ST_OFF), sDS = smem_u32(smem + DS_OFF);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ producer
+      mbar_arrive_expect_tx(kv_full, K_BYTES + V_BYTES);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(sK + c * K_BOX, &tmK, kv_full, p.H + head * DH + 64 * c, j0, b);
+        tma_load_2d(sV + c * V_HALF, &tmVT, kv_full, j0 + 64 * c, (b * p.nh + head) * DH);
+      }
+      int issued = 0;
+      for (int n = 0; n < N; ++n) {
+        const int st = n & 1;
+        if (!mbar_wait(q_empty0 + 8 * st, uint32_t((n >> 1) & 1) ^ 1u, wc, 30)) break;
+        const uint32_t dst = sST + st * STAGE_BYTES;
+        const int i0 = j0 + n * BQ;
+        mbar_arrive_expect_tx(q_full0 + 8 * st, STAGE_BYTES);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(dst + c * QD_BOX, &tmQ, q_full0 + 8 * st, head * DH + 64 * c, i0, b);
+          tma_load_3d(dst + Q_BYTES + c * QD_BOX, &tmDO, q_full0 + 8 * st, head * DH + 64 * c,
+                      i0, b);
+        }
+        issued = n + 1;
+      }
+      // the CTA's own copies land before it may exit
+      mbar_wait_drain(kv_full, 0, drain_ns);
+      for (int n = issued - 2 < 0 ? 0 : issued - 2; n < issued; ++n)
+        mbar_wait_drain(q_full0 + 8 * (n & 1), uint32_t(n >> 1) & 1u, drain_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ MMA issuer
+      const uint32_t id_s = idesc_f32acc(BKV, BQ);                     // K, Q K-major
+      const uint32_t id_dp = idesc_f32acc(BKV, BQ, false, true, false);  // V MN-major
+      const uint32_t id_acc = idesc_f32acc(BKV, DH, false, false, true);  // TMEM A, B MN
+      const uint32_t id_dq = idesc_f32acc(DH, BQ, false, true, true);   // both MN-major
+      const uint64_t dK = sdesc_kmajor_sw128(sK), dKmn = sdesc_mnmajor_sw128(sK, K_BOX);
+      const uint64_t dVmn = sdesc_mnmajor_sw128(sV, V_HALF);
+      const uint64_t dDS = sdesc_mnmajor_sw128(sDS, DS_BYTES);
+      bool ok = mbar_wait(kv_full, 0, wc, 31);
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n & 1;
+        const uint32_t sQ = sST + st * STAGE_BYTES, sDO = sQ + Q_BYTES;
+        if (!mbar_wait(q_full0 + 8 * st, uint32_t(n >> 1) & 1u, wc, 32)) break;
+        tc_fence_after();
+        const uint64_t dQk = sdesc_kmajor_sw128(sQ), dDOk = sdesc_kmajor_sw128(sDO);
+        // S^T = K Q^T and dP^T = V dO^T, K = dh in steps of 16
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint64_t ok_ = uint64_t(((kk >> 2) * K_BOX) >> 4) + 2 * (kk & 3);
+          const uint64_t oq = uint64_t(((kk >> 2) * QD_BOX) >> 4) + 2 * (kk & 3);
+          mma_f16kind_ss(tmem_base + T_S, dK + ok_, dQk + oq, id_s, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint64_t oq = uint64_t(((kk >> 2) * QD_BOX) >> 4) + 2 * (kk & 3);
+          mma_f16kind_ss(tmem_base + T_DP, dVmn + 128 * kk, dDOk + oq, id_dp, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        if (!mbar_wait(p_full, uint32_t(n) & 1u, wc, 33)) break;
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q: K = the step's 64 queries
+        const uint64_t dDOmn = sdesc_mnmajor_sw128(sDO, QD_BOX);
+        const uint64_t dQmn = sdesc_mnmajor_sw128(sQ, QD_BOX);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_f16kind_ts(tmem_base + T_DV, tmem_base + T_S + 8 * kk, dDOmn + 128 * kk, id_acc,
+                         (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_f16kind_ts(tmem_base + T_DK, tmem_base + T_DP + 8 * kk, dQmn + 128 * kk, id_acc,
+                         (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(q_empty0 + 8 * st);  // Q and dO of this stage are read
+        // dQ^T = K^T dS once the previous step's dQ^T has been read out
+        if (n > 0 && !mbar_wait(dq_free, uint32_t(n - 1) & 1u, wc, 34)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          mma_f16kind_ss(tmem_base + T_DQ, dKmn + 128 * kk, dDS + 128 * kk, id_dq,
+                         kk > 0 ? 1u : 0u);
+        mma_commit(mma_done);
+      }
+      mma_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0, drain_ns);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ P and dS
+    const uint32_t quad = warp & 3;
+    const int r = int(quad * 32 + lane);  // key of the tile = TMEM lane
+    const int key = j0 + r;
+    const uint32_t lane_addr = (quad * 32u) << 16;
+    const float c = p.scale_log2;
+    const float* lse = p.lse + int64_t(b * p.nh + head) * p.S;
+    const float* dlt = p.delta + int64_t(b * p.nh + head) * p.S;
+    uint8_t* ds_row = smem + DS_OFF + r * 128;
+    const int sw = r & 7;  // 128-byte swizzle of the row's 16-byte chunks
+    for (int n = 0; n < N; ++n) {
+      if (!mbar_wait_warp(s_full, uint32_t(n) & 1u, wc, 35)) break;
+      tc_fence_after();
+      const int i0 = j0 + n * BQ;
+      // two halves of 32 queries: S^T and dP^T in, P^T and dS^T out over them, dS to shared
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t us[32], ud[32];
+        tmem_ld32(tmem_base + lane_addr + T_S + 32 * hf, us);
+        tmem_ld32(tmem_base + lane_addr + T_DP + 32 * hf, ud);
+        tmem_ld_wait(us);
+        tmem_ld_wait_regs(ud);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int q = i0 + 32 * hf + e + h, d = q - key;
+            pv[h] = 0.f;
+            dv[h] = 0.f;
+            if (d >= 0 && d < p.window && q < p.S) {  // q's window holds the key
+              pv[h] = ex2_approx(__uint_as_float(us[e + h]) * c - __ldg(lse + q));
+              dv[h] = pv[h] * (__uint_as_float(ud[e + h]) - __ldg(dlt + q));
+            }
+          }
+          pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          dk[e / 2] = pack_bf16x2(dv[0], dv[1]);
+        }
+        // P^T over S^T and dS^T over dP^T (the A operands of dV and dK; 32 queries = 16
+        // packed columns), and the dS row's 4 chunks of 16 bytes to shared memory
+        tmem_st16(tmem_base + lane_addr + T_S + 16 * hf, pk);
+        tmem_st16(tmem_base + lane_addr + T_DP + 16 * hf, dk);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          *reinterpret_cast<uint4*>(ds_row + (((4 * hf + ch) ^ sw) << 4)) =
+              make_uint4(dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+  } else {
+    // ------------------------------------------------------------------ dQ, dK, dV out
+    const uint32_t quad = warp & 3;
+    const int r = int(quad * 32 + lane);  // TMEM lane: head dim of dQ^T, key of dV and dK
+    const uint32_t lane_addr = (quad * 32u) << 16;
+    float* dq = p.dq_acc + int64_t(b) * p.S * p.H + head * DH + r;
+    bool ok = true;
+    for (int n = 0; n < N; ++n) {
+      if (!mbar_wait_warp(mma_done, uint32_t(n) & 1u, wc, 36)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[64];
+      tmem_ld64(tmem_base + lane_addr + T_DQ, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+      const int i0 = j0 + n * BQ;
+      const int nq = p.S - i0;
+      // lanes hold consecutive head dims: each query's reduction is one coalesced request
+#pragma unroll
+      for (int e = 0; e < 64; ++e)
+        if (e < nq) atomicAdd(dq + int64_t(i0 + e) * p.H, v[e]);
+    }
+    if (ok) {
+      // the last step's commit covers every dV and dK product
+      const int key = j0 + r;
+      __nv_bfloat16* out = p.dz + (int64_t(b) * p.S + key) * p.ldz + head * DH;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {  // dV to column 2H, dK (scaled) to H
+        const uint32_t t = which ? T_DK : T_DV;
+        const float scale = which ? p.scale : 1.f;
+        __nv_bfloat16* dst = out + (which ? p.H : 2 * p.H);
+#pragma unroll
+        for (int ch = 0; ch < DH / 32; ++ch) {
+          uint32_t u[32];
+          tmem_ld32(tmem_base + lane_addr + t + 32 * ch, u);
+          tmem_ld_wait(u);
+          if (key < p.S) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * ch);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float* f = reinterpret_cast<const float*>(u) + 8 * q;
+              d4[q] = make_uint4(pack_bf16x2(f[0] * scale, f[1] * scale),
+                                 pack_bf16x2(f[2] * scale, f[3] * scale),
+                                 pack_bf16x2(f[4] * scale, f[5] * scale),
+                                 pack_bf16x2(f[6] * scale, f[7] * scale));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmVT, const CUtensorMap& tmDO,
+                           const SwaBwdParams& p, int* status, uint64_t limit_ns,
+                           cudaStream_t stream) {
+  if (p.dh != DH) return cudaErrorInvalidValue;
+  static cudaError_t attr = cudaFuncSetAttribute(
+      swa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
+  if (attr != cudaSuccess) return attr;
+  const int64_t tiles = (int64_t(p.S) + BKV - 1) / BKV;
+  const int64_t grid = tiles * p.nh * p.B;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  swa_bwd_kernel<<<unsigned(grid), THREADS, SMEM, stream>>>(tmQ, tmK, tmVT, tmDO, p, status,
+                                                             limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace pb

@@ -47,7 +47,16 @@ class pb_weights(ctypes.Structure):
 class pb_scratch_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("xn", "qk", "vt", "act", "io", "res0", "res1", "sk", "q8", "qscale", "seq_pad",
-                 "total")]
+                 "total", "hpre", "lse", "d_attn", "delta", "dq_acc", "dz", "dxn", "stats",
+                 "partials", "train_total")]
+
+
+GRAD_FIELDS = ("dx", "dgamma", "dbeta", "dwqkv", "dw1", "dwo", "dw2", "db_qkv", "db1", "db_o",
+               "db2")
+
+
+class pb_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in GRAD_FIELDS]
 
 
 class pb_options(ctypes.Structure):
@@ -80,6 +89,9 @@ SIGNATURES = {
     "pb_last_error_message": (ctypes.c_char_p, []),
     "pb_layernorm": (ctypes.c_int, [_I64, _I32, _P, _P, _P, ctypes.c_float, _P, _P]),
     "pb_quantize_rows_e4m3": (ctypes.c_int, [_I64, _I32, _P, _P, _P, _P]),
+    "pb_train_scratch_bytes": (ctypes.c_int, [_P, _P]),
+    "pb_forward_train": (ctypes.c_int, [_P, _P, _P, _P, _S, _P]),
+    "pb_backward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _S, _P]),
     "pb_gemm_scratch_bytes": (ctypes.c_int, [ctypes.POINTER(_S)]),
     "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _S, _P, _P]),
     "pb_gemm_bf16_layout": (ctypes.c_int, [_I32, _I32, _I32, _P, _I32, _P, _I32, _P, _P, _S, _P,
@@ -150,6 +162,17 @@ def scratch_bytes(dims: pb_dims) -> int:
     return n.value
 
 
+def train_scratch_bytes(dims: pb_dims) -> int:
+    n = ctypes.c_size_t()
+    _check("pb_train_scratch_bytes", lib().pb_train_scratch_bytes(ctypes.byref(dims),
+                                                                  ctypes.byref(n)))
+    return n.value
+
+
+def new_train_scratch(dims: pb_dims, device="cuda") -> torch.Tensor:
+    return torch.empty(train_scratch_bytes(dims), dtype=torch.uint8, device=device)
+
+
 def scratch_layout(dims: pb_dims) -> pb_scratch_layout:
     L = pb_scratch_layout()
     _check("pb_get_scratch_layout", lib().pb_get_scratch_layout(ctypes.byref(dims),
@@ -173,7 +196,11 @@ def scratch_view(scratch: torch.Tensor, dims: pb_dims, name: str,
               "res0": (T, H), "res1": (T, H),
               "vt": (dims.batch, dims.heads, dims.head_dim, L.seq_pad),
               "q8": (T, H + F), "qscale": (2 * T,)}
-    if name in ("res0", "res1", "qscale"):
+    Fp = 2 * F if dims.variant == 1 else F
+    nrow = dims.batch * dims.heads * dims.seq
+    shapes.update({"hpre": (T, Fp), "lse": (nrow,), "d_attn": (T, H), "delta": (nrow,),
+                   "dq_acc": (T, H), "dz": (T, 3 * H + Fp), "dxn": (T, H)})
+    if name in ("res0", "res1", "qscale", "lse", "delta", "dq_acc", "dxn"):
         dtype = torch.float32
     elif name == "q8":
         dtype = torch.uint8
@@ -230,6 +257,47 @@ class ParallelBlock:
                                            _ptr(ln2_beta), _ptr(scratch), scratch.numel(),
                                            _stream(stream)))
         return y
+
+    def forward_train(self, x: torch.Tensor, scratch: torch.Tensor, y: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+        """``pb_forward_train``: the forward pass, keeping in ``scratch`` (a training
+        scratch, ``new_train_scratch``) what ``backward`` reads."""
+        if y is None:
+            y = torch.empty_like(x)
+        _check("pb_forward_train",
+               self._lib.pb_forward_train(self.handle, _ptr(x), _ptr(y), _ptr(scratch),
+                                          scratch.numel(), _stream(stream)))
+        return y
+
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, scratch: torch.Tensor,
+                 grads: dict | None = None, accumulate: bool = False, biases: bool = True,
+                 stream=None) -> dict:
+        """``pb_backward`` after ``forward_train(x, scratch)``: returns the gradients (``dx``
+        bf16, the parameter gradients fp32 in their ``pb_weights`` layout, keyed like
+        ``GRAD_FIELDS``). ``grads`` may hold preallocated buffers (needed for
+        ``accumulate``)."""
+        d = self.dims
+        H, F, T = d.hidden, d.ffn, d.batch * d.seq
+        Fp = 2 * F if d.variant == 1 else F
+        shapes = {"dx": (T, H), "dgamma": (H,), "dbeta": (H,), "dwqkv": (H, 3 * H),
+                  "dw1": (H, Fp), "dwo": (H, H), "dw2": (F, H), "db_qkv": (3 * H,),
+                  "db1": (Fp,), "db_o": (H,), "db2": (H,)}
+        g = dict(grads or {})
+        for n, shp in shapes.items():
+            if n in g:
+                continue
+            if n in ("db_qkv", "db1", "db_o", "db2") and not biases:
+                continue
+            if n == "dbeta" and d.variant == 1:
+                continue
+            dt = torch.bfloat16 if n == "dx" else torch.float32
+            g[n] = torch.zeros(shp, dtype=dt, device=x.device)
+        gs = pb_grads(*[_ptr(g.get(n)) for n in GRAD_FIELDS])
+        _check("pb_backward",
+               self._lib.pb_backward(self.handle, _ptr(x), _ptr(dy), ctypes.byref(gs),
+                                     int(accumulate), _ptr(scratch), scratch.numel(),
+                                     _stream(stream)))
+        return g
 
     def status(self) -> int:
         return self._lib.pb_get_status(self.handle)
