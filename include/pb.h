@@ -118,10 +118,10 @@ typedef struct pb_weights {
  * A training scratch (pb_forward_train / pb_backward, train_total bytes) has the same
  * regions up to `total`, then:
  *   hpre   [T, F']       h before the activation (bf16; SwiGLU: W1cat's interleaved order)
- *   lse    [batch, heads, seq]  fp32 log2-sum-exp of each attention row's scores x
- *                        log2(e) / sqrt(dh)
+ *   lse    [batch * heads, seq64]  fp32 log2-sum-exp of each attention row's scores x
+ *                        log2(e) / sqrt(dh); seq64 = seq rounded up to 64
  *   d_attn [T, H]        dL/d(attention output) (bf16)
- *   delta  [batch, heads, seq]  fp32 dO . O per row
+ *   delta  [batch * heads, seq64]  fp32 dO . O per row
  *   dq_acc [T, H]        fp32 dq accumulator
  *   dz     [T, 3H + F']  [dq | dk | dv | dh], dL/d[q | k | v | h] (bf16, W1cat order)
  *   dxn    [T, H]        fp32 dL/dLN(x)

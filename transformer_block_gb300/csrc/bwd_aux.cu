@@ -45,7 +45,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // One warp per (token, head): dh / 32 consecutive elements per lane.
 __global__ void attn_delta_kernel(const __nv_bfloat16* __restrict__ dO,
                                   const __nv_bfloat16* __restrict__ O, int64_t o_ld, int B, int S,
-                                  int nh, int dh, float* __restrict__ delta) {
+                                  int nh, int dh, float* __restrict__ delta, int64_t lse_ld) {
   const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t T = int64_t(B) * S;
@@ -65,7 +65,7 @@ __global__ void attn_delta_kernel(const __nv_bfloat16* __restrict__ dO,
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
     const int64_t b = t / S, i = t % S;
-    delta[(b * nh + head) * S + i] = acc;
+    delta[(b * nh + head) * lse_ld + i] = acc;
   }
 }
 
@@ -224,13 +224,15 @@ __global__ void col_reduce_kernel(const float* __restrict__ partials, int64_t N,
 }  // namespace
 
 cudaError_t launch_attn_delta(const __nv_bfloat16* dO, const __nv_bfloat16* O, int64_t o_ld,
-                              int B, int S, int nh, int dh, float* delta, cudaStream_t stream) {
+                              int B, int S, int nh, int dh, float* delta, int64_t lse_ld,
+                              cudaStream_t stream) {
   const int64_t warps = int64_t(B) * S * nh;
   if (warps <= 0) return cudaSuccess;
   if (dh % 64 != 0) return cudaErrorInvalidValue;
   const int64_t blocks = (warps * 32 + THREADS - 1) / THREADS;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_delta_kernel<<<unsigned(blocks), THREADS, 0, stream>>>(dO, O, o_ld, B, S, nh, dh, delta);
+  attn_delta_kernel<<<unsigned(blocks), THREADS, 0, stream>>>(dO, O, o_ld, B, S, nh, dh, delta,
+                                                               lse_ld);
   return cudaGetLastError();
 }
 

@@ -41,7 +41,12 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16;
+// Per epilogue warp, a 32 x 32 fp32 chunk (rows padded to 33 words: conflict-free both
+// ways) for the coalesced gradient stores.
+constexpr int STAGE_PITCH = 33;
+constexpr size_t EPI_STAGE_OFF = size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16;
+constexpr size_t SMEM_BYTES = 1024 + EPI_STAGE_OFF + 4 * 32 * STAGE_PITCH * 4;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of the GEMM");
 
 __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
@@ -297,6 +302,50 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
   }
 }
 
+// Destination of columns [col0 + cq, col0 + cq + 4) of gradient row `row` (kEpiGrad).
+__device__ __forceinline__ float* grad_dst(const EpiParams& ep, int row, int col0, int cq) {
+  if (row >= ep.split_row) return ep.g1 + int64_t(row - ep.split_row) * ep.ld1 + col0 + cq;
+  if (col0 >= ep.split_col) {
+    const int c = col0 - ep.split_col;
+    float* base = ep.g1 + int64_t(row) * ep.ld1;
+    if (ep.glu)  // undo the W1cat interleave: 16 gate then 16 up features
+      return cq < 16 ? base + c / 2 + cq : base + ep.F + c / 2 + (cq - 16);
+    return base + c + cq;
+  }
+  return ep.g0 + int64_t(row) * ep.ld0 + col0 + cq;
+}
+
+// kEpiGrad for a warp's 32 rows [row0, row0 + 32) x 32 columns: the chunk goes through
+// shared memory so that each store instruction writes four whole 128-byte rows (eight
+// lanes per row) instead of 32 rows' 16-byte pieces.
+__device__ __forceinline__ void grad_store_warp(const EpiParams& ep, int row0, int col0,
+                                                const float (&v)[32], float* stage) {
+  const int lane = int(threadIdx.x & 31);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) stage[lane * STAGE_PITCH + i] = v[i];
+  __syncwarp();
+  const int cq = (lane & 7) * 4;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = 4 * it + (lane >> 3);
+    const int row = row0 + r;
+    if (row < ep.M) {
+      const float* sr = stage + r * STAGE_PITCH + cq;
+      float4 o = make_float4(sr[0], sr[1], sr[2], sr[3]);
+      float4* dst = reinterpret_cast<float4*>(grad_dst(ep, row, col0, cq));
+      if (ep.accumulate) {
+        const float4 a = *dst;
+        o.x += a.x;
+        o.y += a.y;
+        o.z += a.z;
+        o.w += a.w;
+      }
+      *dst = o;
+    }
+  }
+  __syncwarp();
+}
+
 // The work of one CTA pair: first whole tiles t = cluster, cluster + clusters, ... below
 // dp_tiles, then its contiguous share [cluster * W, (cluster + 1) * W) of the linearised
 // (tile, k-block) iterations of the sk_tiles stream-K tiles that follow them.
@@ -547,6 +596,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // -------------------------------------------------------------- epilogue warps
     const uint32_t quad = warp & 3;
+    float* epi_stage = reinterpret_cast<float*>(smem + EPI_STAGE_OFF) +
+                       (warp - 2) * 32 * STAGE_PITCH;
     int acc = 0;
     uint32_t acc_par = 0;
     UnitIter ui(sc);
@@ -632,7 +683,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               v[4 * q + 3] += pv.w;
             }
           }
-          epilogue32<KIND>(ep, row, col0, v);
+          if (KIND == kEpiGrad)
+            grad_store_warp(ep, row - int(lane), col0, v, epi_stage);
+          else
+            epilogue32<KIND>(ep, row, col0, v);
         }
       }
       tc_fence_before();

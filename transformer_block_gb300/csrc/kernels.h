@@ -125,8 +125,9 @@ struct SwaParams {
   void* out;  // attention output, row (b*S + i), columns [head*dh, (head+1)*dh)
   int64_t out_ld;
   bool out_f16;  // write fp16 (else bf16)
-  float* lse;    // training forward: [B, nh, S] log2-sum-exp of each row's scores
+  float* lse;    // training forward: [B * nh, lse_ld] log2-sum-exp of each row's scores
                  // (times log2(e) / sqrt(dh)), or null
+  int64_t lse_ld;
 };
 constexpr int kSwaBQ = 128;  // query rows per tile (two tiles per CTA)
 constexpr int kSwaBKV = 128;  // keys per tile
@@ -138,7 +139,8 @@ cudaError_t launch_swa(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 
 // ---------------------------------------------------------------- attention backward
 // (swa_bwd.cu). q | k and v^T as the forward left them, dO = d_attn [B][S][H] bf16, the
-// forward's lse and delta[b, head, i] = dO_i . O_i ([B, nh, S] fp32). Adds dq (unscaled)
+// forward's lse and delta[b, head, i] = dO_i . O_i ([B * nh, lse_ld] fp32, lse_ld a multiple
+// of 64 >= S). Adds dq (unscaled)
 // into dq_acc [T, H] fp32 (zeroed by the caller) and writes dk (scaled by 1/sqrt(dh)) and
 // dv as bf16 into dz columns [H, 2H) and [2H, 3H) (row stride ldz). dh == 128.
 struct SwaBwdParams {
@@ -147,6 +149,7 @@ struct SwaBwdParams {
   float scale;       // 1 / sqrt(dh)
   const float* lse;
   const float* delta;
+  int64_t lse_ld;
   float* dq_acc;
   __nv_bfloat16* dz;
   int64_t ldz;
@@ -160,10 +163,11 @@ cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
 
 // ---------------------------------------------------------------- backward helpers
 // (bwd_aux.cu)
-// delta[(b * nh + head) * S + s] = sum_d dO[t, head*dh + d] * O[t, head*dh + d], t = b*S + s
-// (dO: [T, H] bf16; O: the attention output, row stride o_ld).
+// delta[(b * nh + head) * lse_ld + s] = sum_d dO[t, head*dh + d] * O[t, head*dh + d],
+// t = b*S + s (dO: [T, H] bf16; O: the attention output, row stride o_ld).
 cudaError_t launch_attn_delta(const __nv_bfloat16* dO, const __nv_bfloat16* O, int64_t o_ld,
-                              int B, int S, int nh, int dh, float* delta, cudaStream_t stream);
+                              int B, int S, int nh, int dh, float* delta, int64_t lse_ld,
+                              cudaStream_t stream);
 // dz[t * ldz + c] = bf16(dq_acc[t * H + c] * scale), c < H.
 cudaError_t launch_dq_to_bf16(const float* dq_acc, int64_t T, int H, float scale,
                               __nv_bfloat16* dz, int64_t ldz, cudaStream_t stream);

@@ -155,6 +155,10 @@ WsLayout ws_layout(const pb_dims& d) {
   return L;
 }
 
+// Row stride of the per-row attention values of training (log-sum-exp, D): the sequence
+// rounded up to 64, so the backward's 64-row copies of them stay inside a row.
+size_t lse_ld(const pb_dims& d) { return align_up(size_t(d.seq), 64); }
+
 pb_scratch_layout scratch_layout(const pb_dims& d) {
   const size_t H = size_t(d.hidden), F = size_t(d.ffn);
   const size_t T = size_t(d.batch) * size_t(d.seq);
@@ -185,7 +189,7 @@ pb_scratch_layout scratch_layout(const pb_dims& d) {
   // training: what the backward reads from the forward, then its own intermediates
   const size_t Fp = size_t(w1_rows(d)) - 3 * H;  // F, or 2F for SwiGLU
   const size_t NZ = size_t(w1_rows(d));          // columns of dz = [dq | dk | dv | dh]
-  const size_t rows_lse = size_t(d.batch) * size_t(d.heads) * size_t(d.seq);
+  const size_t rows_lse = size_t(d.batch) * size_t(d.heads) * lse_ld(d);
   L.hpre = off;
   off = align_up(off + T * Fp * 2, 1024);
   L.lse = off;
@@ -383,7 +387,10 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   sp.out = act;
   sp.out_ld = H + F;
   sp.out_f16 = h->f16;
-  if (train) sp.lse = reinterpret_cast<float*>(scratch + L.lse);
+  if (train) {
+    sp.lse = reinterpret_cast<float*>(scratch + L.lse);
+    sp.lse_ld = int64_t(lse_ld(d));
+  }
   PB_CUDA(pb::launch_swa(tm_qk, tm_k, tm_vt, sp, h->status, h->limit_ns, st), "attention launch");
   PB_CUDA(mark(3), "cudaEventRecord");
 
@@ -575,7 +582,7 @@ pb_status run_backward(pb_handle* h, const void* x, const void* dy, const pb_gra
           "backward GEMM (d_attn, dh) launch");
   // 2. delta
   PB_CUDA(pb::launch_attn_delta(d_attn, bf(L.act), H + F, d.batch, d.seq, d.heads, d.head_dim,
-                                f32(L.delta), st),
+                                f32(L.delta), int64_t(lse_ld(d)), st),
           "delta launch");
   // 3. attention backward
   CUtensorMap tm_q, tm_k, tm_vt, tm_do;
@@ -606,6 +613,7 @@ pb_status run_backward(pb_handle* h, const void* x, const void* dy, const pb_gra
   sb.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d.head_dim)));
   sb.lse = f32(L.lse);
   sb.delta = f32(L.delta);
+  sb.lse_ld = int64_t(lse_ld(d));
   sb.dq_acc = f32(L.dq_acc);
   sb.dz = dz;
   sb.ldz = NZ;

@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float inv_l = 1.f / l;
         // training forward: the row's log2-sum-exp, from which the backward recomputes P
         if (p.lse != nullptr && i < p.S)
-          p.lse[(int64_t(it.b) * p.nh + it.head) * p.S + i] = m_used + log2f(l);
+          p.lse[(int64_t(it.b) * p.nh + it.head) * p.lse_ld + i] = m_used + log2f(l);
         const int64_t off = (int64_t(it.b) * p.S + i) * p.out_ld + it.head * DH;
         bool bad = false;
 #pragma unroll

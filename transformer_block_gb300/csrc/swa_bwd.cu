@@ -13,24 +13,26 @@
 // One CTA per (128-key tile, head, sequence), the key tiles with the most queries first.
 // It keeps K and V of its keys in shared memory and dV, dK (fp32) in tensor memory, and
 // walks the 64-query steps that reach its keys (from its first key to the last query whose
-// window does):
-//   S^T  = K Q^T        (M = 128 keys, N = 64 queries)        tensor memory
-//   dP^T = V dO^T       (A = V, MN-major from v^T)            tensor memory
-//   softmax warps: P^T, dS^T (bf16) back into tensor memory over S^T and dP^T, and dS
-//                  into shared memory
-//   dV  += P^T dO,  dK += dS^T Q   (A from tensor memory, B = dO, Q read MN-major)
-//   dQ^T = K^T dS       (M = dh, N = 64 queries; both operands MN-major)
-// and a second group of warps adds dQ^T into an fp32 dq accumulator in global memory
-// (one coalesced reduction per query and head; other key tiles add theirs). The same
+// window does). Step n, in tensor-memory buffer b = n % 2:
+//   S^T  = K Q^T        (M = 128 keys, N = 64 queries)              buffer b, columns 0-63
+//   dP^T = V dO^T       (A = V, MN-major from v^T)                  buffer b, columns 64-127
+//   P and dS warps: P^T and dS^T (bf16) over S^T and dP^T, dS into shared memory (b)
+//   dV  += P^T dO,  dK += dS^T Q   (A from tensor memory, B = dO and Q read MN-major)
+//   dQ^T = K^T dS       (M = dh, N = 64 queries; both operands MN-major) over buffer b
+//   dQ warps: dQ^T out, added into the fp32 dq accumulator in global memory (one coalesced
+//             reduction per query and head; other key tiles add theirs)
+// With two buffers the P/dS math of step n + 1 runs while the tensor cores compute the
+// dV, dK and dQ products of step n; buffer b is loaded with the scores of step n + 2 once
+// dQ^T of step n has been read out. The MMAs of one thread execute in issue order, so dQ^T
+// overwrites P^T only after dV has read it; a commit covers every earlier MMA. The same
 // shared-memory tiles serve as K-major and as MN-major operands: a TMA box of 64 16-bit
 // elements per row is both.
-//   warp 0     TMA producer: K and V once, then Q and dO per step (2-stage ring)
+//   warp 0     TMA producer: K and V once, then per step Q, dO and the step's 64 values
+//              of the log-sum-exp and of D (2-stage ring)
 //   warp 1     tensor-memory owner and the MMA-issuing thread
-//   warps 2-5  recompute P and dS, one key per thread (its TMEM lane)
-//   warps 6-9  dQ reduction per step, then the dK and dV rows of the tile
-// Tensor memory: S^T [0, 64) | dP^T [64, 128) | dQ^T [128, 192) | dV [192, 320) |
-// dK [320, 448). The MMAs of one thread execute in issue order, so the next step's S^T
-// overwrites P^T only after dV has read it; a commit covers every earlier MMA.
+//   warps 2-5  P and dS, one key per thread (its TMEM lane)
+//   warps 6-9  dQ per step, then the dK and dV rows of the tile
+// Tensor memory: buffer 0 [0, 128) | buffer 1 [128, 256) | dV [256, 384) | dK [384, 512).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -42,21 +44,23 @@ constexpr int BQ = 64;    // queries per step
 constexpr int DH = 128;   // head dim
 constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 192, T_DK = 320;
+constexpr uint32_t T_BUF = 128, T_DP = 64, T_DV = 256, T_DK = 384;
 constexpr int K_BOX = BKV * 64 * 2;   // 16 KB: 128 keys x 64 dims
 constexpr int K_BYTES = 2 * K_BOX;
 constexpr int V_HALF = DH * 64 * 2;   // 16 KB: dh rows x 64 keys (from v^T)
 constexpr int V_BYTES = 2 * V_HALF;
 constexpr int QD_BOX = BQ * 64 * 2;   // 8 KB: 64 queries x 64 dims
 constexpr int Q_BYTES = 2 * QD_BOX;
-constexpr int STAGE_BYTES = 2 * Q_BYTES;  // Q and dO
+constexpr int ROWVAL_BYTES = BQ * 4;  // 64 fp32 values of L or D
+constexpr int STAGE_TX = 2 * Q_BYTES + 2 * ROWVAL_BYTES;  // Q, dO, L, D
+constexpr int STAGE_BYTES = 2 * Q_BYTES + 1024;           // next stage 1024-aligned
 constexpr int STAGES = 2;
 constexpr int DS_BYTES = BKV * BQ * 2;  // dS: 128 key rows x 64 queries
 constexpr int K_OFF = 0, V_OFF = K_BYTES, ST_OFF = V_OFF + V_BYTES;
 constexpr int DS_OFF = ST_OFF + STAGES * STAGE_BYTES;
-constexpr int BAR_OFF = DS_OFF + DS_BYTES;
-// kv_full, q_full[2], q_empty[2], s_full, p_full, mma_done, dq_free, drain
-constexpr int NUM_BARS = 10;
+constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
+// kv_full, q_full[2], q_empty[2], s_full[2], p_full[2], mma_done[2], dq_free[2], drain
+constexpr int NUM_BARS = 14;
 constexpr size_t SMEM = size_t(BAR_OFF) + NUM_BARS * 8 + 16 + 1024;
 static_assert(SMEM <= 227 * 1024 && 2 * SMEM > 228 * 1024,
               "one CTA per SM: it takes all tensor-memory columns");
@@ -71,7 +75,8 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int e = 0; e < 64; ++e) v[e] = __uint_as_float(u[e]);
 }
 
-// The step's work: the key tile's first query step and the number of 64-query steps.
+// The step count of key tile j0: from its first key to the last query whose window
+// reaches the tile, in 64-query steps.
 __device__ __forceinline__ int num_steps(const SwaBwdParams& p, int j0) {
   const int last = min(p.S - 1, j0 + BKV - 1 + p.window - 1);
   return last / BQ - j0 / BQ + 1;
@@ -87,13 +92,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   const uint32_t kv_full = smem_u32(bars + 0);
-  const uint32_t q_full0 = smem_u32(bars + 1);   // [2]
-  const uint32_t q_empty0 = smem_u32(bars + 3);  // [2]
-  const uint32_t s_full = smem_u32(bars + 5);
-  const uint32_t p_full = smem_u32(bars + 6);    // 4 softmax warps
-  const uint32_t mma_done = smem_u32(bars + 7);  // the step's dV, dK, dQ^T products
-  const uint32_t dq_free = smem_u32(bars + 8);   // 4 reduction warps read dQ^T out
-  const uint32_t drain_bar = smem_u32(bars + 9);
+  const uint32_t q_full0 = smem_u32(bars + 1);    // [2] per stage
+  const uint32_t q_empty0 = smem_u32(bars + 3);   // [2]
+  const uint32_t s_full0 = smem_u32(bars + 5);    // [2] per tensor-memory buffer
+  const uint32_t p_full0 = smem_u32(bars + 7);    // [2] (4 P/dS warps)
+  const uint32_t mma_done0 = smem_u32(bars + 9);  // [2] the step's dV, dK, dQ^T products
+  const uint32_t dq_free0 = smem_u32(bars + 11);  // [2] (4 dQ warps read dQ^T out)
+  const uint32_t drain_bar = smem_u32(bars + 13);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -105,18 +110,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int b = (int(blockIdx.x) / p.nh) % p.B;
   const int j0 = jt * BKV;
   const int N = num_steps(p, j0);
+  const int64_t row_off = int64_t(b * p.nh + head) * p.lse_ld;  // of L and D
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(q_full0 + 8 * s, 1);
       mbar_init(q_empty0 + 8 * s, 1);
+      mbar_init(s_full0 + 8 * s, 1);
+      mbar_init(p_full0 + 8 * s, 4);
+      mbar_init(mma_done0 + 8 * s, 1);
+      mbar_init(dq_free0 + 8 * s, 4);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 4);
-    mbar_init(mma_done, 1);
-    mbar_init(dq_free, 4);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -153,15 +159,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int n = 0; n < N; ++n) {
         const int st = n & 1;
         if (!mbar_wait(q_empty0 + 8 * st, uint32_t((n >> 1) & 1) ^ 1u, wc, 30)) break;
-        const uint32_t dst = sST + st * STAGE_BYTES;
+        const uint32_t dst = sST + st * STAGE_BYTES, bar = q_full0 + 8 * st;
         const int i0 = j0 + n * BQ;
-        mbar_arrive_expect_tx(q_full0 + 8 * st, STAGE_BYTES);
+        mbar_arrive_expect_tx(bar, STAGE_TX);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          tma_load_3d(dst + c * QD_BOX, &tmQ, q_full0 + 8 * st, head * DH + 64 * c, i0, b);
-          tma_load_3d(dst + Q_BYTES + c * QD_BOX, &tmDO, q_full0 + 8 * st, head * DH + 64 * c,
-                      i0, b);
+          tma_load_3d(dst + c * QD_BOX, &tmQ, bar, head * DH + 64 * c, i0, b);
+          tma_load_3d(dst + Q_BYTES + c * QD_BOX, &tmDO, bar, head * DH + 64 * c, i0, b);
         }
+        // the rows' L and D (row stride lse_ld, a multiple of 64: never past the row)
+        bulk_load(dst + 2 * Q_BYTES, p.lse + row_off + i0, ROWVAL_BYTES, bar);
+        bulk_load(dst + 2 * Q_BYTES + ROWVAL_BYTES, p.delta + row_off + i0, ROWVAL_BYTES, bar);
         issued = n + 1;
       }
       // the CTA's own copies land before it may exit
@@ -172,55 +180,68 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------------ MMA issuer
-      const uint32_t id_s = idesc_f32acc(BKV, BQ);                     // K, Q K-major
-      const uint32_t id_dp = idesc_f32acc(BKV, BQ, false, true, false);  // V MN-major
+      const uint32_t id_s = idesc_f32acc(BKV, BQ);                        // K, Q K-major
+      const uint32_t id_dp = idesc_f32acc(BKV, BQ, false, true, false);   // V MN-major
       const uint32_t id_acc = idesc_f32acc(BKV, DH, false, false, true);  // TMEM A, B MN
-      const uint32_t id_dq = idesc_f32acc(DH, BQ, false, true, true);   // both MN-major
+      const uint32_t id_dq = idesc_f32acc(DH, BQ, false, true, true);     // both MN-major
       const uint64_t dK = sdesc_kmajor_sw128(sK), dKmn = sdesc_mnmajor_sw128(sK, K_BOX);
       const uint64_t dVmn = sdesc_mnmajor_sw128(sV, V_HALF);
-      const uint64_t dDS = sdesc_mnmajor_sw128(sDS, DS_BYTES);
-      bool ok = mbar_wait(kv_full, 0, wc, 31);
-      for (int n = 0; ok && n < N; ++n) {
+      // S^T and dP^T of step n into buffer n % 2 (its Q / dO stage is n % 2 too)
+      auto issue_scores = [&](int n) -> bool {
         const int st = n & 1;
-        const uint32_t sQ = sST + st * STAGE_BYTES, sDO = sQ + Q_BYTES;
-        if (!mbar_wait(q_full0 + 8 * st, uint32_t(n >> 1) & 1u, wc, 32)) break;
+        if (!mbar_wait(q_full0 + 8 * st, uint32_t(n >> 1) & 1u, wc, 32)) return false;
         tc_fence_after();
+        const uint32_t sQ = sST + st * STAGE_BYTES, sDO = sQ + Q_BYTES;
         const uint64_t dQk = sdesc_kmajor_sw128(sQ), dDOk = sdesc_kmajor_sw128(sDO);
-        // S^T = K Q^T and dP^T = V dO^T, K = dh in steps of 16
+        const uint32_t t = tmem_base + uint32_t(st) * T_BUF;
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t ok_ = uint64_t(((kk >> 2) * K_BOX) >> 4) + 2 * (kk & 3);
           const uint64_t oq = uint64_t(((kk >> 2) * QD_BOX) >> 4) + 2 * (kk & 3);
-          mma_f16kind_ss(tmem_base + T_S, dK + ok_, dQk + oq, id_s, kk > 0 ? 1u : 0u);
+          mma_f16kind_ss(t, dK + ok_, dQk + oq, id_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t oq = uint64_t(((kk >> 2) * QD_BOX) >> 4) + 2 * (kk & 3);
-          mma_f16kind_ss(tmem_base + T_DP, dVmn + 128 * kk, dDOk + oq, id_dp, kk > 0 ? 1u : 0u);
+          mma_f16kind_ss(t + T_DP, dVmn + 128 * kk, dDOk + oq, id_dp, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, uint32_t(n) & 1u, wc, 33)) break;
+        mma_commit(s_full0 + 8 * st);
+        return true;
+      };
+      bool ok = mbar_wait(kv_full, 0, wc, 31);
+      if (ok) ok = issue_scores(0);
+      if (ok && N > 1) ok = issue_scores(1);
+      for (int n = 0; ok && n < N; ++n) {
+        const int bf = n & 1;
+        const uint32_t par = uint32_t(n >> 1) & 1u;
+        if (!mbar_wait(p_full0 + 8 * bf, par, wc, 33)) break;
         tc_fence_after();
+        const uint32_t t = tmem_base + uint32_t(bf) * T_BUF;
+        const uint32_t sQ = sST + bf * STAGE_BYTES, sDO = sQ + Q_BYTES;
         // dV += P^T dO, dK += dS^T Q: K = the step's 64 queries
         const uint64_t dDOmn = sdesc_mnmajor_sw128(sDO, QD_BOX);
         const uint64_t dQmn = sdesc_mnmajor_sw128(sQ, QD_BOX);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_f16kind_ts(tmem_base + T_DV, tmem_base + T_S + 8 * kk, dDOmn + 128 * kk, id_acc,
+          mma_f16kind_ts(tmem_base + T_DV, t + 8 * kk, dDOmn + 128 * kk, id_acc,
                          (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_f16kind_ts(tmem_base + T_DK, tmem_base + T_DP + 8 * kk, dQmn + 128 * kk, id_acc,
+          mma_f16kind_ts(tmem_base + T_DK, t + T_DP + 8 * kk, dQmn + 128 * kk, id_acc,
                          (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(q_empty0 + 8 * st);  // Q and dO of this stage are read
-        // dQ^T = K^T dS once the previous step's dQ^T has been read out
-        if (n > 0 && !mbar_wait(dq_free, uint32_t(n - 1) & 1u, wc, 34)) break;
-        tc_fence_after();
+        mma_commit(q_empty0 + 8 * bf);  // Q and dO of this stage are read
+        // dQ^T = K^T dS over the buffer's first 64 columns (after dV has read P^T there)
+        const uint64_t dDS = sdesc_mnmajor_sw128(sDS + bf * DS_BYTES, DS_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_f16kind_ss(tmem_base + T_DQ, dKmn + 128 * kk, dDS + 128 * kk, id_dq,
-                         kk > 0 ? 1u : 0u);
-        mma_commit(mma_done);
+          mma_f16kind_ss(t, dKmn + 128 * kk, dDS + 128 * kk, id_dq, kk > 0 ? 1u : 0u);
+        mma_commit(mma_done0 + 8 * bf);
+        // the buffer takes step n + 2's scores once dQ^T of step n is out
+        if (n + 2 < N) {
+          if (!mbar_wait(dq_free0 + 8 * bf, par, wc, 34)) break;
+          tc_fence_after();
+          if (!issue_scores(n + 2)) break;
+        }
       }
       mma_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0, drain_ns);
@@ -233,20 +254,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int key = j0 + r;
     const uint32_t lane_addr = (quad * 32u) << 16;
     const float c = p.scale_log2;
-    const float* lse = p.lse + int64_t(b * p.nh + head) * p.S;
-    const float* dlt = p.delta + int64_t(b * p.nh + head) * p.S;
-    uint8_t* ds_row = smem + DS_OFF + r * 128;
     const int sw = r & 7;  // 128-byte swizzle of the row's 16-byte chunks
     for (int n = 0; n < N; ++n) {
-      if (!mbar_wait_warp(s_full, uint32_t(n) & 1u, wc, 35)) break;
+      const int bf = n & 1;
+      const uint32_t par = uint32_t(n >> 1) & 1u;
+      // the scores, and the stage's L and D values (already complete: the scores were
+      // computed from the same stage)
+      if (!mbar_wait_warp(s_full0 + 8 * bf, par, wc, 35) ||
+          !mbar_wait_warp(q_full0 + 8 * bf, par, wc, 37))
+        break;
       tc_fence_after();
+      const uint32_t t = tmem_base + lane_addr + uint32_t(bf) * T_BUF;
+      const float* Ls =
+          reinterpret_cast<const float*>(smem + ST_OFF + bf * STAGE_BYTES + 2 * Q_BYTES);
+      const float* Ds = Ls + BQ;
+      uint8_t* ds_row = smem + DS_OFF + bf * DS_BYTES + r * 128;
       const int i0 = j0 + n * BQ;
-      // two halves of 32 queries: S^T and dP^T in, P^T and dS^T out over them, dS to shared
+      // two halves of 32 queries: S^T and dP^T in, P^T and dS^T out over them (the halves
+      // already read), the dS row to shared memory
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t us[32], ud[32];
-        tmem_ld32(tmem_base + lane_addr + T_S + 32 * hf, us);
-        tmem_ld32(tmem_base + lane_addr + T_DP + 32 * hf, ud);
+        tmem_ld32(t + 32 * hf, us);
+        tmem_ld32(t + T_DP + 32 * hf, ud);
         tmem_ld_wait(us);
         tmem_ld_wait_regs(ud);
         uint32_t pk[16], dk[16];
@@ -255,21 +285,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           float pv[2], dv[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int q = i0 + 32 * hf + e + h, d = q - key;
-            pv[h] = 0.f;
-            dv[h] = 0.f;
-            if (d >= 0 && d < p.window && q < p.S) {  // q's window holds the key
-              pv[h] = ex2_approx(__uint_as_float(us[e + h]) * c - __ldg(lse + q));
-              dv[h] = pv[h] * (__uint_as_float(ud[e + h]) - __ldg(dlt + q));
-            }
+            const int qi = 32 * hf + e + h;
+            const int q = i0 + qi, d = q - key;
+            const float pr = ex2_approx(__uint_as_float(us[e + h]) * c - Ls[qi]);
+            pv[h] = (d >= 0 && d < p.window && q < p.S) ? pr : 0.f;  // q's window holds the key
+            dv[h] = pv[h] * (__uint_as_float(ud[e + h]) - Ds[qi]);
           }
           pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
           dk[e / 2] = pack_bf16x2(dv[0], dv[1]);
         }
-        // P^T over S^T and dS^T over dP^T (the A operands of dV and dK; 32 queries = 16
-        // packed columns), and the dS row's 4 chunks of 16 bytes to shared memory
-        tmem_st16(tmem_base + lane_addr + T_S + 16 * hf, pk);
-        tmem_st16(tmem_base + lane_addr + T_DP + 16 * hf, dk);
+        tmem_st16(t + 16 * hf, pk);
+        tmem_st16(t + T_DP + 16 * hf, dk);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
           *reinterpret_cast<uint4*>(ds_row + (((4 * hf + ch) ^ sw) << 4)) =
@@ -279,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full0 + 8 * bf);
     }
   } else {
     // ------------------------------------------------------------------ dQ, dK, dV out
@@ -289,16 +315,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* dq = p.dq_acc + int64_t(b) * p.S * p.H + head * DH + r;
     bool ok = true;
     for (int n = 0; n < N; ++n) {
-      if (!mbar_wait_warp(mma_done, uint32_t(n) & 1u, wc, 36)) {
+      const int bf = n & 1;
+      if (!mbar_wait_warp(mma_done0 + 8 * bf, uint32_t(n >> 1) & 1u, wc, 36)) {
         ok = false;
         break;
       }
       tc_fence_after();
       float v[64];
-      tmem_ld64(tmem_base + lane_addr + T_DQ, v);
+      tmem_ld64(tmem_base + lane_addr + uint32_t(bf) * T_BUF, v);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
+      if (lane == 0) mbar_arrive(dq_free0 + 8 * bf);
       const int i0 = j0 + n * BQ;
       const int nq = p.S - i0;
       // lanes hold consecutive head dims: each query's reduction is one coalesced request
@@ -312,13 +339,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       __nv_bfloat16* out = p.dz + (int64_t(b) * p.S + key) * p.ldz + head * DH;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {  // dV to column 2H, dK (scaled) to H
-        const uint32_t t = which ? T_DK : T_DV;
+        const uint32_t tcol = which ? T_DK : T_DV;
         const float scale = which ? p.scale : 1.f;
         __nv_bfloat16* dst = out + (which ? p.H : 2 * p.H);
 #pragma unroll
         for (int ch = 0; ch < DH / 32; ++ch) {
           uint32_t u[32];
-          tmem_ld32(tmem_base + lane_addr + t + 32 * ch, u);
+          tmem_ld32(tmem_base + lane_addr + tcol + 32 * ch, u);
           tmem_ld_wait(u);
           if (key < p.S) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * ch);
@@ -350,7 +377,7 @@ cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmVT, const CUtensorMap& tmDO,
                            const SwaBwdParams& p, int* status, uint64_t limit_ns,
                            cudaStream_t stream) {
-  if (p.dh != DH) return cudaErrorInvalidValue;
+  if (p.dh != DH || p.lse_ld % BQ != 0 || p.lse_ld < p.S) return cudaErrorInvalidValue;
   static cudaError_t attr = cudaFuncSetAttribute(
       swa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
   if (attr != cudaSuccess) return attr;

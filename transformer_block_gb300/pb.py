@@ -197,7 +197,7 @@ def scratch_view(scratch: torch.Tensor, dims: pb_dims, name: str,
               "vt": (dims.batch, dims.heads, dims.head_dim, L.seq_pad),
               "q8": (T, H + F), "qscale": (2 * T,)}
     Fp = 2 * F if dims.variant == 1 else F
-    nrow = dims.batch * dims.heads * dims.seq
+    nrow = dims.batch * dims.heads * ((dims.seq + 63) // 64 * 64)
     shapes.update({"hpre": (T, Fp), "lse": (nrow,), "d_attn": (T, H), "delta": (nrow,),
                    "dq_acc": (T, H), "dz": (T, 3 * H + Fp), "dxn": (T, H)})
     if name in ("res0", "res1", "qscale", "lse", "delta", "dq_acc", "dxn"):
