@@ -155,11 +155,12 @@ struct SwaBwdParams {
   int64_t ldz;
 };
 // tmQ: q|k in boxes of 64 columns x 64 rows; tmK: the same in boxes of 64 x 128 rows;
-// tmVT: v^T in boxes of 64 keys x dh rows; tmDO: d_attn [B][S][H] in boxes of 64 x 64.
+// tmVT: v^T in boxes of 64 keys x dh rows; tmDO: d_attn [B][S][H] in boxes of 64 x 64;
+// tmDQ: dq_acc [B][S][H] fp32, unswizzled boxes of 32 columns x 64 rows.
 cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmVT, const CUtensorMap& tmDO,
-                           const SwaBwdParams& p, int* status, uint64_t limit_ns,
-                           cudaStream_t stream);
+                           const CUtensorMap& tmDQ, const SwaBwdParams& p, int* status,
+                           uint64_t limit_ns, cudaStream_t stream);
 
 // ---------------------------------------------------------------- backward helpers
 // (bwd_aux.cu)

@@ -267,6 +267,26 @@ pb_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d
   return PB_OK;
 }
 
+// fp32 tensor of `rank` dims, no swizzle (boxes land row-major in shared memory).
+pb_status make_map_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn enc;
+  pb_status s = get_encoder(&enc);
+  if (s != PB_OK) return s;
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(rank), const_cast<void*>(base),
+                   gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return PB_OK;
+}
+
 // Row-major [rows, cols] matrix of element type t read in boxes of 128 bytes of columns
 // (64 16-bit or 128 FP8 elements) x box_rows rows.
 pb_status make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -585,7 +605,7 @@ pb_status run_backward(pb_handle* h, const void* x, const void* dy, const pb_gra
                                 f32(L.delta), int64_t(lse_ld(d)), st),
           "delta launch");
   // 3. attention backward
-  CUtensorMap tm_q, tm_k, tm_vt, tm_do;
+  CUtensorMap tm_q, tm_k, tm_vt, tm_do, tm_dq;
   {
     const uint64_t qdims[3] = {2 * uint64_t(H), uint64_t(d.seq), uint64_t(d.batch)};
     const uint64_t qstr[2] = {2 * uint64_t(H) * 2, 2 * uint64_t(H) * 2 * uint64_t(d.seq)};
@@ -599,6 +619,9 @@ pb_status run_backward(pb_handle* h, const void* x, const void* dy, const pb_gra
     if (s == PB_OK) s = make_map(&tm_k, scratch + L.qk, 3, qdims, qstr, kbox);
     if (s == PB_OK) s = make_map(&tm_vt, scratch + L.vt, 2, vdims, vstr, vbox);
     if (s == PB_OK) s = make_map(&tm_do, d_attn, 3, odims, ostr, qbox);
+    const uint64_t fstr[2] = {uint64_t(H) * 4, uint64_t(H) * 4 * uint64_t(d.seq)};
+    const uint32_t fbox[3] = {32, 64, 1};
+    if (s == PB_OK) s = make_map_f32(&tm_dq, scratch + L.dq_acc, 3, odims, fstr, fbox);
     if (s != PB_OK) return s;
   }
   PB_CUDA(cudaMemsetAsync(f32(L.dq_acc), 0, size_t(T) * H * 4, st), "cudaMemsetAsync(dq)");
@@ -617,7 +640,7 @@ pb_status run_backward(pb_handle* h, const void* x, const void* dy, const pb_gra
   sb.dq_acc = f32(L.dq_acc);
   sb.dz = dz;
   sb.ldz = NZ;
-  PB_CUDA(pb::launch_swa_bwd(tm_q, tm_k, tm_vt, tm_do, sb, h->status, h->limit_ns, st),
+  PB_CUDA(pb::launch_swa_bwd(tm_q, tm_k, tm_vt, tm_do, tm_dq, sb, h->status, h->limit_ns, st),
           "attention backward launch");
   PB_CUDA(pb::launch_dq_to_bf16(f32(L.dq_acc), T, H, sb.scale, dz, NZ, st), "dq launch");
   // 4. dLN(x) = dz W1cat

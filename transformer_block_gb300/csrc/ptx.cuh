@@ -193,6 +193,35 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// TMA reduction: adds the box at `src` (this CTA's shared memory, laid out as the tensor
+// map's box) into the global tensor at coordinates (c0, c1, c2), element-wise (fp32 add
+// for an fp32 map). Asynchronous: the source may be reused after bulk_wait_read().
+// Coordinates must not be negative; parts of the box outside the tensor are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int32_t c0,
+                                                  int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until the committed bulk operations of this thread have finished reading shared
+// memory (the writes to global memory may still be in flight).
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until the committed bulk operations of this thread are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Barrier `id` (1-15; 0 is __syncthreads) among `n` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is signalled on an mbarrier of
 // either CTA of the pair (`bar` is a shared::cluster address, e.g. from mapa_shared): both
 // CTAs of a tcgen05 pair can report their copies to the one barrier the MMA issuer waits on.

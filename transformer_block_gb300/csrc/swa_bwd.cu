@@ -19,8 +19,9 @@
 //   P and dS warps: P^T and dS^T (bf16) over S^T and dP^T, dS into shared memory (b)
 //   dV  += P^T dO,  dK += dS^T Q   (A from tensor memory, B = dO and Q read MN-major)
 //   dQ^T = K^T dS       (M = dh, N = 64 queries; both operands MN-major) over buffer b
-//   dQ warps: dQ^T out, added into the fp32 dq accumulator in global memory (one coalesced
-//             reduction per query and head; other key tiles add theirs)
+//   dQ warps: dQ^T out, each warp's 32 head dims x 64 queries staged in shared memory and
+//             added into the fp32 dq accumulator in global memory by one TMA reduction
+//             (other key tiles add theirs)
 // With two buffers the P/dS math of step n + 1 runs while the tensor cores compute the
 // dV, dK and dQ products of step n; buffer b is loaded with the scores of step n + 2 once
 // dQ^T of step n has been read out. The MMAs of one thread execute in issue order, so dQ^T
@@ -58,7 +59,9 @@ constexpr int STAGES = 2;
 constexpr int DS_BYTES = BKV * BQ * 2;  // dS: 128 key rows x 64 queries
 constexpr int K_OFF = 0, V_OFF = K_BYTES, ST_OFF = V_OFF + V_BYTES;
 constexpr int DS_OFF = ST_OFF + STAGES * STAGE_BYTES;
-constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
+constexpr int DQ_WARP_BYTES = 32 * BQ * 4;  // a dQ warp's staging: 64 queries x 32 dims fp32
+constexpr int DQ_OFF = DS_OFF + 2 * DS_BYTES;
+constexpr int BAR_OFF = DQ_OFF + 4 * DQ_WARP_BYTES;
 // kv_full, q_full[2], q_empty[2], s_full[2], p_full[2], mma_done[2], dq_free[2], drain
 constexpr int NUM_BARS = 14;
 constexpr size_t SMEM = size_t(BAR_OFF) + NUM_BARS * 8 + 16 + 1024;
@@ -85,7 +88,8 @@ __device__ __forceinline__ int num_steps(const SwaBwdParams& p, int j0) {
 __global__ void __launch_bounds__(THREADS, 1)
     swa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVT,
-                   const __grid_constant__ CUtensorMap tmDO, const SwaBwdParams p, int* status,
+                   const __grid_constant__ CUtensorMap tmDO,
+                   const __grid_constant__ CUtensorMap tmDQ, const SwaBwdParams p, int* status,
                    uint64_t limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -132,6 +136,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmVT);
     tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDQ);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -312,7 +317,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t quad = warp & 3;
     const int r = int(quad * 32 + lane);  // TMEM lane: head dim of dQ^T, key of dV and dK
     const uint32_t lane_addr = (quad * 32u) << 16;
-    float* dq = p.dq_acc + int64_t(b) * p.S * p.H + head * DH + r;
+    float* dq_st = reinterpret_cast<float*>(smem + DQ_OFF + (warp - 6) * DQ_WARP_BYTES);
+    const uint32_t s_dq = smem_u32(dq_st);
     bool ok = true;
     for (int n = 0; n < N; ++n) {
       const int bf = n & 1;
@@ -327,12 +333,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free0 + 8 * bf);
       const int i0 = j0 + n * BQ;
-      const int nq = p.S - i0;
-      // lanes hold consecutive head dims: each query's reduction is one coalesced request
+      // the warp's [64 queries][32 dims] block of dQ into its staging buffer (once the
+      // previous step's reduction has read it), then one TMA add into dq (rows past the
+      // sequence are outside the map's bounds and skipped)
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
 #pragma unroll
-      for (int e = 0; e < 64; ++e)
-        if (e < nq) atomicAdd(dq + int64_t(i0 + e) * p.H, v[e]);
+      for (int e = 0; e < 64; ++e) dq_st[e * 32 + lane] = v[e];
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tmDQ, s_dq, head * DH + int(quad) * 32, i0, b);
+        bulk_commit();
+      }
     }
+    if (lane == 0) bulk_wait_all();  // before the CTA's shared memory is released
+    __syncwarp();
     if (ok) {
       // the last step's commit covers every dV and dK product
       const int key = j0 + r;
@@ -375,8 +391,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmVT, const CUtensorMap& tmDO,
-                           const SwaBwdParams& p, int* status, uint64_t limit_ns,
-                           cudaStream_t stream) {
+                           const CUtensorMap& tmDQ, const SwaBwdParams& p, int* status,
+                           uint64_t limit_ns, cudaStream_t stream) {
   if (p.dh != DH || p.lse_ld % BQ != 0 || p.lse_ld < p.S) return cudaErrorInvalidValue;
   static cudaError_t attr = cudaFuncSetAttribute(
       swa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
@@ -385,8 +401,8 @@ cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   const int64_t grid = tiles * p.nh * p.B;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  swa_bwd_kernel<<<unsigned(grid), THREADS, SMEM, stream>>>(tmQ, tmK, tmVT, tmDO, p, status,
-                                                             limit_ns);
+  swa_bwd_kernel<<<unsigned(grid), THREADS, SMEM, stream>>>(tmQ, tmK, tmVT, tmDO, tmDQ, p,
+                                                             status, limit_ns);
   return cudaGetLastError();
 }
 
