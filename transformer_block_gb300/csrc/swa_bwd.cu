@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = int(quad * 32 + lane);  // key of the tile = TMEM lane
     const int key = j0 + r;
     const uint32_t lane_addr = (quad * 32u) << 16;
-    const float c = p.scale_log2;
+    const uint64_t c2 = f2(p.scale_log2, p.scale_log2);
     const int sw = r & 7;  // 128-byte swizzle of the row's 16-byte chunks
     for (int n = 0; n < N; ++n) {
       const int bf = n & 1;
@@ -275,8 +275,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float* Ds = Ls + BQ;
       uint8_t* ds_row = smem + DS_OFF + bf * DS_BYTES + r * 128;
       const int i0 = j0 + n * BQ;
+      // Every (query, key) of the step inside the window: no element masks. Keys past the
+      // sequence cannot occur then (they would lie after every query).
+      const bool whole = (i0 >= j0 + BKV - 1) && (i0 + BQ - 1 - j0 < p.window) &&
+                         (i0 + BQ - 1 < p.S);
       // two halves of 32 queries: S^T and dP^T in, P^T and dS^T out over them (the halves
-      // already read), the dS row to shared memory
+      // already read), the dS row to shared memory. Pairs of queries in packed fp32 math;
+      // L and D four queries per shared-memory load (the same address in every lane).
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t us[32], ud[32];
@@ -284,20 +289,33 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(t + T_DP + 32 * hf, ud);
         tmem_ld_wait(us);
         tmem_ld_wait_regs(ud);
+        const float4* L4 = reinterpret_cast<const float4*>(Ls + 32 * hf);
+        const float4* D4 = reinterpret_cast<const float4*>(Ds + 32 * hf);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l = L4[e / 4], dd = D4[e / 4];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int qi = 32 * hf + e + h;
-            const int q = i0 + qi, d = q - key;
-            const float pr = ex2_approx(__uint_as_float(us[e + h]) * c - Ls[qi]);
-            pv[h] = (d >= 0 && d < p.window && q < p.S) ? pr : 0.f;  // q's window holds the key
-            dv[h] = pv[h] * (__uint_as_float(ud[e + h]) - Ds[qi]);
+            const int e2 = e + 2 * h;
+            const uint64_t x2 = f2_fma(f2(__uint_as_float(us[e2]), __uint_as_float(us[e2 + 1])),
+                                       c2, h ? f2(-l.z, -l.w) : f2(-l.x, -l.y));
+            float x0, x1;
+            f2_split(x2, x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (!whole) {  // q's window holds the key: 0 <= q - key < w, q < S
+              const int q = i0 + 32 * hf + e2, d = q - key;
+              if (!(d >= 0 && d < p.window && q < p.S)) p0 = 0.f;
+              if (!(d + 1 >= 0 && d + 1 < p.window && q + 1 < p.S)) p1 = 0.f;
+            }
+            const uint64_t p2 = f2(p0, p1);
+            const uint64_t g2 = f2_sub(f2(__uint_as_float(ud[e2]), __uint_as_float(ud[e2 + 1])),
+                                       h ? f2(dd.z, dd.w) : f2(dd.x, dd.y));
+            float s0, s1;
+            f2_split(f2_mul(p2, g2), s0, s1);
+            pk[e2 / 2] = pack_bf16x2(p0, p1);
+            dk[e2 / 2] = pack_bf16x2(s0, s1);
           }
-          pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          dk[e / 2] = pack_bf16x2(dv[0], dv[1]);
         }
         tmem_st16(t + 16 * hf, pk);
         tmem_st16(t + T_DP + 16 * hf, dk);
