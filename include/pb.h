@@ -111,7 +111,7 @@ typedef struct pb_weights {
  *   vt   [batch, heads, dh, seq_pad] v transposed per head, seq_pad = seq rounded up to 8
  *   act  [T, H + F]      [attention output (before Wo) | GeLU(h)]  (bf16 / fp16)
  *   q8, qscale           the FP8 operands of PB_OPERANDS_FP8 (see the fields)
- *   io   [T, H]          bf16 staging of the host-buffer entry point
+ *   io, io2 [T, H]       bf16 staging of the host-buffer entry points
  *   res0, res1 [T, H]    fp32 residual stream between the layers of a stack
  *   sk                   stream-K partial tiles (fp32) and flags of the two GEMMs
  * T = batch * seq, F' = F (GeLU) or 2F (SwiGLU).
@@ -133,6 +133,7 @@ typedef struct pb_scratch_layout {
   size_t vt;
   size_t act;
   size_t io;
+  size_t io2;
   size_t res0;
   size_t res1;
   size_t sk;  /* stream-K partial tiles and flags of the GEMMs */
@@ -277,6 +278,20 @@ pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const voi
  * The caller synchronises the stream before reading y. */
 pb_status pb_forward_stack_host(pb_handle* const* layers, int32_t n_layers, const void* x_host,
                                 void* y_host, void* scratch, size_t scratch_bytes, void* stream);
+
+/* A sequence of n_steps independent passes of the stack over host inputs, the loop of a
+ * resident model serving a stream of batches: step s copies x_host[s] in, runs the stack,
+ * copies y_host[s] out. Two device staging buffers (scratch io and io2) alternate and the
+ * copies run on a copy stream the library creates in layers[0] on first use (released by
+ * pb_destroy), so the input of step s + 1 and the output of step s - 1 move while step s
+ * computes on `stream`. When `stream` reaches the point after this call, every y_host[s]
+ * is written. x_host, y_host: arrays of n_steps host pointers (pinned memory for
+ * asynchronous copies); a y_host[s] may equal an x_host[t] only if t <= s. The handles
+ * must not be used by another host thread meanwhile. */
+pb_status pb_forward_stack_host_steps(pb_handle* const* layers, int32_t n_layers,
+                                      int32_t n_steps, const void* const* x_host,
+                                      void* const* y_host, void* scratch, size_t scratch_bytes,
+                                      void* stream);
 
 /* Reads the handle's device status word (blocks until the word can be read on the
  * handle's device) and returns PB_OK or the first device-side error recorded since

@@ -313,3 +313,22 @@ def test_tiny_wait_limit_keeps_context_usable():
     torch.cuda.synchronize()
     assert block.status() == pb.PB_OK
     assert torch.equal(again, ok)
+
+
+def test_host_steps_match_device_stack():
+    # the pipelined host-buffer entry point gives, step by step, the device path's bits
+    wl = wl_small("steps", 2, 192, 256, 2, 128, 512, 48, layers=2)
+    x, layers = inputs.make_stack(wl, device="cuda")
+    dims = pb.make_dims(wl)
+    blocks = [pb.ParallelBlock(dims, p) for p in layers]
+    scratch = pb.new_scratch(dims)
+    xs = [x, (x * 0.5).to(torch.bfloat16), (x + 1).to(torch.bfloat16)]
+    want = [pb.forward_stack(blocks, xi, scratch=scratch) for xi in xs]
+    torch.cuda.synchronize()
+    for n in (1, 3):
+        xh = [xi.cpu().pin_memory() for xi in xs[:n]]
+        yh = [torch.empty_like(t).pin_memory() for t in xh]
+        pb.forward_stack_host_steps(blocks, xh, yh, scratch)
+        torch.cuda.current_stream().synchronize()
+        for i in range(n):
+            assert torch.equal(yh[i], want[i].cpu()), (n, i)

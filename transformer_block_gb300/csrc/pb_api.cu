@@ -48,6 +48,10 @@ struct pb_handle {
   std::vector<cudaEvent_t> trace;  // 5 events per traced call
   int trace_max;
   int trace_calls;
+  // pb_forward_stack_host_steps (created on first use, in the stack's first handle): the
+  // copy stream and its events (start, input ready x2, compute done x2, output done)
+  cudaStream_t copy_stream;
+  cudaEvent_t copy_ev[6];
 };
 
 namespace {
@@ -174,6 +178,8 @@ pb_scratch_layout scratch_layout(const pb_dims& d) {
   L.act = off;
   off = align_up(off + T * (H + F) * 2, 1024);
   L.io = off;
+  off = align_up(off + T * H * 2, 1024);
+  L.io2 = off;
   off = align_up(off + T * H * 2, 1024);
   L.res0 = off;
   off = align_up(off + T * H * 4, 1024);
@@ -1103,6 +1109,61 @@ pb_status pb_forward_stack_host(pb_handle* const* layers, int32_t n_layers, cons
   return PB_OK;
 }
 
+pb_status pb_forward_stack_host_steps(pb_handle* const* layers, int32_t n_layers,
+                                      int32_t n_steps, const void* const* x_host,
+                                      void* const* y_host, void* scratch, size_t scratch_bytes,
+                                      void* stream) {
+  pb_status s = check_stack(layers, n_layers, scratch, scratch_bytes);
+  if (s != PB_OK) return s;
+  if (n_steps < 1 || x_host == nullptr || y_host == nullptr)
+    return fail(PB_ERR_INVALID_ARG, "need n_steps >= 1 and arrays of host pointers");
+  for (int32_t i = 0; i < n_steps; ++i)
+    if (x_host[i] == nullptr || y_host[i] == nullptr)
+      return fail(PB_ERR_INVALID_ARG, "x_host[%d] or y_host[%d] is NULL", i, i);
+  pb_handle* h0 = layers[0];
+  if (h0->copy_stream == nullptr) {
+    PB_CUDA(cudaStreamCreateWithFlags(&h0->copy_stream, cudaStreamNonBlocking),
+            "cudaStreamCreateWithFlags");
+    for (cudaEvent_t& e : h0->copy_ev)
+      PB_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate");
+  }
+  const pb_dims& d = h0->d;
+  const size_t n = size_t(d.batch) * d.seq * d.hidden * 2;
+  const pb_scratch_layout L = scratch_layout(d);
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  void* io[2] = {sc + L.io, sc + L.io2};
+  cudaStream_t st = static_cast<cudaStream_t>(stream), cs = h0->copy_stream;
+  cudaEvent_t ev_start = h0->copy_ev[0], ev_out = h0->copy_ev[5];
+  cudaEvent_t ev_in[2] = {h0->copy_ev[1], h0->copy_ev[2]};
+  cudaEvent_t ev_done[2] = {h0->copy_ev[3], h0->copy_ev[4]};
+  // The copy stream starts after the work already queued on `stream` (which may use io).
+  // Its order is H2D(0), H2D(1), D2H(0), H2D(2), D2H(1), ...: the input of step s + 1 and
+  // the output of step s - 1 move while step s computes; an io buffer is refilled only
+  // after its previous output has been copied out (the copy stream is in order).
+  PB_CUDA(cudaEventRecord(ev_start, st), "cudaEventRecord");
+  PB_CUDA(cudaStreamWaitEvent(cs, ev_start, 0), "cudaStreamWaitEvent");
+  PB_CUDA(cudaMemcpyAsync(io[0], x_host[0], n, cudaMemcpyHostToDevice, cs), "copy x");
+  PB_CUDA(cudaEventRecord(ev_in[0], cs), "cudaEventRecord");
+  for (int32_t i = 0; i < n_steps; ++i) {
+    const int b = i & 1;
+    PB_CUDA(cudaStreamWaitEvent(st, ev_in[b], 0), "cudaStreamWaitEvent");
+    s = run_stack(layers, n_layers, io[b], io[b], sc, st);
+    if (s != PB_OK) return s;
+    PB_CUDA(cudaEventRecord(ev_done[b], st), "cudaEventRecord");
+    if (i + 1 < n_steps) {
+      PB_CUDA(cudaMemcpyAsync(io[b ^ 1], x_host[i + 1], n, cudaMemcpyHostToDevice, cs),
+              "copy x");
+      PB_CUDA(cudaEventRecord(ev_in[b ^ 1], cs), "cudaEventRecord");
+    }
+    PB_CUDA(cudaStreamWaitEvent(cs, ev_done[b], 0), "cudaStreamWaitEvent");
+    PB_CUDA(cudaMemcpyAsync(y_host[i], io[b], n, cudaMemcpyDeviceToHost, cs), "copy y");
+  }
+  // `stream` reaches the point after this call only when every output is on the host
+  PB_CUDA(cudaEventRecord(ev_out, cs), "cudaEventRecord");
+  PB_CUDA(cudaStreamWaitEvent(st, ev_out, 0), "cudaStreamWaitEvent");
+  return PB_OK;
+}
+
 pb_status pb_get_status(pb_handle* h) {
   pb_status s = check_handle(h);
   if (s != PB_OK) return s;
@@ -1170,6 +1231,11 @@ pb_status pb_destroy(pb_handle* h) {
   if (h == nullptr) return fail(PB_ERR_BAD_HANDLE, "handle is NULL");
   if (h->magic != kMagic) return fail(PB_ERR_BAD_HANDLE, "handle is destroyed or invalid");
   trace_free(h);
+  if (h->copy_stream != nullptr) {
+    cudaStreamSynchronize(h->copy_stream);
+    for (cudaEvent_t e : h->copy_ev) cudaEventDestroy(e);
+    cudaStreamDestroy(h->copy_stream);
+  }
   h->magic = kDead;
   delete h;
   return PB_OK;

@@ -46,7 +46,7 @@ class pb_weights(ctypes.Structure):
 
 class pb_scratch_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("xn", "qk", "vt", "act", "io", "res0", "res1", "sk", "q8", "qscale", "seq_pad",
+                ("xn", "qk", "vt", "act", "io", "io2", "res0", "res1", "sk", "q8", "qscale", "seq_pad",
                  "total", "hpre", "lse", "d_attn", "delta", "dq_acc", "dz", "dxn", "stats",
                  "partials", "train_total")]
 
@@ -91,6 +91,7 @@ SIGNATURES = {
     "pb_quantize_rows_e4m3": (ctypes.c_int, [_I64, _I32, _P, _P, _P, _P]),
     "pb_train_scratch_bytes": (ctypes.c_int, [_P, _P]),
     "pb_forward_train": (ctypes.c_int, [_P, _P, _P, _P, _S, _P]),
+    "pb_forward_stack_host_steps": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _S, _P]),
     "pb_backward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _S, _P]),
     "pb_gemm_scratch_bytes": (ctypes.c_int, [ctypes.POINTER(_S)]),
     "pb_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _S, _P, _P]),
@@ -352,6 +353,19 @@ def forward_stack_host(blocks, x_host, y_host, scratch, stream=None):
            lib().pb_forward_stack_host(_handles(blocks), len(blocks), _ptr(x_host), _ptr(y_host),
                                        _ptr(scratch), scratch.numel(), _stream(stream)))
     return y_host
+
+
+def forward_stack_host_steps(blocks, x_hosts, y_hosts, scratch, stream=None):
+    """Host (pinned) x_hosts[s] -> stack -> y_hosts[s] for every step s, the copies of
+    neighbouring steps overlapping each step's compute (``pb_forward_stack_host_steps``)."""
+    n = len(x_hosts)
+    assert len(y_hosts) == n
+    xs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in x_hosts])
+    ys = (ctypes.c_void_p * n)(*[t.data_ptr() for t in y_hosts])
+    _check("pb_forward_stack_host_steps",
+           lib().pb_forward_stack_host_steps(_handles(blocks), len(blocks), n, xs, ys,
+                                             _ptr(scratch), scratch.numel(), _stream(stream)))
+    return y_hosts
 
 
 def layernorm(x, gamma, beta, eps=1e-5, out=None, stream=None):
