@@ -241,3 +241,41 @@ def test_backward_rejects_unsupported_handles():
             x, scratch)
     with pytest.raises(pb.PbError):  # y must not overwrite x
         pb.ParallelBlock(dims, params).forward_train(x, scratch, y=x)
+
+
+def test_two_layer_training_through_per_layer_calls():
+    # A stack trains through per-layer calls, each layer with its own training scratch:
+    # forward layer by layer, then backward in reverse, layer l's dx the dy of layer l - 1.
+    wl = Workload("bwd-stack2", 2, 130, 256, 2, 128, 512, 48, 2, 0.02)
+    x, layers = inputs.make_stack(wl, device="cuda")
+    dims = pb.make_dims(wl)
+    blocks = [pb.ParallelBlock(dims, p) for p in layers]
+    scr = [pb.new_train_scratch(dims) for _ in blocks]
+    acts = [x]
+    for b, s in zip(blocks, scr):
+        acts.append(b.forward_train(acts[-1], s))
+    g = torch.Generator(device="cuda").manual_seed(5)
+    dy = torch.randn(x.shape, generator=g, device="cuda").to(torch.bfloat16)
+    grads = [None, None]
+    d = dy
+    for i in (1, 0):
+        grads[i] = blocks[i].backward(acts[i], d, scr[i], biases=False)
+        d = grads[i]["dx"]
+    torch.cuda.synchronize()
+    for b in blocks:
+        assert b.status() == pb.PB_OK
+    # the oracle, on its own fp64 activations
+    B, S, H = wl.batch, wl.seq, wl.hidden
+    od = oracle_dims(wl)
+    hp = [host_params(p) for p in layers]
+    xs = [host(x).reshape(B, S, H)]
+    xs.append(O.block_forward(od, xs[0], hp[0]))
+    ref1 = O.block_backward(od, xs[1], hp[1], host(dy).reshape(B, S, H))
+    ref0 = O.block_backward(od, xs[0], hp[0], ref1["dx"])
+    assert_parity(host(grads[0]["dx"]), ref0["dx"].reshape(-1, H), "stack2 dx")
+    for i, ref in ((0, ref0), (1, ref1)):
+        for n, k in (("wqkv", "dwqkv"), ("w1", "dw1"), ("wo", "dwo"), ("w2", "dw2"),
+                     ("ln_gamma", "dgamma")):
+            tol = DS_MEAN_TOL if n in ("wqkv", "ln_gamma") else COMPOUND_MEAN_TOL
+            assert_parity(grads[i][k].cpu().numpy(), ref[n], f"stack2 layer {i} d{n}",
+                          mean_tol=tol)
