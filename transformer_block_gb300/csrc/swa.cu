@@ -23,8 +23,13 @@
 //   warp 1     tensor-memory owner and the single MMA-issuing thread, in the order
 //                S0 = Q0 K_j^T, S1 = Q1 K_j^T, then per tile h: O_h += P_h V_j followed
 //                by S_h = Q_h K_{j+1}^T
-//              so the tensor cores work on one query tile while the other's softmax runs
-//   warps 2-3  idle (they complete the first warpgroup, whose registers go to the softmax)
+//              so the tensor cores work on one query tile while the other's softmax runs;
+//              it waits only for P_h: each mbarrier wait in that thread idles the tensor
+//              pipe for about its latency
+//   warp 2     watcher: waits for the V tile of each step and the next K tile and adds an
+//              arrival to query tile 0's P barrier, so the issuer's wait for P_0 also
+//              covers them
+//   warp 3     idle (warps 0-3 form the warpgroup whose registers go to the softmax)
 //   warps 4-7  softmax of query tile 0, one row per thread (the thread's TMEM lane)
 //   warps 8-11 softmax of query tile 1
 // Tensor memory: S0 | S1 | O0 | O1 (128 columns each). The softmax writes P (bf16) over
@@ -183,7 +188,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(v_full0 + 8 * s, 1);
       mbar_init(v_empty0 + 8 * s, 1);
       mbar_init(s_full0 + 8 * s, 1);
-      mbar_init(p_full0 + 8 * s, 4);
+      // query tile 0: its 4 softmax warps and the watcher (the V and next K tiles landed)
+      mbar_init(p_full0 + 8 * s, s == 0 ? 5 : 4);
       mbar_init(o_final0 + 8 * s, 1);
     }
     mbar_init(drain_bar, 1);
@@ -324,12 +330,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t pv_started = 0;  // bit h: O_h holds this item's partial sum
         for (int idx = 0; ok && idx < it.U; ++idx) {
           const int j = it.kt_begin + idx;
-          const uint32_t gv = vc + uint32_t(idx), gk = kc + uint32_t(idx + 1);
+          const uint32_t gv = vc + uint32_t(idx);
           const uint64_t dv = dV + uint64_t(((gv & 1) * L::V_BYTES) >> 4);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(p_full0 + 8 * h, (tb + uint32_t(idx)) & 1, wc, 13) ||
-                (h == 0 && !mbar_wait(v_full0 + 8 * (gv & 1), (gv >> 1) & 1, wc, 17))) {
+            // P_0's phase also certifies that V tile gv and K tile gk have landed (the
+            // watcher's arrival), so one wait per query tile and key tile suffices.
+            if (!mbar_wait(p_full0 + 8 * h, (tb + uint32_t(idx)) & 1, wc, 13)) {
               ok = false;
               break;
             }
@@ -350,14 +357,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (h == 1) mma_commit(v_empty0 + 8 * (gv & 1));  // both PV products have V
             if (idx + 1 == it.U) mma_commit(o_final0 + 8 * h);  // once per item
-            if (idx + 1 < it.U) {
-              if (h == 0 && !mbar_wait(k_full0 + 8 * (gk % 3), (gk / 3) & 1, wc, 15)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              issue_s(h, idx + 1);
-            }
+            if (idx + 1 < it.U) issue_s(h, idx + 1);
           }
         }
         kc += uint32_t(it.U);
@@ -366,6 +366,40 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       mma_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0, drain_ns);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- watcher
+      // Every mbarrier wait in the MMA-issuing thread idles the tensor pipe for about its
+      // latency, so that thread waits only for P. This thread waits for the V tile of each
+      // step and the K tile of the next one, then adds its arrival to query tile 0's
+      // p_full phase. It waits for that phase to complete before the next step, so it
+      // never arrives in a later phase; a V or K stage cannot be refilled before the
+      // phase completes, because the issuer reads it only afterwards.
+      uint32_t kc = 0, vc = 0, tb = 0;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int r = item_index(n, cta, G);
+        if (r >= num_items) break;
+        const Item it = make_item(p, r);
+        for (int idx = 0; idx < it.U; ++idx) {
+          const uint32_t gv = vc + uint32_t(idx), gk = kc + uint32_t(idx + 1);
+          if (!mbar_wait(v_full0 + 8 * (gv & 1), (gv >> 1) & 1, wc, 17) ||
+              (idx + 1 < it.U && !mbar_wait(k_full0 + 8 * (gk % 3), (gk / 3) & 1, wc, 15))) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(p_full0);
+          if (!mbar_wait(p_full0, (tb + uint32_t(idx)) & 1, wc, 19)) {
+            ok = false;
+            break;
+          }
+        }
+        kc += uint32_t(it.U);
+        vc += uint32_t(it.U);
+        tb += uint32_t(it.U);
+      }
     }
     __syncwarp();
   }
