@@ -69,7 +69,8 @@ def test_gemm_stream_k_matches_oracle(M, N, K):
     assert not torch.equal(c_sk, c_dp)
 
 
-@pytest.mark.parametrize("rows,H", [(37, 256), (5, 2048), (3, 12288), (64, 16384)])
+@pytest.mark.parametrize("rows,H", [(37, 256), (7, 128), (9, 384), (5, 2048), (300, 4096), (3, 12288),
+                                    (64, 16384)])
 def test_layernorm_matches_oracle(rows, H):
     g = torch.Generator(device="cuda").manual_seed(rows + H)
     x = (torch.randn(rows, H, generator=g, device="cuda") * 2 + 0.5).to(torch.bfloat16)

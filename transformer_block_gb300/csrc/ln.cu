@@ -1,7 +1,9 @@
 // ln.cu — LayerNorm of the token rows (the single LN shared by both branches of the
 // parallel block, MegaScale reading notes, section 1.1, eq. (4)).
 //
-// One 256-thread CTA per row. Each thread keeps its share of the row in registers as
+// Rows of up to 4096 bf16 (2048 fp32) elements: one warp per row, 8 rows per CTA, warp
+// shuffles only (layernorm_warp_kernel). Longer rows: one 256-thread CTA per row. Each
+// thread keeps its share of the row in registers as
 // vectors of 8 elements (one 128-bit load of bf16, or two of fp32 for the fp32 residual
 // stream of a stack), so x is read from HBM once; the mean and then the centred
 // variance are reduced across the CTA in fp32 (warp shuffles, then 8 partial sums in
@@ -132,6 +134,117 @@ __global__ void __launch_bounds__(THREADS) layernorm_kernel(const TIn* __restric
   if (F16 && out_of_range && status != nullptr) atomicCAS(status, 0, kStatusRange);
 }
 
+// Rows that fit a warp's registers: one warp per row, 8 rows per CTA, so the mean and the
+// variance need only warp shuffles and each SM keeps many rows' loads in flight. Lane l
+// holds vectors l, l + 32, ... (VPL of them) of 8 elements, as loaded (bf16 stays packed;
+// fp32 as loaded) and converts them on each of the three passes.
+template <typename TIn>
+struct RowVec;
+template <>
+struct RowVec<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* row, int idx) {
+    u = reinterpret_cast<const uint4*>(row)[idx];
+  }
+  // A bf16 is the top half of its fp32 value. The shifts are volatile so that each pass
+  // converts again instead of the compiler keeping all fp32 values live (spills).
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t lo, hi;
+      asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w[e]));
+      asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w[e]));
+      f[2 * e] = __uint_as_float(lo);
+      f[2 * e + 1] = __uint_as_float(hi);
+    }
+  }
+};
+template <>
+struct RowVec<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* row, int idx) {
+    a = reinterpret_cast<const float4*>(row)[2 * idx];
+    b = reinterpret_cast<const float4*>(row)[2 * idx + 1];
+  }
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <typename TIn, bool F16, bool RMS, int VPL>
+__global__ void __launch_bounds__(THREADS, 2) layernorm_warp_kernel(
+    const TIn* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+    const __nv_bfloat16* __restrict__ beta, uint4* __restrict__ out, int64_t rows, int H,
+    float eps, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * (THREADS / 32) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int nv = H / 8;
+  const TIn* xr = x + row * H;
+  RowVec<TIn> v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int idx = lane + 32 * i;
+    if (idx < nv) v[i].load(xr, idx);
+  }
+  float sum = 0.f;
+  if (!RMS) {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (lane + 32 * i < nv) {
+        float f[8];
+        v[i].get(f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum += f[e];
+      }
+    }
+  }
+  const float mean = RMS ? 0.f : warp_sum(sum) / float(H);
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    if (lane + 32 * i < nv) {
+      float f[8];
+      v[i].get(f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sq += (f[e] - mean) * (f[e] - mean);
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(sq) / float(H) + eps);
+  uint4* orow = out + row * nv;
+  bool out_of_range = false;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int idx = lane + 32 * i;
+    if (idx < nv) {
+      float f[8], g[8], b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, o[8];
+      v[i].get(f);
+      load8(gamma, idx, g);
+      if (!RMS) load8(beta, idx, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+        if (F16) out_of_range |= !(fabsf(o[e]) <= kF16Max);
+      }
+      uint4 u;
+      u.x = pack2<F16>(o[0], o[1]);
+      u.y = pack2<F16>(o[2], o[3]);
+      u.z = pack2<F16>(o[4], o[5]);
+      u.w = pack2<F16>(o[6], o[7]);
+      orow[idx] = u;
+    }
+  }
+  if (F16 && out_of_range && status != nullptr) atomicCAS(status, 0, kStatusRange);
+}
+
 // LayerNorm / RMSNorm straight to FP8 E4M3 (the FP8 GEMM operand): the normalised row is
 // computed in fp32 as above, its largest magnitude reduced across the CTA, and each value
 // written as E4M3(o * 448 / amax), the row's scale amax / 448 to scales[row] (per-row
@@ -194,10 +307,38 @@ __global__ void __launch_bounds__(THREADS) layernorm_e4m3_kernel(
   }
 }
 
+template <typename TIn, bool F16, int VPL>
+cudaError_t launch_warp(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
+                        const __nv_bfloat16* beta, float eps, void* out, int* status,
+                        cudaStream_t stream) {
+  const int64_t grid = (rows + THREADS / 32 - 1) / (THREADS / 32);
+  if (beta == nullptr)
+    layernorm_warp_kernel<TIn, F16, true, VPL><<<unsigned(grid), THREADS, 0, stream>>>(
+        static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), rows, H, eps, status);
+  else
+    layernorm_warp_kernel<TIn, F16, false, VPL><<<unsigned(grid), THREADS, 0, stream>>>(
+        static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), rows, H, eps, status);
+  return cudaGetLastError();
+}
+
+// Vectors of 8 per lane a warp-per-row launch may hold: 16 packed bf16 vectors (64
+// registers, H <= 4096) or 8 fp32 vectors (H <= 2048).
+template <typename TIn>
+constexpr int kWarpRowMaxVpl = sizeof(TIn) == 2 ? 16 : 8;
+
 template <typename TIn, bool F16>
 cudaError_t launch_t(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
                      const __nv_bfloat16* beta, float eps, void* out, int* status,
                      cudaStream_t stream) {
+  const int vpl = (H / 8 + 31) / 32;
+  if (vpl <= kWarpRowMaxVpl<TIn>) {
+    if (vpl <= 1) return launch_warp<TIn, F16, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if (vpl <= 2) return launch_warp<TIn, F16, 2>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if (vpl <= 4) return launch_warp<TIn, F16, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if (vpl <= 8) return launch_warp<TIn, F16, 8>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if constexpr (kWarpRowMaxVpl<TIn> >= 16)
+      return launch_warp<TIn, F16, 16>(rows, H, x, gamma, beta, eps, out, status, stream);
+  }
   if (beta == nullptr)
     layernorm_kernel<TIn, F16, true><<<unsigned(rows), THREADS, 0, stream>>>(
         static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), H, eps, status);
