@@ -2,7 +2,8 @@
 // parallel block, MegaScale reading notes, section 1.1, eq. (4)).
 //
 // Rows of up to 4096 bf16 (2048 fp32) elements: one warp per row, 8 rows per CTA, warp
-// shuffles only (layernorm_warp_kernel). Longer rows: one 256-thread CTA per row. Each
+// shuffles only; up to 16384 bf16 (8192 fp32): four warps per row, 2 rows per CTA
+// (layernorm_rows_kernel). Longer fp32 rows: one 256-thread CTA per row. Each
 // thread keeps its share of the row in registers as
 // vectors of 8 elements (one 128-bit load of bf16, or two of fp32 for the fp32 residual
 // stream of a stack), so x is read from HBM once; the mean and then the centred
@@ -134,10 +135,11 @@ __global__ void __launch_bounds__(THREADS) layernorm_kernel(const TIn* __restric
   if (F16 && out_of_range && status != nullptr) atomicCAS(status, 0, kStatusRange);
 }
 
-// Rows that fit a warp's registers: one warp per row, 8 rows per CTA, so the mean and the
-// variance need only warp shuffles and each SM keeps many rows' loads in flight. Lane l
-// holds vectors l, l + 32, ... (VPL of them) of 8 elements, as loaded (bf16 stays packed;
-// fp32 as loaded) and converts them on each of the three passes.
+// Rows that fit the registers of one or four warps: the mean and the variance need only
+// warp shuffles (and, for four warps, one exchange through shared memory), and each SM
+// keeps many rows' loads in flight. Thread t of a row holds vectors t, t + 32 WPR, ...
+// (VPL of them) of 8 elements as loaded (bf16 stays packed) and converts them on each of
+// the three passes.
 template <typename TIn>
 struct RowVec;
 template <>
@@ -179,27 +181,48 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <typename TIn, bool F16, bool RMS, int VPL>
-__global__ void __launch_bounds__(THREADS, 2) layernorm_warp_kernel(
+// Sum over the WPR warps of one row: warp shuffles, then (WPR > 1) the warps' partial sums
+// through shared memory behind the row's own named barrier. `slot` separates the two
+// reductions of a row, so no slot is written twice.
+template <int WPR>
+__device__ __forceinline__ float row_sum(float v, float* red, int slot) {
+  v = warp_sum(v);
+  if (WPR == 1) return v;
+  const int warp = threadIdx.x >> 5, grp = warp / WPR;
+  if ((threadIdx.x & 31) == 0) red[slot * (THREADS / 32) + warp] = v;
+  named_barrier(1 + grp, 32 * WPR);
+  float s = 0.f;
+#pragma unroll
+  for (int w = 0; w < WPR; ++w) s += red[slot * (THREADS / 32) + grp * WPR + w];
+  return s;
+}
+
+// WPR warps per row (1 or 4), THREADS / (32 WPR) rows per CTA. Every thread of a row's
+// warps takes the same branches around the named barriers (the early exit depends only on
+// the row).
+template <typename TIn, bool F16, bool RMS, int VPL, int WPR>
+__global__ void __launch_bounds__(THREADS, 2) layernorm_rows_kernel(
     const TIn* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
     const __nv_bfloat16* __restrict__ beta, uint4* __restrict__ out, int64_t rows, int H,
     float eps, int* status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * (THREADS / 32) + (threadIdx.x >> 5);
+  __shared__ float red[2 * (THREADS / 32)];
+  constexpr int RT = 32 * WPR;  // threads per row
+  const int t = int(threadIdx.x) % RT;
+  const int64_t row = int64_t(blockIdx.x) * (THREADS / RT) + int(threadIdx.x) / RT;
   if (row >= rows) return;
   const int nv = H / 8;
   const TIn* xr = x + row * H;
   RowVec<TIn> v[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    const int idx = lane + 32 * i;
+    const int idx = t + RT * i;
     if (idx < nv) v[i].load(xr, idx);
   }
   float sum = 0.f;
   if (!RMS) {
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      if (lane + 32 * i < nv) {
+      if (t + RT * i < nv) {
         float f[8];
         v[i].get(f);
 #pragma unroll
@@ -207,23 +230,23 @@ __global__ void __launch_bounds__(THREADS, 2) layernorm_warp_kernel(
       }
     }
   }
-  const float mean = RMS ? 0.f : warp_sum(sum) / float(H);
+  const float mean = RMS ? 0.f : row_sum<WPR>(sum, red, 0) / float(H);
   float sq = 0.f;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    if (lane + 32 * i < nv) {
+    if (t + RT * i < nv) {
       float f[8];
       v[i].get(f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) sq += (f[e] - mean) * (f[e] - mean);
     }
   }
-  const float rstd = rsqrtf(warp_sum(sq) / float(H) + eps);
+  const float rstd = rsqrtf(row_sum<WPR>(sq, red, 1) / float(H) + eps);
   uint4* orow = out + row * nv;
   bool out_of_range = false;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    const int idx = lane + 32 * i;
+    const int idx = t + RT * i;
     if (idx < nv) {
       float f[8], g[8], b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, o[8];
       v[i].get(f);
@@ -307,37 +330,45 @@ __global__ void __launch_bounds__(THREADS) layernorm_e4m3_kernel(
   }
 }
 
-template <typename TIn, bool F16, int VPL>
-cudaError_t launch_warp(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
+template <typename TIn, bool F16, int VPL, int WPR>
+cudaError_t launch_rows(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
                         const __nv_bfloat16* beta, float eps, void* out, int* status,
                         cudaStream_t stream) {
-  const int64_t grid = (rows + THREADS / 32 - 1) / (THREADS / 32);
+  constexpr int RPC = THREADS / (32 * WPR);  // rows per CTA
+  const int64_t grid = (rows + RPC - 1) / RPC;
   if (beta == nullptr)
-    layernorm_warp_kernel<TIn, F16, true, VPL><<<unsigned(grid), THREADS, 0, stream>>>(
+    layernorm_rows_kernel<TIn, F16, true, VPL, WPR><<<unsigned(grid), THREADS, 0, stream>>>(
         static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), rows, H, eps, status);
   else
-    layernorm_warp_kernel<TIn, F16, false, VPL><<<unsigned(grid), THREADS, 0, stream>>>(
+    layernorm_rows_kernel<TIn, F16, false, VPL, WPR><<<unsigned(grid), THREADS, 0, stream>>>(
         static_cast<const TIn*>(x), gamma, beta, static_cast<uint4*>(out), rows, H, eps, status);
   return cudaGetLastError();
 }
 
-// Vectors of 8 per lane a warp-per-row launch may hold: 16 packed bf16 vectors (64
-// registers, H <= 4096) or 8 fp32 vectors (H <= 2048).
+// Vectors of 8 elements a thread of layernorm_rows_kernel may hold: 16 packed bf16 vectors
+// (64 registers) or 8 fp32 vectors; so one warp covers rows up to 4096 bf16 / 2048 fp32
+// elements and four warps up to 16384 / 8192.
 template <typename TIn>
-constexpr int kWarpRowMaxVpl = sizeof(TIn) == 2 ? 16 : 8;
+constexpr int kRowMaxVpl = sizeof(TIn) == 2 ? 16 : 8;
 
 template <typename TIn, bool F16>
 cudaError_t launch_t(int64_t rows, int H, const void* x, const __nv_bfloat16* gamma,
                      const __nv_bfloat16* beta, float eps, void* out, int* status,
                      cudaStream_t stream) {
-  const int vpl = (H / 8 + 31) / 32;
-  if (vpl <= kWarpRowMaxVpl<TIn>) {
-    if (vpl <= 1) return launch_warp<TIn, F16, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
-    if (vpl <= 2) return launch_warp<TIn, F16, 2>(rows, H, x, gamma, beta, eps, out, status, stream);
-    if (vpl <= 4) return launch_warp<TIn, F16, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
-    if (vpl <= 8) return launch_warp<TIn, F16, 8>(rows, H, x, gamma, beta, eps, out, status, stream);
-    if constexpr (kWarpRowMaxVpl<TIn> >= 16)
-      return launch_warp<TIn, F16, 16>(rows, H, x, gamma, beta, eps, out, status, stream);
+  const int nv = H / 8;
+  const int vpl1 = (nv + 31) / 32, vpl4 = (nv + 127) / 128;
+  if (vpl1 <= kRowMaxVpl<TIn>) {
+    if (vpl1 <= 1) return launch_rows<TIn, F16, 1, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if (vpl1 <= 2) return launch_rows<TIn, F16, 2, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if (vpl1 <= 4) return launch_rows<TIn, F16, 4, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if (vpl1 <= 8) return launch_rows<TIn, F16, 8, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if constexpr (kRowMaxVpl<TIn> >= 16)
+      return launch_rows<TIn, F16, 16, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
+  }
+  if (vpl4 <= kRowMaxVpl<TIn>) {
+    if (vpl4 <= 8) return launch_rows<TIn, F16, 8, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if constexpr (kRowMaxVpl<TIn> >= 16)
+      return launch_rows<TIn, F16, 16, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
   }
   if (beta == nullptr)
     layernorm_kernel<TIn, F16, true><<<unsigned(rows), THREADS, 0, stream>>>(
