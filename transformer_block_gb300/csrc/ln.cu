@@ -1,15 +1,18 @@
 // ln.cu — LayerNorm of the token rows (the single LN shared by both branches of the
 // parallel block, MegaScale reading notes, section 1.1, eq. (4)).
 //
-// Rows of up to 4096 bf16 (2048 fp32) elements: one warp per row, 8 rows per CTA, warp
-// shuffles only; up to 16384 bf16 (8192 fp32): four warps per row, 2 rows per CTA
-// (layernorm_rows_kernel). Longer fp32 rows: one 256-thread CTA per row. Each
-// thread keeps its share of the row in registers as
-// vectors of 8 elements (one 128-bit load of bf16, or two of fp32 for the fp32 residual
-// stream of a stack), so x is read from HBM once; the mean and then the centred
-// variance are reduced across the CTA in fp32 (warp shuffles, then 8 partial sums in
-// shared memory); the normalised, affine-mapped row is written back as bf16 or fp16
-// (round to nearest even). HBM-bound: one read and one write of the row.
+// Each thread keeps its share of the row in registers as vectors of 8 elements (one
+// 128-bit load of bf16, or two of fp32 for the fp32 residual stream of a stack), so x is
+// read from HBM once. The mean and then the centred variance are reduced in fp32, and the
+// normalised, affine-mapped row is written back as bf16 or fp16 (round to nearest even).
+// HBM-bound: one read and one write of the row. Three shapes of work:
+//   * rows up to 4096 bf16 (2048 fp32) elements: one warp per row, 8 rows per CTA,
+//     reductions by warp shuffles only (layernorm_rows_kernel, 1 warp per row);
+//   * up to 16384 bf16 (8192 fp32): four warps per row, 2 rows per CTA, the warps' partial
+//     sums through shared memory (layernorm_rows_kernel, 4 warps per row);
+//   * longer fp32 rows: one 256-thread CTA per row, CTA-wide reductions
+//     (layernorm_kernel). The FP8 variant (layernorm_e4m3_kernel) uses this shape for all
+//     rows.
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -19,7 +22,8 @@ namespace pb {
 namespace {
 
 constexpr int THREADS = 256;
-constexpr int MAXV = kLnMaxH / (8 * THREADS);  // 8 vectors of 8 elements per thread
+// vectors of 8 elements per thread in the one-CTA-per-row kernels (rows up to kLnMaxH)
+constexpr int MAXV = kLnMaxH / (8 * THREADS);
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
