@@ -92,52 +92,57 @@ __device__ __forceinline__ void store_f32(float* dst, const float* v, bool accum
   }
 }
 
+// 32 bytes from one lane in one instruction; p must be 32-byte aligned. A warp's row-wise
+// stores touch 32 rows per instruction, and each instruction costs the L1 data path (shared
+// with the TMA writes and the MMAs' operand reads of the main loop) about one pass per row
+// it touches, so halving the instructions per row halves that cost.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// N consecutive 16-bit values (N a multiple of 8) from one lane: 32-byte stores where dst
+// is 32-byte aligned, else 16-byte stores.
+template <int N>
+__device__ __forceinline__ void store_words16(void* dst, const uint32_t (&w)[N / 2]) {
+  if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0 && N % 16 == 0) {
+#pragma unroll
+    for (int q = 0; q < N / 16; ++q) st_global_v8(static_cast<char*>(dst) + 32 * q, w + 8 * q);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < N / 8; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
 template <bool F16>
 __device__ __forceinline__ void store_row32(void* dst, const float (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  uint32_t w[16];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 u;
-    if (F16) {
-      u.x = pack_f16x2(v[8 * q + 0], v[8 * q + 1]);
-      u.y = pack_f16x2(v[8 * q + 2], v[8 * q + 3]);
-      u.z = pack_f16x2(v[8 * q + 4], v[8 * q + 5]);
-      u.w = pack_f16x2(v[8 * q + 6], v[8 * q + 7]);
-    } else {
-      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    }
-    d[q] = u;
-  }
+  for (int e = 0; e < 16; ++e)
+    w[e] = F16 ? pack_f16x2(v[2 * e], v[2 * e + 1]) : pack_bf16x2(v[2 * e], v[2 * e + 1]);
+  store_words16<32>(dst, w);
 }
 
 template <bool F16>
 __device__ __forceinline__ void store_row16(void* dst, const float (&v)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  uint32_t w[8];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    uint4 u;
-    if (F16) {
-      u.x = pack_f16x2(v[8 * q + 0], v[8 * q + 1]);
-      u.y = pack_f16x2(v[8 * q + 2], v[8 * q + 3]);
-      u.z = pack_f16x2(v[8 * q + 4], v[8 * q + 5]);
-      u.w = pack_f16x2(v[8 * q + 6], v[8 * q + 7]);
-    } else {
-      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    }
-    d[q] = u;
-  }
+  for (int e = 0; e < 8; ++e)
+    w[e] = F16 ? pack_f16x2(v[2 * e], v[2 * e + 1]) : pack_bf16x2(v[2 * e], v[2 * e + 1]);
+  store_words16<16>(dst, w);
 }
 
 __device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]) {
-  float4* d = reinterpret_cast<float4*>(dst);
+  if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    for (int q = 0; q < 4; ++q) st_global_v8(dst + 8 * q, reinterpret_cast<const uint32_t*>(v + 8 * q));
+  } else {
+    float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
 }
 
 // Epilogue of 32 consecutive columns [col0, col0 + 32) of one output row.
