@@ -145,9 +145,89 @@ __device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]
   }
 }
 
-// Epilogue of 32 consecutive columns [col0, col0 + 32) of one output row.
+// Transposes 16-byte pieces inside each group of 4 lanes: lane 4g + k, holding pieces
+// 0..3 of row 4g + k in w (4 words each), ends up holding piece k of row 4g + i as piece i.
+// Two exchange rounds: the off-diagonal 2 x 2 blocks of pieces with lane ^ 2, then the
+// off-diagonal pieces inside each block with lane ^ 1.
+__device__ __forceinline__ void transpose_pieces4(uint32_t (&w)[16]) {
+  const int k = int(threadIdx.x & 3);
+  const bool hi = (k & 2) != 0, odd = (k & 1) != 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t y = __shfl_xor_sync(0xffffffffu, hi ? w[4 * s + e] : w[4 * (2 + s) + e], 2);
+      if (hi)
+        w[4 * s + e] = y;
+      else
+        w[4 * (2 + s) + e] = y;
+    }
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t y =
+          __shfl_xor_sync(0xffffffffu, odd ? w[4 * (2 * c) + e] : w[4 * (2 * c + 1) + e], 1);
+      if (odd)
+        w[4 * (2 * c) + e] = y;
+      else
+        w[4 * (2 * c + 1) + e] = y;
+    }
+}
+
+// Warp-wide: the warp's 32 x 32 block of 16-bit values (lane l holds row l's 32 values as
+// 16 words) to rows [0, nrows) at base (row stride ld_bytes). After the transpose each
+// store instruction writes 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes:
+// a quarter of the L1 data-path passes, which the main loop's TMA writes and operand
+// reads share.
+__device__ __forceinline__ void store_rows32_16b(char* base, int64_t ld_bytes, int nrows,
+                                                 uint32_t (&w)[16]) {
+  transpose_pieces4(w);
+  const int lane = int(threadIdx.x & 31), k = lane & 3, g = lane >> 2;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * g + i;
+    if (r < nrows)
+      *reinterpret_cast<uint4*>(base + r * ld_bytes + 16 * k) =
+          make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+
+template <bool F16>
+__device__ __forceinline__ void pack_words16(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    w[e] = F16 ? pack_f16x2(v[2 * e], v[2 * e + 1]) : pack_bf16x2(v[2 * e], v[2 * e + 1]);
+}
+
+// Epilogue of 32 consecutive columns [col0, col0 + 32) of one output row. Called by all 32
+// lanes of a warp together, lane l holding row `row` = the warp's first row + l: the plain
+// store is warp-wide (the fused epilogues store row-wise per lane, where the transpose's
+// extra instructions cost more than its fewer store passes save).
 template <int KIND>
 __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col0, float (&v)[32]) {
+  if (KIND == kEpiStore) {
+    const int row0 = row - int(threadIdx.x & 31);
+    const int nrows = ep.M - row0 < 32 ? ep.M - row0 : 32;
+    if (nrows <= 0) return;
+    if (ep.scale_a != nullptr) {  // FP8 operands: undo the row and channel scales
+      const float sa = row < ep.M ? ep.scale_a[row] : 0.f;
+      const float4* s4 = reinterpret_cast<const float4*>(ep.scale_b + col0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 sb = __ldg(s4 + q);
+        v[4 * q + 0] *= sa * sb.x;
+        v[4 * q + 1] *= sa * sb.y;
+        v[4 * q + 2] *= sa * sb.z;
+        v[4 * q + 3] *= sa * sb.w;
+      }
+    }
+    uint32_t w[16];
+    pack_words16<false>(v, w);
+    store_rows32_16b(reinterpret_cast<char*>(ep.c + int64_t(row0) * ep.ldc + col0),
+                     int64_t(ep.ldc) * 2, nrows, w);
+    return;
+  }
   if (row >= ep.M) return;
   if (ep.scale_a != nullptr) {  // FP8 operands: undo the row and channel scales
     const float sa = ep.scale_a[row];
@@ -172,9 +252,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
       v[4 * q + 3] += b.w;
     }
   }
-  if (KIND == kEpiStore) {
-    store_row32<false>(ep.c + int64_t(row) * ep.ldc + col0, v);
-  } else if (KIND == kEpiBlockIn) {
+  if (KIND == kEpiBlockIn) {
     const int H = ep.H;
     const int cc = col0 + ep.col_base;  // column of [q | k | v | h]
     if (cc < 2 * H) {  // q | k
