@@ -92,6 +92,11 @@ BWD = [
     wl_b("bwd-b1-s1", 1, 1, 256, 2, 128, 512, 4),
     wl_b("bwd-glu-b2-s130-w64", 2, 130, 256, 2, 128, 512, 64, variant=1),
     wl_b("bwd-glu-b1-s200-w200", 1, 200, 256, 2, 128, 768, 200, variant=1),
+    # rows wider than 4096: the normalisation backward's four-warps-per-row kernel, with
+    # a ragged last vector per thread (528 vectors of 8 over 128 threads); weights at the
+    # scale of the wide workloads (std 0.006), so each branch stays below x as there
+    Workload("bwd-b1-s64-h4224", 1, 64, 4224, 33, 128, 256, 64, 1, 0.006),
+    Workload("bwd-glu-b1-s64-h4224", 1, 64, 4224, 33, 128, 256, 64, 1, 0.006, variant=1),
 ]
 
 

@@ -16,7 +16,6 @@ namespace pb {
 namespace {
 
 constexpr int THREADS = 256;
-constexpr int MAXV = kLnMaxH / (8 * THREADS);  // vectors of 8 per thread and row
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -27,19 +26,6 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
     f[2 * e] = v.x;
     f[2 * e + 1] = v.y;
   }
-}
-
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float s = 0.f;
-#pragma unroll
-  for (int w = 0; w < THREADS / 32; ++w) s += red[w];
-  __syncthreads();
-  return s;
 }
 
 // One warp per (token, head): dh / 32 consecutive elements per lane.
@@ -83,75 +69,150 @@ __global__ void dq_to_bf16_kernel(const float* __restrict__ dq, int64_t T, int H
   }
 }
 
-// One CTA per row. The statistics follow the forward kernel: fp32, two passes.
-template <bool RMS>
-__global__ void __launch_bounds__(THREADS) norm_bwd_kernel(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
-    const float* __restrict__ dxn, const __nv_bfloat16* __restrict__ dy, int H, float eps,
-    __nv_bfloat16* __restrict__ dx, float2* __restrict__ stats) {
-  __shared__ float red[THREADS / 32];
-  const int64_t row = blockIdx.x;
-  const int nv = H / 8;
-  const __nv_bfloat16* xr = x + row * H;
-  float v[MAXV][8];
-  float sum = 0.f;
+// A bf16 is the top half of its fp32 value. The shifts are volatile so that each pass
+// converts the packed row again instead of the compiler keeping all fp32 values live.
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
-    if (idx < nv) {
-      load8(xr + idx * 8, v[i]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum += v[i][e];
-    }
+  for (int e = 0; e < 4; ++e) {
+    uint32_t lo, hi;
+    asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w[e]));
+    asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w[e]));
+    f[2 * e] = __uint_as_float(lo);
+    f[2 * e + 1] = __uint_as_float(hi);
   }
-  const float mu = RMS ? 0.f : block_sum(sum, red) / float(H);
+}
+
+// Sum over the WPR warps of one row: warp shuffles, then (WPR > 1) the warps' partial sums
+// through shared memory behind the row's own named barrier; `slot` keeps the four
+// reductions of a row apart, so no slot is written twice.
+template <int WPR>
+__device__ __forceinline__ float row_sum(float v, float* red, int slot) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (WPR == 1) return v;
+  const int warp = threadIdx.x >> 5, grp = warp / WPR;
+  if ((threadIdx.x & 31) == 0) red[slot * (THREADS / 32) + warp] = v;
+  named_barrier(1 + grp, 32 * WPR);
+  float s = 0.f;
+#pragma unroll
+  for (int w = 0; w < WPR; ++w) s += red[slot * (THREADS / 32) + grp * WPR + w];
+  return s;
+}
+
+// WPR warps per row (1 or 4), THREADS / (32 WPR) rows per CTA; thread t of a row holds
+// the row's x vectors t, t + 32 WPR, ... packed in registers and reads dxn, gamma and dy
+// in the passes that need them (dxn twice: the second read hits in cache). The
+// statistics follow the forward kernel: fp32, two passes. Every thread of a row's warps
+// takes the same branches around the named barriers.
+template <bool RMS, int VPL, int WPR>
+__global__ void __launch_bounds__(THREADS, 2) norm_bwd_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+    const float* __restrict__ dxn, const __nv_bfloat16* __restrict__ dy, int64_t T, int H,
+    float eps, __nv_bfloat16* __restrict__ dx, float2* __restrict__ stats) {
+  __shared__ float red[4 * (THREADS / 32)];
+  constexpr int RT = 32 * WPR;  // threads per row
+  const int t = int(threadIdx.x) % RT;
+  const int64_t row = int64_t(blockIdx.x) * (THREADS / RT) + int(threadIdx.x) / RT;
+  if (row >= T) return;
+  const int nv = H / 8;
+  uint4 xv[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int idx = t + RT * i;
+    if (idx < nv) xv[i] = *reinterpret_cast<const uint4*>(x + row * H + idx * 8);
+  }
+  float sum = 0.f;
+  if (!RMS) {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (t + RT * i < nv) {
+        float f[8];
+        unpack8(xv[i], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum += f[e];
+      }
+  }
+  const float mu = RMS ? 0.f : row_sum<WPR>(sum, red, 0) / float(H);
   float sq = 0.f;
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
-    if (idx < nv) {
+  for (int i = 0; i < VPL; ++i)
+    if (t + RT * i < nv) {
+      float f[8];
+      unpack8(xv[i], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sq += (v[i][e] - mu) * (v[i][e] - mu);
+      for (int e = 0; e < 8; ++e) sq += (f[e] - mu) * (f[e] - mu);
     }
-  }
-  const float rstd = rsqrtf(block_sum(sq, red) / float(H) + eps);
-  // v becomes xhat; g = dxn * gamma
-  float g[MAXV][8];
+  const float rstd = rsqrtf(row_sum<WPR>(sq, red, 1) / float(H) + eps);
+  // g = dxn * gamma; sums of g and of g * xhat
   float sg = 0.f, sgx = 0.f;
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
+  for (int i = 0; i < VPL; ++i) {
+    const int idx = t + RT * i;
     if (idx < nv) {
-      float gm[8];
+      float f[8], gm[8];
+      unpack8(xv[i], f);
       load8(gamma + idx * 8, gm);
       const float4 d0 = *reinterpret_cast<const float4*>(dxn + row * H + idx * 8);
       const float4 d1 = *reinterpret_cast<const float4*>(dxn + row * H + idx * 8 + 4);
       const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        v[i][e] = (v[i][e] - mu) * rstd;
-        g[i][e] = d[e] * gm[e];
-        sg += g[i][e];
-        sgx += g[i][e] * v[i][e];
+        const float g = d[e] * gm[e];
+        sg += g;
+        sgx += g * (f[e] - mu) * rstd;
       }
     }
   }
-  const float mean_g = RMS ? 0.f : block_sum(sg, red) / float(H);
-  const float mean_gx = block_sum(sgx, red) / float(H);
+  const float mean_g = RMS ? 0.f : row_sum<WPR>(sg, red, 2) / float(H);
+  const float mean_gx = row_sum<WPR>(sgx, red, 3) / float(H);
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
+  for (int i = 0; i < VPL; ++i) {
+    const int idx = t + RT * i;
     if (idx < nv) {
-      float r[8];
+      float f[8], gm[8], r[8];
+      unpack8(xv[i], f);
+      load8(gamma + idx * 8, gm);
       load8(dy + row * H + idx * 8, r);
+      const float4 d0 = *reinterpret_cast<const float4*>(dxn + row * H + idx * 8);
+      const float4 d1 = *reinterpret_cast<const float4*>(dxn + row * H + idx * 8 + 4);
+      const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r[e] += rstd * (g[i][e] - mean_g - v[i][e] * mean_gx);
+      for (int e = 0; e < 8; ++e)
+        r[e] += rstd * (d[e] * gm[e] - mean_g - (f[e] - mu) * rstd * mean_gx);
       *reinterpret_cast<uint4*>(dx + row * H + idx * 8) =
           make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]),
                      pack_bf16x2(r[6], r[7]));
     }
   }
-  if (threadIdx.x == 0) stats[row] = make_float2(mu, rstd);
+  if (t == 0) stats[row] = make_float2(mu, rstd);
+}
+
+template <bool RMS, int VPL, int WPR>
+void launch_norm_rows(int64_t T, int H, const __nv_bfloat16* x, const __nv_bfloat16* gamma,
+                      const float* dxn, const __nv_bfloat16* dy, float eps, __nv_bfloat16* dx,
+                      float2* stats, cudaStream_t stream) {
+  constexpr int RPC = THREADS / (32 * WPR);  // rows per CTA
+  const int64_t grid = (T + RPC - 1) / RPC;
+  norm_bwd_kernel<RMS, VPL, WPR><<<unsigned(grid), THREADS, 0, stream>>>(x, gamma, dxn, dy, T,
+                                                                          H, eps, dx, stats);
+}
+
+template <bool RMS>
+void launch_norm_bwd_t(int64_t T, int H, const __nv_bfloat16* x, const __nv_bfloat16* gamma,
+                       const float* dxn, const __nv_bfloat16* dy, float eps,
+                       __nv_bfloat16* dx, float2* stats, cudaStream_t stream) {
+  // one warp per row up to 4096 elements (16 packed vectors per lane), else four warps
+  // (up to 16384 = kLnMaxH)
+  const int nv = H / 8;
+  const int vpl1 = (nv + 31) / 32, vpl4 = (nv + 127) / 128;
+  if (vpl1 <= 1) return launch_norm_rows<RMS, 1, 1>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
+  if (vpl1 <= 2) return launch_norm_rows<RMS, 2, 1>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
+  if (vpl1 <= 4) return launch_norm_rows<RMS, 4, 1>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
+  if (vpl1 <= 8) return launch_norm_rows<RMS, 8, 1>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
+  if (vpl1 <= 16) return launch_norm_rows<RMS, 16, 1>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
+  if (vpl4 <= 8) return launch_norm_rows<RMS, 8, 4>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
+  return launch_norm_rows<RMS, 16, 4>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
 }
 
 // Partial column sums over row block blockIdx.y: one column per thread (coalesced rows).
@@ -251,11 +312,9 @@ cudaError_t launch_norm_bwd(int64_t T, int H, const __nv_bfloat16* x,
   if (T <= 0) return cudaSuccess;
   if (H <= 0 || H % 8 != 0 || H > kLnMaxH || T > 0x7fffffff) return cudaErrorInvalidValue;
   if (rms)
-    norm_bwd_kernel<true><<<unsigned(T), THREADS, 0, stream>>>(x, gamma, dxn, dy, H, eps, dx,
-                                                               stats);
+    launch_norm_bwd_t<true>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
   else
-    norm_bwd_kernel<false><<<unsigned(T), THREADS, 0, stream>>>(x, gamma, dxn, dy, H, eps, dx,
-                                                                stats);
+    launch_norm_bwd_t<false>(T, H, x, gamma, dxn, dy, eps, dx, stats, stream);
   return cudaGetLastError();
 }
 
