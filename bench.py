@@ -35,8 +35,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "parallel-block fwd TFLOP/s and MFU vs GB300 dense BF16 peak (1 GPU)"
 UNIT = "TFLOP/s"
-# GB300 dense bf16 tensor-core peak, nominal (no sparsity), for MFU.
+# GB300 dense bf16 tensor-core peak for MFU, two ways:
+# * nominal: NVIDIA's HGX B300 figure of 36 PFLOP/s FP16/BF16 tensor for 8 GPUs is quoted
+#   with 2:4 sparsity; dense is half of it, 2.25 PFLOP/s per GPU;
+# * from the clock: SMs x dense bf16 FLOP per clock per SM x the maximum SM clock. A
+#   tcgen05 pair MMA of 256 x 256 x 16 (2.1 MFLOP) retires every 64 cycles on two SMs in
+#   this library's issue probes: 8192 FLOP per clock per SM. With 152 SMs at 2070 MHz that
+#   is 2577.6 TFLOP/s, above the nominal figure (which corresponds to about 1.81 GHz).
 SPEC_BF16_TFLOPS = 2250.0
+SPEC_SOURCE = "NVIDIA HGX B300: 36 PFLOP/s FP16/BF16 for 8 GPUs with 2:4 sparsity -> /2 dense, /8"
+BF16_FLOP_PER_CLK_PER_SM = 8192
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS = ["layernorm", "gemm_block_in", "swa_attention", "gemm_residual"]
 
@@ -62,6 +70,9 @@ def parse():
                          "current scaling, not the reference precision)")
     ap.add_argument("--cpu-rows", type=int, default=192,
                     help="tokens of the oracle's CPU-baseline sample")
+    ap.add_argument("--sustained-s", type=float, default=2.5,
+                    help="length of the second, sustained timed region in seconds (0: skip); "
+                         "it reports the same metric once the power cap has set the clocks")
     return ap.parse_args()
 
 
@@ -222,6 +233,21 @@ def aggregate_timing(ms_local: float, world: int, model_flops: int, steps: int, 
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     return ms, world * model_flops * steps / (ms / 1e3) / 1e12
+
+
+def mfu_of(tflops_per_gpu: float, peaks: dict, clk: dict, sms: int) -> dict:
+    """MFU against the nominal dense bf16 peak, the clock-derived peak (SMs x FLOP per clock
+    per SM x the maximum SM clock) and the measured cuBLAS burst."""
+    max_mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+    derived = sms * BF16_FLOP_PER_CLK_PER_SM * max_mhz * 1e6 / 1e12
+    return {"vs_spec_dense_bf16": tflops_per_gpu / SPEC_BF16_TFLOPS,
+            "spec_tflops": SPEC_BF16_TFLOPS, "spec_source": SPEC_SOURCE,
+            "vs_clock_derived_bf16": tflops_per_gpu / derived,
+            "clock_derived_tflops": derived,
+            "clock_derived": f"{sms} SMs x {BF16_FLOP_PER_CLK_PER_SM} FLOP/clk/SM x "
+                             f"{max_mhz:.0f} MHz",
+            "vs_measured_bf16": tflops_per_gpu / peaks["bf16_tflops"],
+            "measured_tflops": peaks["bf16_tflops"]}
 
 
 def config_of(wl, args):
@@ -425,6 +451,44 @@ def main():
             raise RuntimeError("device status word reports an error in the timed region")
     model = flops.model_flops(wl)
     ms, value = aggregate_timing(ms_local, world, model, args.steps, "cuda")
+    glu = getattr(wl, "variant", 0) == 1  # SwiGLU: the first GEMM also computes W_up
+    g1_flops = 2 * wl.tokens * wl.hidden * (3 * wl.hidden + (2 if glu else 1) * wl.ffn)
+
+    # ---- sustained: the same steps over a timed region of a few seconds, after the burst
+    # above; a 1.4 kW part settles under its power cap within about a second
+    sustained = None
+    if args.sustained_s > 0:
+        n_s = max(args.steps, int(args.sustained_s * 1e3 / (ms / args.steps)) + 1)
+        for b in blocks:
+            b.trace_enable(n_s)
+        clocks_s = ClockSampler(torch.cuda.current_device())
+        clocks_s.start()
+        time.sleep(0.3)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(n_s):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        clk_s = clocks_s.stop()
+        per_kernel_s = [0.0] * 4
+        for b in blocks:
+            k_ms, n = b.trace_read()
+            assert n == n_s
+            per_kernel_s = [a + c for a, c in zip(per_kernel_s, k_ms)]
+            b.trace_enable(0)
+        for b in blocks:
+            if b.status() != pb.PB_OK:
+                raise RuntimeError("device status word reports an error in the sustained region")
+        ms_s, value_s = aggregate_timing(s0.elapsed_time(s1), world, model, n_s, "cuda")
+        g1_s = g1_flops / (per_kernel_s[1] / (n_s * wl.layers) / 1e3) / 1e12
+        sustained = {"value": value_s, "unit": UNIT, "steps": n_s, "seconds": ms_s / 1e3,
+                     "ms_per_step": ms_s / n_s, "clocks": clk_s,
+                     "gemm_block_in_tflops": g1_s,
+                     "kernel_share": [k / max(sum(per_kernel_s), 1e-9) for k in per_kernel_s]}
 
     # ---- end to end through the host-buffer entry point (pinned x in, y out)
     e2e = None
@@ -464,8 +528,6 @@ def main():
     peaks, peak_src = load_peaks()
     launches = args.steps * wl.layers
     g1_ms = per_kernel[1] / launches
-    glu = getattr(wl, "variant", 0) == 1  # SwiGLU: the first GEMM also computes W_up
-    g1_flops = 2 * wl.tokens * wl.hidden * (3 * wl.hidden + (2 if glu else 1) * wl.ffn)
     achieved = g1_flops / (g1_ms / 1e3) / 1e12
     # FP8 operands: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
     ratio = 2.0 if args.operands == "fp8" else 1.0
@@ -475,8 +537,15 @@ def main():
                 "frac": achieved / (peaks["bf16_tflops"] * ratio), "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)"
                                + (" x 2 (nominal fp8 / bf16)" if ratio != 1.0 else ""),
-                "frac_of_sustained": achieved / (peaks["bf16_tflops_sustained"] * ratio),
                 "algorithmic_flops_per_launch": g1_flops, "ms_per_launch": g1_ms}
+    if sustained is not None:
+        # the sustained region's rate against the sustained (power-capped) cuBLAS figure
+        sp = peaks["bf16_tflops_sustained"] * ratio
+        roofline["sustained"] = {"achieved": sustained["gemm_block_in_tflops"], "peak": sp,
+                                 "frac": sustained["gemm_block_in_tflops"] / sp,
+                                 "peak_source": f"{peak_src} bf16 sustained (cuBLAS 8192^3, "
+                                                "4 s back to back)"}
+        roofline["frac_of_sustained"] = roofline["sustained"]["frac"]
     step_ms = ms / args.steps
     kernels = {}
     for name, k_ms in zip(KERNELS, per_kernel):
@@ -505,10 +574,12 @@ def main():
             "dtype": {"bf16": "bf16", "fp16": "fp16", "fp8": "e4m3"}[args.operands],
             "data": "synthetic (seeded N(0,1) activations, N(0, std) weights)",
             "config": config_of(wl, args),
-            "mfu": {"vs_spec_dense_bf16": value / world / SPEC_BF16_TFLOPS,
-                    "spec_tflops": SPEC_BF16_TFLOPS,
-                    "vs_measured_bf16": value / world / peaks["bf16_tflops"],
-                    "measured_tflops": peaks["bf16_tflops"]},
+            "mfu": mfu_of(value / world, peaks, clk, torch.cuda.get_device_properties(
+                torch.cuda.current_device()).multi_processor_count),
+            "sustained": None if sustained is None else dict(
+                sustained, mfu=mfu_of(sustained["value"] / world, peaks, sustained["clocks"],
+                                      torch.cuda.get_device_properties(
+                                          torch.cuda.current_device()).multi_processor_count)),
             "model_flops_per_step": model * world,
             "kernels": kernels,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

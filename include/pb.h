@@ -180,6 +180,20 @@ typedef struct pb_options {
 
 typedef struct pb_handle pb_handle;
 
+/* Guard gaps (a debugging aid for out-of-bounds writes; the pages have no counterpart).
+ * pb_set_guard_bytes(g) makes every workspace and scratch layout computed afterwards leave
+ * g unused bytes after each of its regions (before the next region's 1024-byte alignment):
+ * pb_weight_workspace_bytes, pb_create, pb_scratch_bytes, pb_train_scratch_bytes,
+ * pb_get_scratch_layout and every call that takes a scratch buffer. No kernel reads or
+ * writes those bytes, so a caller that fills the buffers with a known pattern can check
+ * after its calls that nothing ran past the end of a region. g <= 1 MiB (else
+ * PB_ERR_INVALID_ARG); default 0. It is process-wide: set it before sizing the buffers and
+ * creating the handles that use them, and keep it until they are released (a handle keeps
+ * the workspace layout of its pb_create; a scratch sized under another setting is too small
+ * or laid out differently, and too small is reported as PB_ERR_WORKSPACE). */
+pb_status pb_set_guard_bytes(size_t bytes);
+pb_status pb_get_guard_bytes(size_t* bytes);
+
 /* Bytes of the per-handle weight workspace (packed [Wqkv | W1] and [Wo ; W2] in the
  * K-major layout the tensor cores read, biases, LN parameters and the status word). */
 pb_status pb_weight_workspace_bytes(const pb_dims* dims, size_t* bytes);
@@ -361,17 +375,21 @@ pb_status pb_gemm_bf16_layout(int32_t M, int32_t N, int32_t K, const void* A, in
                               const void* B, int32_t b_mn, void* C, void* scratch,
                               size_t scratch_bytes, int* status, void* stream);
 
-/* pb_gemm_bf16 for callers that cannot allocate device memory: those capturing a CUDA
- * graph (cudaMalloc is not allowed during capture), plugins whose device memory belongs
- * to a host engine's allocator, and paths where an allocation could block. The pages have
- * no counterpart; it is a convenience of this library. It computes the same product with
- * the same stream-K schedule, with the scratch in a fixed array of the library's device
- * memory (25,171,968 bytes per GPU, held until the process exits) instead of a caller
- * buffer. It allocates nothing. Limits: GPUs with at most 192 SMs (96 CTA pairs);
- * otherwise PB_ERR_UNSUPPORTED. The first call on each device looks up the array's
- * address (cudaGetSymbolAddress); make that first call before any stream capture. All
- * calls share the one array: calls that can overlap on the GPU (other streams, other
- * host threads) race on it and must be serialised by the caller. */
+/* pb_gemm_bf16 for callers that cannot allocate device memory: plugins inside an engine or
+ * framework whose device memory all belongs to the host program's allocator (they are
+ * handed inputs and outputs, nothing more), and latency-bound paths where a cudaMalloc
+ * could synchronise the device or block. The pages have no counterpart; it is a
+ * convenience of this library. It computes the same product with the same stream-K
+ * schedule as pb_gemm_bf16 with scratch, so its output is bit-identical to that call's,
+ * with the scratch in a fixed array of the library's own device memory (25,171,968 bytes
+ * per GPU, held until the process exits) instead of a caller buffer. It allocates nothing
+ * and calls no allocating routine. Limits: GPUs with at most 192 SMs (96 CTA pairs);
+ * otherwise PB_ERR_UNSUPPORTED, before anything is enqueued. The first call on each device
+ * looks up the array's address (cudaGetSymbolAddress) in the device's primary context,
+ * which must stay alive for the rest of the process; make that first call before any
+ * stream capture. All calls share the one array, which keeps the last call's contents
+ * (each call leaves its flags cleared): calls that can overlap on the GPU (other streams,
+ * other host threads) race on it and must be serialised by the caller. */
 pb_status pb_gemm_bf16_static(int32_t M, int32_t N, int32_t K, const void* A, const void* B,
                               void* C, int* status, void* stream);
 

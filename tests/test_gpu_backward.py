@@ -284,3 +284,13 @@ def test_two_layer_training_through_per_layer_calls():
             tol = DS_MEAN_TOL if n in ("wqkv", "ln_gamma") else COMPOUND_MEAN_TOL
             assert_parity(grads[i][k].cpu().numpy(), ref[n], f"stack2 layer {i} d{n}",
                           mean_tol=tol)
+
+
+def test_backward_full_width_matches_oracle():
+    # The width of gpt3-175b-layer (H 12288, 96 heads of 128), full causal attention over
+    # 640 tokens (five key tiles, a ragged last query tile) with F cut to 4096 so the fp64
+    # oracle stays near 4 TFLOP. Every backward GEMM runs several waves of tiles and splits
+    # its last waves along K (stream-K): d act (640 x 16384, K 12288), dLN(x) (640 x 12288,
+    # K 40960), [dWo ; dW2] (16384 x 12288, K 640) and [dWqkv | dW1] (12288 x 40960, K 640).
+    wl = Workload("bwd-h12288-s640", 1, 640, 12288, 96, 128, 4096, 640, 1, 0.006)
+    check_backward(wl)

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from oracle import oracle as O
-from tests.parity import assert_parity, host, host_params, oracle_dims, report
+from tests.parity import assert_parity, host, host_params, metrics, oracle_dims, report
 from transformer_block_gb300 import WORKLOADS, inputs, pb
 from transformer_block_gb300.configs import Workload
 
@@ -67,6 +67,35 @@ def test_gemm_stream_k_matches_oracle(M, N, K):
     # the split changes the fp32 summation order, so some rounded outputs differ: the
     # stream-K path really ran
     assert not torch.equal(c_sk, c_dp)
+
+
+def test_stream_k_leaves_its_flags_cleared():
+    # Each stream-K flag is read by one warp, which clears it: after any completed call the
+    # flags region (the last 96 pairs x 2 CTAs x 4 warps x 8 bytes of the scratch) is zero
+    # again, so a later launch that carries the same epoch value cannot take a stale flag
+    # (and the partial tiles next to it) for its own. New inputs on the second call make
+    # stale partials visible in the output.
+    M, N, K = 2048, 12288, 1024
+    g = torch.Generator(device="cuda").manual_seed(11)
+    a1 = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    a2 = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = torch.zeros(pb.gemm_scratch_bytes(), dtype=torch.uint8, device="cuda")
+    flags = scratch[-96 * 2 * 4 * 8:].view(torch.int64)
+    c1 = pb.gemm(a1, b, scratch=scratch, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert int(flags.count_nonzero()) == 0
+    c2 = pb.gemm(a2, b, scratch=scratch, status=status)
+    d2 = pb.gemm(a2, b, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert int(flags.count_nonzero()) == 0
+    rows = np.arange(0, M, 8)
+    assert_parity(host(c2)[rows], O.linear(host(a2)[rows], host(b).T), "stream-K, second call")
+    assert_parity(host(c1)[rows], O.linear(host(a1)[rows], host(b).T), "stream-K, first call")
+    assert not torch.equal(c2, d2)
 
 
 @pytest.mark.parametrize("rows,H", [(37, 256), (7, 128), (9, 384), (5, 2048), (300, 4096), (3, 12288),
@@ -235,34 +264,60 @@ def test_full_size_sampled_rows(name, clusters):
     report(g - xs, ref - xs, f"{name} sampled y-x")
 
 
-def test_full_size_stack_prefix_rows():
-    # By causality the first P rows of every layer depend only on the first P inputs, so
-    # the oracle runs the 8 layers on a P-token prefix. Both operand precisions run on
-    # the same inputs; fp16 operands meet the acceptance bar, bf16 operands are held to
-    # the max bar and their mean error is reported (8 layers of bf16 GEMM operands
-    # accumulate about 3.2e-3 mean relative error, see the design notes).
+# stack8-h5120 (8 layers, window 1024) on a prefix of sequence 0. By causality the first P
+# rows of every layer depend only on the first P inputs, so the fp64 oracle chains the 8
+# layers on P tokens (about 7.7 TFLOP). P = 1536: from token 1023 on the 1024-key window is
+# full, so a third of the graded rows see the window's far edge and its masking in every
+# layer.
+STACK8_P = 1536
+
+
+@pytest.fixture(scope="module")
+def stack8_prefix():
     wl = WORKLOADS["stack8-h5120"]
-    P = 96
     x, layers = inputs.make_stack(wl, device="cuda")
-    dims = pb.make_dims(wl)
     od = oracle_dims(wl)
-    od = O.Dims(od.batch, P, od.hidden, od.heads, od.head_dim, od.ffn, od.window, od.ln_eps)
-    z = host(x).reshape(wl.batch, wl.seq, wl.hidden)[:, :P].astype(np.float64)
+    od = O.Dims(1, STACK8_P, od.hidden, od.heads, od.head_dim, od.ffn, od.window, od.ln_eps)
+    z = host(x).reshape(wl.batch, wl.seq, wl.hidden)[:1, :STACK8_P].astype(np.float64)
     for p in layers:
         z = O.block_forward(od, z, host_params(p))
-    for prec in ("fp16", "bf16"):
-        blocks = [pb.ParallelBlock(dims, p, operand_precision=PRECISIONS[prec]) for p in layers]
-        y = pb.forward_stack(blocks, x)
-        torch.cuda.synchronize()
-        for b in blocks:
-            assert b.status() == pb.PB_OK
-        g = host(y).reshape(wl.batch, wl.seq, wl.hidden)[:, :P]
-        del blocks, y
-        if prec == "fp16":
-            assert_parity(g, z, f"stack8 fp16 operands, prefix {P} rows")
-        else:
-            report(g, z, f"stack8 bf16 operands, prefix {P} rows")
-            assert_parity(g, z, f"stack8 bf16 operands, prefix {P} rows", mean_tol=4e-3)
+    return wl, x, layers, z.reshape(STACK8_P, wl.hidden)
+
+
+def stack8_gpu_prefix(wl, x, layers, prec):
+    dims = pb.make_dims(wl)
+    blocks = [pb.ParallelBlock(dims, p, operand_precision=PRECISIONS[prec]) for p in layers]
+    y = pb.forward_stack(blocks, x)
+    torch.cuda.synchronize()
+    for b in blocks:
+        assert b.status() == pb.PB_OK
+    return host(y).reshape(wl.batch, wl.seq, wl.hidden)[0, :STACK8_P]
+
+
+def test_full_size_stack_prefix_fp16_operands(stack8_prefix):
+    # The graded configuration of the 8-layer stack: 16-bit GEMM operands with 3 more
+    # mantissa bits than bf16 (same tensor rate), fp32 accumulation, at the standard bar.
+    wl, x, layers, z = stack8_prefix
+    g = stack8_gpu_prefix(wl, x, layers, "fp16")
+    report(g[1023:], z[1023:], "stack8 fp16 operands, window-full rows 1023..1535")
+    assert_parity(g, z, f"stack8 fp16 operands, prefix {STACK8_P} rows")
+
+
+@pytest.mark.xfail(strict=True, reason=(
+    "known: with bf16 GEMM operands the 8-layer stack sits at about 3.2e-3 mean relative "
+    "error, above the 3e-3 bar; a CPU emulation of the same rounding points predicts it "
+    "(3.17e-3 on this prefix), and rounding the GEMM operands to bf16 with everything else "
+    "exact already exceeds the bar"))
+def test_full_size_stack_prefix_bf16_operands(stack8_prefix):
+    # The default bf16 operands at the standard bar, kept as a recorded known failure: the
+    # max bar holds, the mean bar does not (strict: a pass would be reported).
+    wl, x, layers, z = stack8_prefix
+    g = stack8_gpu_prefix(wl, x, layers, "bf16")
+    report(g, z, f"stack8 bf16 operands, prefix {STACK8_P} rows")
+    report(g[1023:], z[1023:], "stack8 bf16 operands, window-full rows 1023..1535")
+    mx, _ = metrics(g, z)
+    assert mx <= 2e-2
+    assert_parity(g, z, f"stack8 bf16 operands, prefix {STACK8_P} rows")
 
 
 def test_fp16_range_violation_is_reported():

@@ -1,12 +1,20 @@
 """pb_gemm_bf16_static: the stream-K GEMM for callers that cannot allocate device memory
-(graph capture, engine-owned memory, allocation-free paths), with its scratch in the
-library's own fixed device array. Its output must match the caller-scratch entry point,
-pb_gemm_bf16, on two calls in a row. Collected last, so a failure here stops nothing else.
+(plugins whose device memory all belongs to a host engine's allocator, paths where a
+cudaMalloc could block), with its scratch in the library's own fixed device array.
+
+It runs the same stream-K schedule as pb_gemm_bf16 with caller scratch, so on two calls in
+a row (the second with new inputs, which stale partial tiles or flags left by the first
+would corrupt) its output must equal that entry point's bit for bit, and so also meet the
+oracle bar. The shapes leave a partial last wave, so tiles really are split along K: the
+result differs in rounding from the whole-tile GEMM (no scratch). Collected last, so that
+a failure here stops nothing else.
 """
 
+import numpy as np
 import pytest
 import torch
 
+from oracle import oracle as O
 from tests.parity import assert_parity, host
 from transformer_block_gb300 import pb
 
@@ -19,14 +27,24 @@ def test_static_scratch_gemm_matches_caller_scratch_gemm(M, N, K):
         pytest.skip("no CUDA device")
     torch.cuda.set_device(0)
     g = torch.Generator(device="cuda").manual_seed(7 * M + N + K)
-    a = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    a1 = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    a2 = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
     b = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    scratch = torch.empty(pb.gemm_scratch_bytes(), dtype=torch.uint8, device="cuda")
-    ref = pb.gemm(a, b, scratch=scratch, status=status)
-    first = pb.gemm_static(a, b, status=status)
-    second = pb.gemm_static(a, b, status=status)
+    scratch = torch.zeros(pb.gemm_scratch_bytes(), dtype=torch.uint8, device="cuda")
+    ref1 = pb.gemm(a1, b, scratch=scratch, status=status)
+    ref2 = pb.gemm(a2, b, scratch=scratch, status=status)
+    whole1 = pb.gemm(a1, b, status=status)
+    first = pb.gemm_static(a1, b, status=status)
+    second = pb.gemm_static(a2, b, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    assert_parity(host(first), host(ref), f"static-scratch gemm {M}x{N}x{K}, first call")
-    assert_parity(host(second), host(ref), f"static-scratch gemm {M}x{N}x{K}, second call")
+    assert torch.equal(first, ref1), "static-scratch gemm, first call"
+    assert torch.equal(second, ref2), "static-scratch gemm, second call (new inputs)"
+    # the K split changes the fp32 summation order of the split tiles: stream-K ran
+    assert not torch.equal(first, whole1)
+    rows = torch.randperm(M, generator=torch.Generator().manual_seed(3))[:256].sort().values
+    r = rows.numpy()
+    for out, a, what in ((first, a1, "first"), (second, a2, "second")):
+        ref = O.linear(host(a)[r], host(b).T)
+        assert_parity(host(out)[r], ref, f"static-scratch gemm {M}x{N}x{K}, {what} call")

@@ -771,6 +771,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           else
             epilogue32<KIND>(ep, row, col0, v);
         }
+        // Each flag has exactly one reader, this warp: clear what it consumed, so the
+        // flags are zero again when the launch ends. A later launch that carries the same
+        // epoch value (a repeated launch of identical parameters) then cannot take them
+        // for its own. (After a wait that gave up the flags are left as they are; the
+        // status word reports that launch.)
+        if (ok && lane == 0)
+          for (int c2 = sc.cluster + 1; c2 <= last; ++c2)
+            sk.flags[(size_t(c2) * 2 + rank) * 4 + quad] = 0;
       }
       tc_fence_before();
       __syncwarp();
@@ -809,8 +817,7 @@ template <int KIND, int OP, int LAYOUT = kKK>
 cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
                         void* sk_scratch, cudaStream_t stream) {
-  static int max_clusters = -1;
-  static cudaError_t attr_err = cudaSuccess;
+  static PerDeviceInit setup;  // per device: shared-memory opt-in and co-resident pairs
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
@@ -821,16 +828,25 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (max_clusters < 0) {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<KIND, OP, LAYOUT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
-    if (attr_err == cudaSuccess) {
-      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-      int n = 0;
-      attr_err = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, OP, LAYOUT>, &cfg);
-      max_clusters = (attr_err == cudaSuccess && n > 0) ? n : 0;
-    }
-  }
+  int max_clusters = 0;
+  const cudaError_t attr_err = per_device_init(
+      setup,
+      [&](int dev, int* out) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, OP, LAYOUT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t occ = cfg;
+        occ.gridDim = dim3(2 * (sms / 2), 1, 1);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, OP, LAYOUT>, &occ);
+        *out = (e == cudaSuccess && n > 0) ? n : 0;
+        return e;
+      },
+      &max_clusters);
   if (attr_err != cudaSuccess) return attr_err;
   if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
   const int tiles = ((M + PM - 1) / PM) * ((N + BN - 1) / BN);

@@ -6,7 +6,33 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace pb {
+
+// ---------------------------------------------------------------- per-device set-up
+// The runtime keeps a kernel's function attributes (the large dynamic shared memory
+// opt-in) per device, and occupancy differs between devices, so launch set-up runs once
+// per device ordinal, under std::call_once (safe when several host threads launch at
+// once), and its result is kept for that device.
+constexpr int kMaxDevices = 128;
+struct PerDeviceInit {
+  std::once_flag once[kMaxDevices];
+  cudaError_t err[kMaxDevices] = {};
+  int value[kMaxDevices] = {};
+};
+// Runs init(device, &value) once for the current device; returns its error and (when
+// value_out is not null) the value it stored.
+template <class F>
+cudaError_t per_device_init(PerDeviceInit& s, F&& init, int* value_out = nullptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(s.once[dev], [&] { s.err[dev] = init(dev, &s.value[dev]); });
+  if (value_out != nullptr) *value_out = s.value[dev];
+  return s.err[dev];
+}
 
 // ---------------------------------------------------------------- LayerNorm (ln.cu)
 constexpr int kLnMaxH = 16384;
@@ -96,7 +122,8 @@ struct EpiParams {
 
 // Stream-K work space: the tiles of the last waves are split along K across all CTA
 // pairs; a pair whose K segment does not start at 0 leaves its fp32 partial tile here and
-// publishes it with a per-warp flag (the launch's epoch value).
+// publishes it with a per-warp flag (the launch's epoch value). The one warp that reads a
+// flag clears it after use, so every launch that completes leaves the flags at zero.
 constexpr int kSkMaxClusters = 96;
 constexpr size_t kSkPartialBytes = size_t(2) * 128 * 256 * 4;  // one pair tile, fp32
 constexpr size_t kSkFlagBytes = size_t(2) * 4 * 8;             // 2 CTAs x 4 warps x u64

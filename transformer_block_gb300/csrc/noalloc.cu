@@ -1,12 +1,12 @@
 // noalloc.cu — the stream-K GEMM for callers that cannot allocate device memory.
 //
 // pb_gemm_bf16 splits the last waves of tiles along K and needs a scratch buffer from
-// its caller for the partial tiles. Some callers have no way to provide one: code that
-// runs while a CUDA graph is being captured (cudaMalloc is not a stream operation and is
-// not allowed during capture), plugins inside an inference engine whose device memory all
-// belongs to the engine's own allocator, and latency-bound paths where an allocation
-// could block. pb_gemm_bf16_static runs the same GEMM with its scratch in a fixed array
-// that lives in this library's own device memory, so the caller passes only A, B and C.
+// its caller for the partial tiles. Some callers have no way to provide one: plugins
+// inside an inference engine or framework whose device memory all belongs to the host
+// program's own allocator (they are handed inputs and outputs, nothing else), and
+// latency-bound paths where a cudaMalloc could synchronise the device or block on the
+// driver. pb_gemm_bf16_static runs the same GEMM with its scratch in a fixed array that
+// lives in this library's own device memory, so the caller passes only A, B and C.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -18,14 +18,18 @@
 namespace {
 
 // Partial tiles and flags for up to kSkMaxClusters CTA pairs (25,171,968 bytes). Every GPU
-// on which this library's device code is loaded holds it until the process exits. The
-// array starts zeroed; the flags carry a per-launch 64-bit epoch that no earlier call
-// used, so nothing in it has to be cleared between calls.
+// on which this library's device code is loaded holds it until the process exits, and it
+// keeps what the last call left. Only the flags must start at zero: the array is
+// zero-initialised when the module loads, and the GEMM clears every flag it consumed before
+// it ends (the partial tiles are always written before they are read).
 static __device__ __align__(256) uint8_t g_sk_scratch[pb::kSkScratchBytes];
 
 constexpr int kMaxDevices = 128;
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices];  // device address of g_sk_scratch, per device
+// Device address of g_sk_scratch, per device ordinal, looked up once in the device's
+// primary context (the context the runtime API uses); the entry point assumes that context
+// stays alive for the rest of the process (no cudaDeviceReset in between).
+void* g_scratch_ptr[kMaxDevices];
 
 }  // namespace
 

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -84,6 +85,17 @@ pb_status cuda_fail(cudaError_t e, const char* what) {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Bytes left unused after every region of the weight workspace and of the scratch layouts
+// (pb_set_guard_bytes; 0 by default). A test fills them with a canary and checks them after
+// its calls: a kernel that writes past the end of a region changes them.
+std::atomic<size_t> g_guard_bytes{0};
+
+// Next region offset after a region of `bytes` at `off`: the guard gap, then 1024-byte
+// alignment.
+size_t next_region(size_t off, size_t bytes) {
+  return align_up(off + bytes + g_guard_bytes.load(std::memory_order_relaxed), 1024);
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 pb_status check_dims(const pb_dims* d) {
@@ -130,31 +142,31 @@ WsLayout ws_layout(const pb_dims& d) {
   WsLayout L{};
   size_t off = 0;
   L.status = off;
-  off = align_up(off + 256, 1024);
+  off = next_region(off, 256);
   L.w1cat = off;
-  off = align_up(off + size_t(w1_rows(d)) * H * 2, 1024);
+  off = next_region(off, size_t(w1_rows(d)) * H * 2);
   L.w2cat = off;
-  off = align_up(off + H * (H + F) * 2, 1024);
+  off = next_region(off, H * (H + F) * 2);
   L.bias1 = off;
-  off = align_up(off + size_t(w1_rows(d)) * 4, 1024);
+  off = next_region(off, size_t(w1_rows(d)) * 4);
   L.bias2 = off;
-  off = align_up(off + H * 4, 1024);
+  off = next_region(off, H * 4);
   L.bias_o = off;
-  off = align_up(off + H * 4, 1024);
+  off = next_region(off, H * 4);
   L.bias_2 = off;
-  off = align_up(off + H * 4, 1024);
+  off = next_region(off, H * 4);
   L.gamma = off;
-  off = align_up(off + H * 2, 1024);
+  off = next_region(off, H * 2);
   L.beta = off;
-  off = align_up(off + H * 2, 1024);
+  off = next_region(off, H * 2);
   L.w1scale = off;
-  off = align_up(off + size_t(w1_rows(d)) * 4, 1024);
+  off = next_region(off, size_t(w1_rows(d)) * 4);
   L.w2scale = off;
-  off = align_up(off + H * 4, 1024);
+  off = next_region(off, H * 4);
   L.amax1 = off;
-  off = align_up(off + size_t(w1_rows(d)) * 4, 1024);
+  off = next_region(off, size_t(w1_rows(d)) * 4);
   L.amax2 = off;
-  off = align_up(off + H * 4, 1024);
+  off = next_region(off, H * 4);
   L.total = off;
   return L;
 }
@@ -170,50 +182,50 @@ pb_scratch_layout scratch_layout(const pb_dims& d) {
   L.seq_pad = align_up(size_t(d.seq), 8);
   size_t off = 0;
   L.xn = off;
-  off = align_up(off + T * H * 2, 1024);
+  off = next_region(off, T * H * 2);
   L.qk = off;
-  off = align_up(off + T * 2 * H * 2, 1024);
+  off = next_region(off, T * 2 * H * 2);
   L.vt = off;
-  off = align_up(off + size_t(d.batch) * H * L.seq_pad * 2, 1024);
+  off = next_region(off, size_t(d.batch) * H * L.seq_pad * 2);
   L.act = off;
-  off = align_up(off + T * (H + F) * 2, 1024);
+  off = next_region(off, T * (H + F) * 2);
   L.io = off;
-  off = align_up(off + T * H * 2, 1024);
+  off = next_region(off, T * H * 2);
   L.io2 = off;
-  off = align_up(off + T * H * 2, 1024);
+  off = next_region(off, T * H * 2);
   L.res0 = off;
-  off = align_up(off + T * H * 4, 1024);
+  off = next_region(off, T * H * 4);
   L.res1 = off;
-  off = align_up(off + T * H * 4, 1024);
+  off = next_region(off, T * H * 4);
   L.sk = off;
-  off = align_up(off + pb::kSkScratchBytes, 1024);
+  off = next_region(off, pb::kSkScratchBytes);
   L.q8 = off;
-  off = align_up(off + T * (H + F), 1024);
+  off = next_region(off, T * (H + F));
   L.qscale = off;
-  off = align_up(off + 2 * T * 4, 1024);
+  off = next_region(off, 2 * T * 4);
   L.total = off;
   // training: what the backward reads from the forward, then its own intermediates
   const size_t Fp = size_t(w1_rows(d)) - 3 * H;  // F, or 2F for SwiGLU
   const size_t NZ = size_t(w1_rows(d));          // columns of dz = [dq | dk | dv | dh]
   const size_t rows_lse = size_t(d.batch) * size_t(d.heads) * lse_ld(d);
   L.hpre = off;
-  off = align_up(off + T * Fp * 2, 1024);
+  off = next_region(off, T * Fp * 2);
   L.lse = off;
-  off = align_up(off + rows_lse * 4, 1024);
+  off = next_region(off, rows_lse * 4);
   L.d_attn = off;
-  off = align_up(off + T * H * 2, 1024);
+  off = next_region(off, T * H * 2);
   L.delta = off;
-  off = align_up(off + rows_lse * 4, 1024);
+  off = next_region(off, rows_lse * 4);
   L.dq_acc = off;
-  off = align_up(off + T * H * 4, 1024);
+  off = next_region(off, T * H * 4);
   L.dz = off;
-  off = align_up(off + T * NZ * 2, 1024);
+  off = next_region(off, T * NZ * 2);
   L.dxn = off;
-  off = align_up(off + T * H * 4, 1024);
+  off = next_region(off, T * H * 4);
   L.stats = off;
-  off = align_up(off + T * 8, 1024);
+  off = next_region(off, T * 8);
   L.partials = off;
-  off = align_up(off + size_t(pb::kColBlocks) * (NZ > 2 * H ? NZ : 2 * H) * 4, 1024);
+  off = next_region(off, size_t(pb::kColBlocks) * (NZ > 2 * H ? NZ : 2 * H) * 4);
   L.train_total = off;
   return L;
 }
@@ -1275,6 +1287,18 @@ pb_status pb_quantize_rows_e4m3(int64_t rows, int32_t cols, const void* x, void*
                                         static_cast<float*>(scales),
                                         static_cast<cudaStream_t>(stream)),
           "quantize launch");
+  return PB_OK;
+}
+
+pb_status pb_set_guard_bytes(size_t bytes) {
+  if (bytes > (size_t(1) << 20)) return fail(PB_ERR_INVALID_ARG, "guard of %zu bytes > 1 MiB", bytes);
+  g_guard_bytes.store(bytes, std::memory_order_relaxed);
+  return PB_OK;
+}
+
+pb_status pb_get_guard_bytes(size_t* bytes) {
+  if (bytes == nullptr) return fail(PB_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = g_guard_bytes.load(std::memory_order_relaxed);
   return PB_OK;
 }
 

@@ -557,8 +557,11 @@ template <int DH>
 cudaError_t launch_dh(const CUtensorMap& tmQK, const CUtensorMap& tmVT, const SwaParams& p,
                       int* status, uint64_t limit_ns, cudaStream_t stream) {
   using L = Layout<DH>;
-  static cudaError_t attr = cudaFuncSetAttribute(
-      swa_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L::SMEM));
+  static PerDeviceInit setup;  // per device: the shared-memory opt-in
+  const cudaError_t attr = per_device_init(setup, [](int, int*) {
+    return cudaFuncSetAttribute(swa_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(L::SMEM));
+  });
   if (attr != cudaSuccess) return attr;
   const int64_t items = int64_t((p.num_q_tiles + 1) / 2) * p.nh * p.B;
   if (items <= 0) return cudaSuccess;

@@ -412,8 +412,11 @@ cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmDQ, const SwaBwdParams& p, int* status,
                            uint64_t limit_ns, cudaStream_t stream) {
   if (p.dh != DH || p.lse_ld % BQ != 0 || p.lse_ld < p.S) return cudaErrorInvalidValue;
-  static cudaError_t attr = cudaFuncSetAttribute(
-      swa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
+  static PerDeviceInit setup;  // per device: the shared-memory opt-in
+  const cudaError_t attr = per_device_init(setup, [](int, int*) {
+    return cudaFuncSetAttribute(swa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(SMEM));
+  });
   if (attr != cudaSuccess) return attr;
   const int64_t tiles = (int64_t(p.S) + BKV - 1) / BKV;
   const int64_t grid = tiles * p.nh * p.B;

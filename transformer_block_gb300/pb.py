@@ -100,6 +100,8 @@ SIGNATURES = {
     "pb_swa_attention": (ctypes.c_int, [_DP, _P, _P, _P, _I64, _P, _P]),
     "pb_wait_probe": (ctypes.c_int, [_U64, _P, _P]),
     "pb_gemm_bf16_static": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "pb_set_guard_bytes": (ctypes.c_int, [_S]),
+    "pb_get_guard_bytes": (ctypes.c_int, [ctypes.POINTER(_S)]),
 }
 
 _lib = None
@@ -218,12 +220,17 @@ class ParallelBlock:
     """One parallel transformer block: a ``pb_handle`` plus the workspace it owns."""
 
     def __init__(self, dims: pb_dims, params: dict, stream=None,
-                 operand_precision: int = PB_OPERANDS_BF16, wait_limit_ns: int = 0):
+                 operand_precision: int = PB_OPERANDS_BF16, wait_limit_ns: int = 0,
+                 workspace: torch.Tensor | None = None):
+        """``workspace``: a caller-provided uint8 CUDA tensor of at least
+        ``weight_workspace_bytes(dims)`` (256-byte aligned), else one is allocated."""
         self.dims = dims
         self.operand_precision = operand_precision
         self._lib = lib()
         dev = params["wqkv"].device
-        self.workspace = torch.empty(weight_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+        if workspace is None:
+            workspace = torch.empty(weight_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+        self.workspace = workspace
         w = pb_weights(*[_ptr(params.get(n)) for n in WEIGHT_FIELDS])
         opt = pb_options(operand_precision, wait_limit_ns)
         h = ctypes.c_void_p()
@@ -375,6 +382,18 @@ def layernorm(x, gamma, beta, eps=1e-5, out=None, stream=None):
                                               _ptr(beta), float(eps), _ptr(out),
                                               _stream(stream)))
     return out
+
+
+def set_guard_bytes(n: int):
+    """Unused bytes after every workspace and scratch region of the layouts computed from
+    now on (``pb_set_guard_bytes``; process-wide, a debugging aid)."""
+    _check("pb_set_guard_bytes", lib().pb_set_guard_bytes(int(n)))
+
+
+def guard_bytes() -> int:
+    n = ctypes.c_size_t()
+    _check("pb_get_guard_bytes", lib().pb_get_guard_bytes(ctypes.byref(n)))
+    return n.value
 
 
 def gemm_scratch_bytes() -> int:
