@@ -156,11 +156,11 @@ struct SwaParams {
                  // (times log2(e) / sqrt(dh)), or null
   int64_t lse_ld;
 };
-constexpr int kSwaBQ = 128;  // query rows per tile (one tile per CTA of a pair)
-constexpr int kSwaBKV = 128;  // keys per tile (half of them in each CTA of the pair)
+constexpr int kSwaBQ = 128;  // query rows per tile (two tiles per CTA)
+constexpr int kSwaBKV = 128;  // keys per tile
 // tmQ: the [B][S][2H] q|k buffer in boxes of 64 columns x kSwaBQ rows; tmK: the same buffer
-// in boxes of 64 columns x kSwaBKV / 2 rows; tmVT: v^T [B*nh*dh][seq_pad] in boxes of 64
-// keys x dh / 2 rows.
+// in boxes of 64 columns x kSwaBKV rows; tmVT: v^T [B*nh*dh][seq_pad] in boxes of kSwaBKV
+// keys x dh rows.
 cudaError_t launch_swa(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmVT,
                        const SwaParams& p, int* status, uint64_t limit_ns, cudaStream_t stream);
 

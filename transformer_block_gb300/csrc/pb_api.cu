@@ -316,23 +316,21 @@ pb_status make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
   return make_map(m, base, 2, dims, strides, box, t);
 }
 
-// Tensor maps of the attention step, whose key and value tiles are split between the two
-// CTAs of a pair: q|k [B][S][2H] read as query tiles (64 columns x 128 rows) and as half
-// key tiles (64 columns x 64 rows), and v^T [B*H][seq_pad] in boxes of 64 keys x dh / 2
-// rows (half a V^T tile's rows).
+// Tensor maps of the attention step: q|k [B][S][2H] read as query tiles and as key tiles,
+// and v^T [B*H][seq_pad] read in boxes of 64 keys x dh rows.
 pb_status make_swa_maps(const pb_dims& d, const void* qk, const void* vt, size_t seq_pad,
                         CUtensorMap* tm_q, CUtensorMap* tm_k, CUtensorMap* tm_vt) {
   const uint64_t H = uint64_t(d.hidden);
   const uint64_t dims[3] = {2 * H, uint64_t(d.seq), uint64_t(d.batch)};
   const uint64_t strides[2] = {2 * H * 2, 2 * H * 2 * uint64_t(d.seq)};
   const uint32_t qbox[3] = {64, uint32_t(pb::kSwaBQ), 1};
-  const uint32_t kbox[3] = {64, uint32_t(pb::kSwaBKV / 2), 1};
+  const uint32_t kbox[3] = {64, uint32_t(pb::kSwaBKV), 1};
   pb_status s = make_map(tm_q, qk, 3, dims, strides, qbox);
   if (s == PB_OK) s = make_map(tm_k, qk, 3, dims, strides, kbox);
   if (s != PB_OK) return s;
   const uint64_t vdims[2] = {uint64_t(d.seq), uint64_t(d.batch) * H};
   const uint64_t vstr[1] = {uint64_t(seq_pad) * 2};
-  const uint32_t vbox[2] = {64, uint32_t(d.head_dim / 2)};  // 64 keys = one 128-byte row
+  const uint32_t vbox[2] = {64, uint32_t(d.head_dim)};  // 64 keys = one 128-byte swizzle row
   return make_map(tm_vt, vt, 2, vdims, vstr, vbox);
 }
 

@@ -234,17 +234,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// 3-D form of tma_load_2d_pair.
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m,
-                                                 uint32_t bar, int32_t c0, int32_t c1,
-                                                 int32_t c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
 // global to this CTA's shared memory, completing on the mbarrier at `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -324,19 +313,6 @@ __device__ __forceinline__ void mma_f8kind_ss_pair(uint32_t d_tmem, uint64_t a_d
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Pair MMA with A in tensor memory: each CTA's tensor memory holds its 128 rows of A at
-// `a_tmem` (16-bit elements packed two per column, K = 16 per instruction = 8 columns),
-// each CTA's shared memory half of the N rows of B.
-__device__ __forceinline__ void mma_f16kind_ts_pair(uint32_t d_tmem, uint32_t a_tmem,
-                                                    uint64_t b_desc, uint32_t idesc,
-                                                    uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrives once on the mbarrier at offset `bar` in every CTA of `cta_mask` when all pair
