@@ -132,3 +132,36 @@ def test_step_entry_points_validate(lib):
     assert lib.pb_gemm_scratch_bytes(ctypes.byref(n)) == 0 and n.value > 0
     assert lib.pb_layernorm(4, 12, None, None, None, 1e-5, None, None) == 2   # H % 8
     assert lib.pb_layernorm(4, 16, None, None, None, 1e-5, None, None) == 1   # NULL
+
+
+def test_guard_gaps_in_every_layout(lib):
+    # pb_set_guard_bytes leaves the requested gap after every region (CPU only: layouts are
+    # host arithmetic), keeps 1024-byte alignment, and rejects more than 1 MiB.
+    d = dims(batch=2, seq=130, head_dim=128, heads=2)
+    assert pb.guard_bytes() == 0
+    plain = pb.scratch_layout(d)
+    ws0 = pb.weight_workspace_bytes(d)
+    try:
+        pb.set_guard_bytes(4096)
+        assert pb.guard_bytes() == 4096
+        g = pb.scratch_layout(d)
+        names = ["xn", "qk", "vt", "act", "io", "io2", "res0", "res1", "sk", "q8", "qscale",
+                 "hpre", "lse", "d_attn", "delta", "dq_acc", "dz", "dxn", "stats", "partials"]
+        offs = [getattr(g, n) for n in names] + [g.train_total]
+        plain_offs = [getattr(plain, n) for n in names] + [plain.train_total]
+        for k in range(len(names)):
+            assert offs[k] % 1024 == 0
+            # the region keeps its size and is followed by at least 4096 unused bytes
+            size = plain_offs[k + 1] - plain_offs[k]  # an upper bound of the region's size
+            assert offs[k + 1] - offs[k] >= 4096
+            assert offs[k + 1] - offs[k] <= size + 4096 + 1024
+        assert g.total == g.hpre and g.total > plain.total
+        assert pb.scratch_bytes(d) == g.total
+        assert pb.train_scratch_bytes(d) == g.train_total
+        assert pb.weight_workspace_bytes(d) >= ws0 + 13 * 4096
+        with pytest.raises(pb.PbError):
+            pb.set_guard_bytes((1 << 20) + 1)
+        assert pb.guard_bytes() == 4096
+    finally:
+        pb.set_guard_bytes(0)
+    assert pb.scratch_bytes(d) == plain.total

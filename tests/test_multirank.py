@@ -77,3 +77,19 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = bench.argparse.Namespace(gpus=2, steps=1, warmup=0)
     assert bench.run_reference(args, WORKLOADS["tiny"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_mfu_denominators():
+    # MFU against the nominal dense peak (2.25 PF), the clock-derived peak (SMs x 8192
+    # FLOP/clk/SM x the maximum SM clock) and the measured burst
+    sys.path.insert(0, ROOT)
+    import bench
+
+    peaks = {"bf16_tflops": 1891.2, "bf16_tflops_sustained": 1692.7, "hbm_gbs": 6788.6}
+    m = bench.mfu_of(1800.0, peaks, {"sm_max_mhz": 2070.0}, 152)
+    assert abs(m["vs_spec_dense_bf16"] - 1800.0 / 2250.0) < 1e-12
+    assert abs(m["clock_derived_tflops"] - 152 * 8192 * 2070e6 / 1e12) < 1e-9
+    assert abs(m["vs_clock_derived_bf16"] - 1800.0 / m["clock_derived_tflops"]) < 1e-12
+    assert abs(m["vs_measured_bf16"] - 1800.0 / 1891.2) < 1e-12
+    # no clock record: the documented maximum clock
+    assert bench.mfu_of(1.0, peaks, None, 152)["clock_derived_tflops"] == m["clock_derived_tflops"]
