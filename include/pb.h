@@ -287,6 +287,13 @@ pb_status pb_forward_serial(pb_handle* h, const void* x, void* y, const void* ln
 pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const void* x, void* y,
                            void* scratch, size_t scratch_bytes, void* stream);
 
+/* As pb_forward_stack, with y in fp32 (float [batch*seq, hidden], 16-byte aligned, not
+ * overlapping x): the residual stream the stack carries between its layers, returned
+ * without the final rounding to bf16 (the same stream as pb_forward_stack's y before that
+ * rounding). For callers that keep the residual stream in fp32 across stacks. */
+pb_status pb_forward_stack_f32(pb_handle* const* layers, int32_t n_layers, const void* x,
+                               float* y, void* scratch, size_t scratch_bytes, void* stream);
+
 /* As pb_forward_stack, with x and y in HOST memory (pinned memory gives asynchronous
  * copies): copies x to the device, runs the stack, copies y back, all on `stream`.
  * The caller synchronises the stream before reading y. */

@@ -767,10 +767,10 @@ pb_status check_stack(pb_handle* const* layers, int32_t n_layers, const void* sc
   return PB_OK;
 }
 
-// Layer 0 reads bf16 x, the last layer writes bf16 y; in between the residual stream
-// alternates between the fp32 buffers res0 and res1.
+// Layer 0 reads bf16 x, the last layer writes y (bf16, or fp32 when y_f32); in between
+// the residual stream alternates between the fp32 buffers res0 and res1.
 pb_status run_stack(pb_handle* const* layers, int32_t n, const void* x, void* y,
-                    uint8_t* scratch, cudaStream_t st) {
+                    uint8_t* scratch, cudaStream_t st, bool y_f32 = false) {
   const pb_scratch_layout L = scratch_layout(layers[0]->d);
   void* res[2] = {scratch + L.res0, scratch + L.res1};
   const void* in = x;
@@ -778,7 +778,7 @@ pb_status run_stack(pb_handle* const* layers, int32_t n, const void* x, void* y,
   for (int32_t l = 0; l < n; ++l) {
     const bool last = (l == n - 1);
     void* out = last ? y : res[l % 2];
-    pb_status s = run_block(layers[l], in, in_f32, out, !last, scratch, st);
+    pb_status s = run_block(layers[l], in, in_f32, out, !last || y_f32, scratch, st);
     if (s != PB_OK) return s;
     in = out;
     in_f32 = !last;
@@ -1098,6 +1098,22 @@ pb_status pb_forward_stack(pb_handle* const* layers, int32_t n_layers, const voi
     return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
   return run_stack(layers, n_layers, x, y, static_cast<uint8_t*>(scratch),
                    static_cast<cudaStream_t>(stream));
+}
+
+pb_status pb_forward_stack_f32(pb_handle* const* layers, int32_t n_layers, const void* x,
+                               float* y, void* scratch, size_t scratch_bytes, void* stream) {
+  pb_status s = check_stack(layers, n_layers, scratch, scratch_bytes);
+  if (s != PB_OK) return s;
+  if (x == nullptr || y == nullptr || !aligned(x, 16) || !aligned(y, 16))
+    return fail(PB_ERR_INVALID_ARG, "x and y must be 16-byte aligned device pointers");
+  const pb_dims& d = layers[0]->d;
+  const size_t nx = size_t(d.batch) * d.seq * d.hidden * 2, ny = 2 * nx;
+  if (overlap(x, nx, y, ny)) return fail(PB_ERR_INVALID_ARG, "x and y overlap");
+  const pb_scratch_layout L = scratch_layout(d);
+  if (overlap(x, nx, scratch, L.total) || overlap(y, ny, scratch, L.total))
+    return fail(PB_ERR_INVALID_ARG, "x or y overlaps the scratch buffer");
+  return run_stack(layers, n_layers, x, y, static_cast<uint8_t*>(scratch),
+                   static_cast<cudaStream_t>(stream), true);
 }
 
 pb_status pb_forward_stack_host(pb_handle* const* layers, int32_t n_layers, const void* x_host,

@@ -79,6 +79,7 @@ SIGNATURES = {
     "pb_forward_serial": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _S, _P]),
     "pb_forward_stack": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
     "pb_forward_stack_host": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
+    "pb_forward_stack_f32": (ctypes.c_int, [ctypes.POINTER(_P), _I32, _P, _P, _P, _S, _P]),
     "pb_get_status": (ctypes.c_int, [_P]),
     "pb_clear_status": (ctypes.c_int, [_P, _P]),
     "pb_set_wait_limit_ns": (ctypes.c_int, [_P, _U64]),
@@ -351,6 +352,19 @@ def forward_stack(blocks, x, y=None, scratch=None, stream=None):
     _check("pb_forward_stack", lib().pb_forward_stack(_handles(blocks), len(blocks), _ptr(x),
                                                       _ptr(y), _ptr(scratch), scratch.numel(),
                                                       _stream(stream)))
+    return y
+
+
+def forward_stack_f32(blocks, x, y=None, scratch=None, stream=None):
+    """``forward_stack`` returning the fp32 residual stream (float32 [T, H]) instead of its
+    bf16 rounding (``pb_forward_stack_f32``)."""
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    if scratch is None:
+        scratch = new_scratch(blocks[0].dims, x.device)
+    _check("pb_forward_stack_f32", lib().pb_forward_stack_f32(_handles(blocks), len(blocks),
+                                                              _ptr(x), _ptr(y), _ptr(scratch),
+                                                              scratch.numel(), _stream(stream)))
     return y
 
 
