@@ -180,9 +180,11 @@ def test_stack_and_host_paths_stay_inside_their_regions(w):
     xs = [xh, (x * 0.5).to(torch.bfloat16).cpu().pin_memory()]
     ys = [torch.empty_like(t).pin_memory() for t in xs]
     pb.forward_stack_host_steps(blocks, xs, ys, sg.t)
+    y32g, y32 = guarded_tensor((w.tokens, w.hidden), torch.float32)
+    pb.forward_stack_f32(blocks, x, y=y32, scratch=sg.t)
     what = f"{w.name} stack of 2"
     finish(what, blocks, [(ws, "workspace") for ws, _ in made] +
-           [(yg, "y"), (lambda: check_scratch(sg, dims, False, what), "")])
+           [(yg, "y"), (y32g, "fp32 y"), (lambda: check_scratch(sg, dims, False, what), "")])
     assert torch.equal(yh, y.cpu())
 
 
