@@ -9,7 +9,9 @@
 //   * rows up to 4096 bf16 (2048 fp32) elements: one warp per row, 8 rows per CTA,
 //     reductions by warp shuffles only (layernorm_rows_kernel, 1 warp per row);
 //   * up to 16384 bf16 (8192 fp32): four warps per row, 2 rows per CTA, the warps' partial
-//     sums through shared memory (layernorm_rows_kernel, 4 warps per row);
+//     sums through shared memory (layernorm_rows_kernel, 4 warps per row); each thread
+//     holds only as many vectors as the row needs (4, 6, 8, 12 or 16), and with 12 or fewer
+//     three CTAs fit per SM, so more rows are in flight on the few-row workloads;
 //   * longer fp32 rows: one 256-thread CTA per row, CTA-wide reductions
 //     (layernorm_kernel). The FP8 variant (layernorm_e4m3_kernel) uses this shape for all
 //     rows.
@@ -205,7 +207,7 @@ __device__ __forceinline__ float row_sum(float v, float* red, int slot) {
 // warps takes the same branches around the named barriers (the early exit depends only on
 // the row).
 template <typename TIn, bool F16, bool RMS, int VPL, int WPR>
-__global__ void __launch_bounds__(THREADS, 2) layernorm_rows_kernel(
+__global__ void __launch_bounds__(THREADS, (WPR == 4 && VPL <= 12) ? 3 : 2) layernorm_rows_kernel(
     const TIn* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
     const __nv_bfloat16* __restrict__ beta, uint4* __restrict__ out, int64_t rows, int H,
     float eps, int* status) {
@@ -370,9 +372,15 @@ cudaError_t launch_t(int64_t rows, int H, const void* x, const __nv_bfloat16* ga
       return launch_rows<TIn, F16, 16, 1>(rows, H, x, gamma, beta, eps, out, status, stream);
   }
   if (vpl4 <= kRowMaxVpl<TIn>) {
+    // as few vector registers as the row needs: fewer registers, more rows in flight per SM
+    if (vpl4 <= 4) return launch_rows<TIn, F16, 4, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
+    if (vpl4 <= 6) return launch_rows<TIn, F16, 6, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
     if (vpl4 <= 8) return launch_rows<TIn, F16, 8, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
-    if constexpr (kRowMaxVpl<TIn> >= 16)
+    if constexpr (kRowMaxVpl<TIn> >= 16) {
+      if (vpl4 <= 12)
+        return launch_rows<TIn, F16, 12, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
       return launch_rows<TIn, F16, 16, 4>(rows, H, x, gamma, beta, eps, out, status, stream);
+    }
   }
   if (beta == nullptr)
     layernorm_kernel<TIn, F16, true><<<unsigned(rows), THREADS, 0, stream>>>(
