@@ -44,8 +44,11 @@ constexpr int NUM_BARS = 2 * STAGES + 5;
 // Per epilogue warp, a 32 x 32 fp32 chunk (rows padded to 33 words: conflict-free both
 // ways) for the coalesced gradient stores.
 constexpr int STAGE_PITCH = 33;
-constexpr size_t EPI_STAGE_OFF = size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16;
+// 1024-byte aligned: the forward epilogues' TMA-store buffers (64-byte swizzle) live here
+constexpr size_t EPI_STAGE_OFF =
+    (size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16 + 1023) / 1024 * 1024;
 constexpr size_t SMEM_BYTES = 1024 + EPI_STAGE_OFF + 4 * 32 * STAGE_PITCH * 4;
+static_assert(4 * 32 * STAGE_PITCH * 4 >= 4 * 4096, "four warps' two 2 KB store buffers");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of the GEMM");
 
 __device__ __forceinline__ float gelu_erf(float z) {
@@ -200,12 +203,48 @@ __device__ __forceinline__ void pack_words16(const float (&v)[32], uint32_t (&w)
     w[e] = F16 ? pack_f16x2(v[2 * e], v[2 * e + 1]) : pack_bf16x2(v[2 * e], v[2 * e + 1]);
 }
 
+// A warp's TMA stores: two 2 KB staging buffers (32 rows of 64 bytes) used in turn.
+struct StoreStage {
+  uint32_t base;  // shared-memory address of the warp's buffers
+  uint32_t n;     // stores issued so far
+};
+
+// Warp-wide: the warp's 32 rows (lane l holds row row0 + l as 16 words of 16-bit pairs) of
+// the 32 columns at col0 to the tensor of `tm`, by one TMA store. Rows past the tensor's
+// end are dropped by the copy.
+__device__ __forceinline__ void tma_store_rows32(StoreStage& ss, const CUtensorMap* tm, int row0,
+                                                 int col0, int M, const uint32_t (&w)[16]) {
+  if (row0 >= M) return;  // the whole warp is past the last row (uniform in the warp)
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t buf = ss.base + (ss.n & 1u) * 2048u;
+  if (ss.n >= 2) {  // the buffer's previous store (two ago) must have read it
+    if (lane == 0) bulk_wait_read_1();
+    __syncwarp();
+  }
+  // 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3), which
+  // also spreads the warp's writes over all banks
+  const uint32_t rb = buf + lane * 64u, sw = (lane >> 1) & 3u;
+#pragma unroll
+  for (uint32_t j = 0; j < 4; ++j)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((j ^ sw) << 4)),
+                 "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                 : "memory");
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm, buf, col0, row0);
+    bulk_commit();
+  }
+  ++ss.n;
+}
+
 // Epilogue of 32 consecutive columns [col0, col0 + 32) of one output row. Called by all 32
 // lanes of a warp together, lane l holding row `row` = the warp's first row + l: the plain
 // store is warp-wide (the fused epilogues store row-wise per lane, where the transpose's
 // extra instructions cost more than its fewer store passes save).
 template <int KIND>
-__device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col0, float (&v)[32]) {
+__device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col0, float (&v)[32],
+                                           StoreStage& ss) {
   if (KIND == kEpiStore) {
     const int row0 = row - int(threadIdx.x & 31);
     const int nrows = ep.M - row0 < 32 ? ep.M - row0 : 32;
@@ -228,9 +267,13 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
                      int64_t(ep.ldc) * 2, nrows, w);
     return;
   }
-  if (row >= ep.M) return;
+  // With TMA stores every lane takes part in the warp's copies, rows past M included (the
+  // copy drops them); otherwise a lane past M has nothing to do.
+  const bool tma = ep.tma_store && (KIND == kEpiResidual || (KIND == kEpiBlockIn && !ep.glu));
+  if (row >= ep.M && !tma) return;
+  const bool live = row < ep.M;
   if (ep.scale_a != nullptr) {  // FP8 operands: undo the row and channel scales
-    const float sa = ep.scale_a[row];
+    const float sa = live ? ep.scale_a[row] : 0.f;
     const float4* s4 = reinterpret_cast<const float4*>(ep.scale_b + col0);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -255,9 +298,17 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
   if (KIND == kEpiBlockIn) {
     const int H = ep.H;
     const int cc = col0 + ep.col_base;  // column of [q | k | v | h]
+    const int row0 = row - int(threadIdx.x & 31);
     if (cc < 2 * H) {  // q | k
-      store_row32<false>(ep.qk + int64_t(row) * (2 * H) + cc, v);
+      if (tma) {
+        uint32_t w[16];
+        pack_words16<false>(v, w);
+        tma_store_rows32(ss, &ep.tm_out0, row0, cc, ep.M, w);
+      } else {
+        store_row32<false>(ep.qk + int64_t(row) * (2 * H) + cc, v);
+      }
     } else if (cc < 3 * H) {  // v, stored transposed per (sequence, head)
+      if (!live) return;
       const int c = cc - 2 * H;
       const int head = c / ep.dh, d0 = c - head * ep.dh;
       const int b = row / ep.S, s = row - b * ep.S;
@@ -266,7 +317,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
 #pragma unroll
       for (int i = 0; i < 32; ++i) dst[int64_t(i) * ep.seq_pad] = __float2bfloat16_rn(v[i]);
     } else {
-      if (ep.hpre != nullptr)  // training forward: keep h for the backward
+      if (ep.hpre != nullptr && live)  // training forward: keep h for the backward
         store_row32<false>(ep.hpre + int64_t(row) * (ep.N + ep.col_base - 3 * H) + (cc - 3 * H),
                            v);
       if (ep.glu) {
@@ -292,8 +343,17 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
         if (ep.act_f16) {
           bool bad = false;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) bad |= !(fabsf(v[i]) <= kF16Max);
+          for (int i = 0; i < 32; ++i) bad |= live && !(fabsf(v[i]) <= kF16Max);
           if (bad) report_range(ep.status);
+        }
+        if (tma) {
+          uint32_t w[16];
+          if (ep.act_f16)
+            pack_words16<true>(v, w);
+          else
+            pack_words16<false>(v, w);
+          tma_store_rows32(ss, &ep.tm_out1, row0, H + (cc - 3 * H), ep.M, w);
+        } else if (ep.act_f16) {
           store_row32<true>(static_cast<__half*>(ep.act) + off, v);
         } else {
           store_row32<false>(static_cast<__nv_bfloat16*>(ep.act) + off, v);
@@ -351,7 +411,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
       store_f32<32>(ep.g0 + int64_t(row) * ep.ld0 + col0, v, ep.accumulate);
     }
   } else {  // kEpiResidual: y = D + bias + x
-    const int64_t off = int64_t(row) * ep.N + col0;
+    const int64_t off = int64_t(live ? row : 0) * ep.N + col0;
     if (ep.resid_f32) {
       const float4* x4 = reinterpret_cast<const float4*>(static_cast<const float*>(ep.resid) + off);
 #pragma unroll
@@ -378,10 +438,15 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
         }
       }
     }
-    if (ep.y_f32)
+    if (tma) {
+      uint32_t w[16];
+      pack_words16<false>(v, w);
+      tma_store_rows32(ss, &ep.tm_out0, row - int(threadIdx.x & 31), col0, ep.M, w);
+    } else if (ep.y_f32) {
       store_row32_f32(static_cast<float*>(ep.y) + off, v);
-    else
+    } else {
       store_row32<false>(static_cast<__nv_bfloat16*>(ep.y) + off, v);
+    }
   }
 }
 
@@ -499,7 +564,8 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
 template <int KIND, int OP, int LAYOUT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                int K, const EpiParams ep, const SkParams sk, int* status, uint64_t limit_ns) {
+                int K, const __grid_constant__ EpiParams ep, const SkParams sk, int* status,
+                uint64_t limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -681,6 +747,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t quad = warp & 3;
     float* epi_stage = reinterpret_cast<float*>(smem + EPI_STAGE_OFF) +
                        (warp - 2) * 32 * STAGE_PITCH;
+    // the same area as two 2 KB TMA-store buffers per warp (forward kinds only)
+    StoreStage ss{smem_u32(smem + EPI_STAGE_OFF) + (warp - 2) * 4096u, 0u};
     int acc = 0;
     uint32_t acc_par = 0;
     UnitIter ui(sc);
@@ -769,7 +837,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (KIND == kEpiGrad)
             grad_store_warp(ep, row - int(lane), col0, v, epi_stage);
           else
-            epilogue32<KIND>(ep, row, col0, v);
+            epilogue32<KIND>(ep, row, col0, v, ss);
         }
         // Each flag has exactly one reader, this warp: clear what it consumed, so the
         // flags are zero again when the launch ends. A later launch that carries the same
@@ -791,6 +859,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_par ^= 1;
     }
+    // the warp's TMA stores must have read their buffers, and landed, before the CTA ends
+    if (ss.n > 0 && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -70,6 +70,14 @@ enum EpiKind : int {
 enum GemmLayout : int { kKK = 0, kMK = 1, kKM = 2, kMM = 3 };
 
 struct EpiParams {
+  // TMA stores of the 16-bit row-major outputs (tma_store): kEpiBlockIn writes q|k through
+  // tm_out0 ([T, 2H]) and GeLU(h) through tm_out1 ([T, H + F]), kEpiResidual writes y
+  // through tm_out0 ([T, N]); boxes of 32 columns x 32 rows, 64-byte swizzle. Each
+  // epilogue warp stages its 32 x 32 chunk in shared memory and one lane issues the copy,
+  // so the stores leave the load/store path the main loop's operand traffic uses.
+  alignas(64) CUtensorMap tm_out0;
+  alignas(64) CUtensorMap tm_out1;
+  bool tma_store;
   int M, N;
   int* status;  // device status word (fp16 range errors), may be null
   // kEpiStore

@@ -305,6 +305,25 @@ pb_status make_map_f32(CUtensorMap* m, const void* base, int rank, const uint64_
   return PB_OK;
 }
 
+// Row-major [rows, cols] 16-bit output (bf16, or fp16 when f16) written by the GEMM
+// epilogues' TMA stores: boxes of 32 columns x 32 rows with 64-byte swizzle (one epilogue
+// warp's chunk).
+pb_status make_store_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                         uint64_t ld, bool f16) {
+  EncodeTiledFn enc;
+  pb_status s = get_encoder(&enc);
+  if (s != PB_OK) return s;
+  const cuuint64_t gd[2] = {cols, rows};
+  const cuuint64_t gs[1] = {ld * 2};
+  const cuuint32_t bx[2] = {32, 32}, es[2] = {1, 1};
+  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return PB_OK;
+}
+
 // Row-major [rows, cols] matrix of element type t read in boxes of 128 bytes of columns
 // (64 16-bit or 128 FP8 elements) x box_rows rows.
 pb_status make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -404,6 +423,12 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
     e1.scale_b = h->w1scale;
   }
   if (train) e1.hpre = reinterpret_cast<__nv_bfloat16*>(scratch + L.hpre);
+  if (!glu) {  // q|k and GeLU(h) by TMA stores (SwiGLU's 16-column outputs stay row stores)
+    s = make_store_map(&e1.tm_out0, qk, T, 2 * uint64_t(H), 2 * uint64_t(H), false);
+    if (s == PB_OK) s = make_store_map(&e1.tm_out1, act, T, uint64_t(H + F), uint64_t(H + F), h->f16);
+    if (s != PB_OK) return s;
+    e1.tma_store = true;
+  }
   PB_CUDA(pb::launch_gemm(pb::kEpiBlockIn, h->gop, tm_xn, h->tm_w1cat, T, int(w1_rows(d)), H,
                           e1, h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),
           "first GEMM launch");
@@ -454,6 +479,11 @@ pb_status run_block(pb_handle* h, const void* x, bool x_f32, void* y, bool y_f32
   if (h->fp8) {
     e2.scale_a = qscale + T;
     e2.scale_b = h->w2scale;
+  }
+  if (!y_f32) {  // bf16 y by TMA stores
+    s = make_store_map(&e2.tm_out0, y, T, uint64_t(H), uint64_t(H), false);
+    if (s != PB_OK) return s;
+    e2.tma_store = true;
   }
   PB_CUDA(pb::launch_gemm(pb::kEpiResidual, h->gop, tm_act, h->tm_w2cat, T, H, H + F, e2,
                           h->num_sms, h->status, h->limit_ns, scratch + L.sk, st),

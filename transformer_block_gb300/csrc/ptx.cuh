@@ -205,6 +205,22 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// TMA store of the box at `src` (this CTA's shared memory, laid out as the tensor map's
+// box) to the global tensor at coordinates (c0, c1); parts of the box outside the tensor
+// are skipped. Asynchronous, in the thread's bulk group: the source may be reused after
+// bulk_wait_read*().
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+// Waits until at most one committed bulk group of this thread still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
