@@ -75,8 +75,8 @@ struct EpiParams {
   // through tm_out0 ([T, N]); boxes of 32 columns x 32 rows, 64-byte swizzle. Each
   // epilogue warp stages its 32 x 32 chunk in shared memory and one lane issues the copy,
   // so the stores leave the load/store path the main loop's operand traffic uses.
-  alignas(64) CUtensorMap tm_out0;
-  alignas(64) CUtensorMap tm_out1;
+  CUtensorMap tm_out0;  // the type carries the alignment TMA needs
+  CUtensorMap tm_out1;
   bool tma_store;
   int M, N;
   int* status;  // device status word (fp16 range errors), may be null
