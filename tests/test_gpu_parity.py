@@ -98,7 +98,38 @@ def test_stream_k_leaves_its_flags_cleared():
     assert not torch.equal(c2, d2)
 
 
-@pytest.mark.parametrize("rows,H", [(37, 256), (7, 128), (9, 384), (5, 2048), (300, 4096), (3, 12288),
+def test_stream_k_gemms_on_two_streams_at_once():
+    # Distinct scratch buffers make concurrent calls independent: two streams issue
+    # stream-K GEMMs back to back, and every result equals the same call made alone.
+    # A stream-K owner waits (boundedly) for its contributor pairs; a launch that could
+    # never get them resident would end with a timeout status, checked here.
+    M, N, K = 2048, 12288, 4096
+    g = torch.Generator(device="cuda").manual_seed(13)
+    A = [torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16) for _ in range(2)]
+    B = [torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16) for _ in range(2)]
+    scr = [torch.zeros(pb.gemm_scratch_bytes(), dtype=torch.uint8, device="cuda")
+           for _ in range(2)]
+    status = [torch.zeros(1, dtype=torch.int32, device="cuda") for _ in range(2)]
+    ref = [pb.gemm(A[i], B[i], scratch=scr[i]) for i in range(2)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [[torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+            for _ in range(2)]
+    for it in range(8):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                pb.gemm(A[i], B[i], out=outs[i][it], scratch=scr[i], status=status[i],
+                        stream=streams[i])
+    torch.cuda.synchronize()
+    assert [int(s.item()) for s in status] == [0, 0]
+    for i in range(2):
+        for it in range(8):
+            assert torch.equal(outs[i][it], ref[i]), f"stream {i}, call {it}"
+
+
+@pytest.mark.parametrize("rows,H",[(37, 256), (7, 128), (9, 384), (5, 2048), (300, 4096), (3, 12288),
                                     (64, 16384)])
 def test_layernorm_matches_oracle(rows, H):
     g = torch.Generator(device="cuda").manual_seed(rows + H)
