@@ -227,7 +227,8 @@ pb_status pb_forward(pb_handle* h, const void* x, void* y, void* scratch, size_t
  * backward reads: h before its activation and each attention row's log-sum-exp. The
  * attention probabilities are not kept; pb_backward recomputes them (the selective
  * recomputation of the MegaScale reading notes, section 1.3). Supported: bf16 operands
- * (PB_OPERANDS_BF16) and head_dim 128; otherwise PB_ERR_UNSUPPORTED.
+ * (PB_OPERANDS_BF16), head_dim 64 or 128; other operand precisions give
+ * PB_ERR_UNSUPPORTED.
  * ---------------------------------------------------------------------------------- */
 
 /* Bytes of the training scratch of pb_forward_train / pb_backward (train_total). */

@@ -188,7 +188,7 @@ def test_stack_and_host_paths_stay_inside_their_regions(w):
     assert torch.equal(yh, y.cpu())
 
 
-@pytest.mark.parametrize("w", RAGGED_DH128, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", RAGGED + [RAGGED_DH128[1], RAGGED_DH128[3]], ids=lambda w: w.name)
 def test_backward_writes_stay_inside_their_regions(w):
     dims = pb.make_dims(w)
     x, params = inputs.make_layer(w, 0, device="cuda", biases=True)

@@ -769,7 +769,6 @@ pb_status run_backward(pb_handle* h, const void* x, const void* dy, const pb_gra
 pb_status check_train(pb_handle* h) {
   if (h->f16 || h->fp8)
     return fail(PB_ERR_UNSUPPORTED, "training needs PB_OPERANDS_BF16 operands");
-  if (h->d.head_dim != 128) return fail(PB_ERR_UNSUPPORTED, "training needs head_dim 128");
   return PB_OK;
 }
 

@@ -18,7 +18,8 @@
 //   dP^T = V dO^T       (A = V, MN-major from v^T)                  buffer b, columns 64-127
 //   P and dS warps: P^T and dS^T (bf16) over S^T and dP^T, dS into shared memory (b)
 //   dV  += P^T dO,  dK += dS^T Q   (A from tensor memory, B = dO and Q read MN-major)
-//   dQ^T = K^T dS       (M = dh, N = 64 queries; both operands MN-major) over buffer b
+//   dQ^T = K^T dS       (M = 128 head dims, N = 64 queries; both operands MN-major) over
+//                       buffer b; with dh = 64 the upper 64 rows of K^T are a zero box
 //   dQ warps: dQ^T out, each warp's 32 head dims x 64 queries staged in shared memory and
 //             added into the fp32 dq accumulator in global memory by one TMA reduction
 //             (other key tiles add theirs)
@@ -33,7 +34,8 @@
 //   warp 1     tensor-memory owner and the MMA-issuing thread
 //   warps 2-5  P and dS, one key per thread (its TMEM lane)
 //   warps 6-9  dQ per step, then the dK and dV rows of the tile
-// Tensor memory: buffer 0 [0, 128) | buffer 1 [128, 256) | dV [256, 384) | dK [384, 512).
+// Tensor memory: buffer 0 [0, 128) | buffer 1 [128, 256) | dV [256, 256 + dh) |
+// dK [384, 384 + dh). Head sizes 64 and 128.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -42,31 +44,40 @@ namespace {
 
 constexpr int BKV = 128;  // keys per CTA
 constexpr int BQ = 64;    // queries per step
-constexpr int DH = 128;   // head dim
 constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_BUF = 128, T_DP = 64, T_DV = 256, T_DK = 384;
 constexpr int K_BOX = BKV * 64 * 2;   // 16 KB: 128 keys x 64 dims
-constexpr int K_BYTES = 2 * K_BOX;
-constexpr int V_HALF = DH * 64 * 2;   // 16 KB: dh rows x 64 keys (from v^T)
-constexpr int V_BYTES = 2 * V_HALF;
+constexpr int K_BYTES = 2 * K_BOX;    // two boxes whatever the head size (see below)
 constexpr int QD_BOX = BQ * 64 * 2;   // 8 KB: 64 queries x 64 dims
-constexpr int Q_BYTES = 2 * QD_BOX;
 constexpr int ROWVAL_BYTES = BQ * 4;  // 64 fp32 values of L or D
-constexpr int STAGE_TX = 2 * Q_BYTES + 2 * ROWVAL_BYTES;  // Q, dO, L, D
-constexpr int STAGE_BYTES = 2 * Q_BYTES + 1024;           // next stage 1024-aligned
 constexpr int STAGES = 2;
 constexpr int DS_BYTES = BKV * BQ * 2;  // dS: 128 key rows x 64 queries
-constexpr int K_OFF = 0, V_OFF = K_BYTES, ST_OFF = V_OFF + V_BYTES;
-constexpr int DS_OFF = ST_OFF + STAGES * STAGE_BYTES;
 constexpr int DQ_WARP_BYTES = 32 * BQ * 4;  // a dQ warp's staging: 64 queries x 32 dims fp32
-constexpr int DQ_OFF = DS_OFF + 2 * DS_BYTES;
-constexpr int BAR_OFF = DQ_OFF + 4 * DQ_WARP_BYTES;
 // kv_full, q_full[2], q_empty[2], s_full[2], p_full[2], mma_done[2], dq_free[2], drain
 constexpr int NUM_BARS = 14;
-constexpr size_t SMEM = size_t(BAR_OFF) + NUM_BARS * 8 + 16 + 1024;
-static_assert(SMEM <= 227 * 1024 && 2 * SMEM > 228 * 1024,
-              "one CTA per SM: it takes all tensor-memory columns");
+
+// Shared-memory layout for head size DH (64 or 128). K always takes two 64-dim boxes: with
+// DH = 64 the second is zero, so dQ^T = K^T dS stays an M = 128 product whose rows 64-127
+// are zero (the dQ warps of those rows skip their reductions).
+template <int DH>
+struct BwdLayout {
+  static_assert(DH == 64 || DH == 128, "head size");
+  static constexpr int K_TX = (DH / 64) * K_BOX;  // bytes the K load brings
+  static constexpr int V_HALF = DH * 64 * 2;      // dh rows x 64 keys (from v^T)
+  static constexpr int V_BYTES = 2 * V_HALF;
+  static constexpr int Q_BYTES = (DH / 64) * QD_BOX;
+  static constexpr int STAGE_TX = 2 * Q_BYTES + 2 * ROWVAL_BYTES;  // Q, dO, L, D
+  static constexpr int STAGE_BYTES = 2 * Q_BYTES + 1024;           // next stage 1024-aligned
+  static constexpr int K_OFF = 0, V_OFF = K_BYTES, ST_OFF = V_OFF + V_BYTES;
+  static constexpr int DS_OFF = ST_OFF + STAGES * STAGE_BYTES;
+  static constexpr int DQ_OFF = DS_OFF + 2 * DS_BYTES;
+  static constexpr int BAR_OFF = DQ_OFF + 4 * DQ_WARP_BYTES;
+  static constexpr size_t NEED = size_t(BAR_OFF) + NUM_BARS * 8 + 16 + 1024;
+  // one CTA per SM: it takes all tensor-memory columns
+  static constexpr size_t SMEM = NEED > 120 * 1024 ? NEED : 120 * 1024;
+  static_assert(SMEM <= 227 * 1024 && 2 * SMEM > 228 * 1024, "shared memory layout");
+};
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   uint32_t u[64];
@@ -85,12 +96,18 @@ __device__ __forceinline__ int num_steps(const SwaBwdParams& p, int j0) {
   return last / BQ - j0 / BQ + 1;
 }
 
+template <int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     swa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVT,
                    const __grid_constant__ CUtensorMap tmDO,
                    const __grid_constant__ CUtensorMap tmDQ, const SwaBwdParams p, int* status,
                    uint64_t limit_ns) {
+  using Lb = BwdLayout<DH>;
+  constexpr int K_TX = Lb::K_TX, V_HALF = Lb::V_HALF, V_BYTES = Lb::V_BYTES;
+  constexpr int Q_BYTES = Lb::Q_BYTES, STAGE_TX = Lb::STAGE_TX, STAGE_BYTES = Lb::STAGE_BYTES;
+  constexpr int K_OFF = Lb::K_OFF, V_OFF = Lb::V_OFF, ST_OFF = Lb::ST_OFF;
+  constexpr int DS_OFF = Lb::DS_OFF, DQ_OFF = Lb::DQ_OFF, BAR_OFF = Lb::BAR_OFF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -131,6 +148,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (DH == 64) {
+    // the second K box: zero rows of K^T for the M = 128 dQ^T product
+    uint4* kz = reinterpret_cast<uint4*>(smem + K_OFF + K_BOX);
+    for (int e = int(threadIdx.x); e < K_BOX / 16; e += THREADS) kz[e] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
@@ -154,12 +177,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ producer
-      mbar_arrive_expect_tx(kv_full, K_BYTES + V_BYTES);
+      mbar_arrive_expect_tx(kv_full, K_TX + V_BYTES);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < DH / 64; ++c)
         tma_load_3d(sK + c * K_BOX, &tmK, kv_full, p.H + head * DH + 64 * c, j0, b);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)  // two halves of 64 keys
         tma_load_2d(sV + c * V_HALF, &tmVT, kv_full, j0 + 64 * c, (b * p.nh + head) * DH);
-      }
       int issued = 0;
       for (int n = 0; n < N; ++n) {
         const int st = n & 1;
@@ -168,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int i0 = j0 + n * BQ;
         mbar_arrive_expect_tx(bar, STAGE_TX);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < DH / 64; ++c) {
           tma_load_3d(dst + c * QD_BOX, &tmQ, bar, head * DH + 64 * c, i0, b);
           tma_load_3d(dst + Q_BYTES + c * QD_BOX, &tmDO, bar, head * DH + 64 * c, i0, b);
         }
@@ -188,7 +212,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t id_s = idesc_f32acc(BKV, BQ);                        // K, Q K-major
       const uint32_t id_dp = idesc_f32acc(BKV, BQ, false, true, false);   // V MN-major
       const uint32_t id_acc = idesc_f32acc(BKV, DH, false, false, true);  // TMEM A, B MN
-      const uint32_t id_dq = idesc_f32acc(DH, BQ, false, true, true);     // both MN-major
+      // dQ^T: M = the two 64-dim K boxes (the second zero when DH = 64), both MN-major
+      const uint32_t id_dq = idesc_f32acc(128, BQ, false, true, true);
       const uint64_t dK = sdesc_kmajor_sw128(sK), dKmn = sdesc_mnmajor_sw128(sK, K_BOX);
       const uint64_t dVmn = sdesc_mnmajor_sw128(sV, V_HALF);
       // S^T and dP^T of step n into buffer n % 2 (its Q / dO stage is n % 2 too)
@@ -350,6 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free0 + 8 * bf);
+      if (int(quad) * 32 >= DH) continue;  // rows of the zero K box (DH = 64)
       const int i0 = j0 + n * BQ;
       // the warp's [64 queries][32 dims] block of dQ into its staging buffer (once the
       // previous step's reduction has read it), then one TMA add into dq (rows past the
@@ -405,16 +431,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-}  // namespace
 
-cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmVT, const CUtensorMap& tmDO,
-                           const CUtensorMap& tmDQ, const SwaBwdParams& p, int* status,
-                           uint64_t limit_ns, cudaStream_t stream) {
-  if (p.dh != DH || p.lse_ld % BQ != 0 || p.lse_ld < p.S) return cudaErrorInvalidValue;
+template <int DH>
+cudaError_t launch_dh(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmVT,
+                      const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const SwaBwdParams& p,
+                      int* status, uint64_t limit_ns, cudaStream_t stream) {
+  constexpr size_t SMEM = BwdLayout<DH>::SMEM;
   static PerDeviceInit setup;  // per device: the shared-memory opt-in
   const cudaError_t attr = per_device_init(setup, [](int, int*) {
-    return cudaFuncSetAttribute(swa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(swa_bwd_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 int(SMEM));
   });
   if (attr != cudaSuccess) return attr;
@@ -422,9 +447,21 @@ cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   const int64_t grid = tiles * p.nh * p.B;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  swa_bwd_kernel<<<unsigned(grid), THREADS, SMEM, stream>>>(tmQ, tmK, tmVT, tmDO, tmDQ, p,
-                                                             status, limit_ns);
+  swa_bwd_kernel<DH><<<unsigned(grid), THREADS, SMEM, stream>>>(tmQ, tmK, tmVT, tmDO, tmDQ, p,
+                                                                 status, limit_ns);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_swa_bwd(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmVT, const CUtensorMap& tmDO,
+                           const CUtensorMap& tmDQ, const SwaBwdParams& p, int* status,
+                           uint64_t limit_ns, cudaStream_t stream) {
+  if (p.lse_ld % BQ != 0 || p.lse_ld < p.S) return cudaErrorInvalidValue;
+  if (p.dh == 64) return launch_dh<64>(tmQ, tmK, tmVT, tmDO, tmDQ, p, status, limit_ns, stream);
+  if (p.dh == 128) return launch_dh<128>(tmQ, tmK, tmVT, tmDO, tmDQ, p, status, limit_ns, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pb
