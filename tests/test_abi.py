@@ -29,6 +29,37 @@ def test_header_declares_the_api():
         assert required in names
 
 
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    # A C program (not C++) that includes the header and calls into the library: the
+    # declarations are C, and the exported names link without C++ mangling.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_pb.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "pb.h"\n'
+        "int main(void) {\n"
+        "  pb_dims d = {1, 128, 256, 4, 64, 1024, 32, 1e-5f, PB_BLOCK_LN_GELU};\n"
+        "  size_t ws = 0, scr = 0;\n"
+        "  if (pb_weight_workspace_bytes(&d, &ws) != PB_OK) return 1;\n"
+        "  if (pb_scratch_bytes(&d, &scr) != PB_OK) return 2;\n"
+        "  d.head_dim = 96;\n  d.hidden = 384;\n"
+        "  if (pb_scratch_bytes(&d, &scr) != PB_ERR_UNSUPPORTED) return 3;\n"
+        '  printf("%zu %zu %s\\n", ws, scr, pb_status_string(PB_ERR_UNSUPPORTED));\n'
+        "  return 0;\n}\n")
+    exe = tmp_path / "use_pb"
+    libdir = os.path.dirname(pb.library_path())
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lpb", "-Wl,-rpath," + libdir],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == pb.weight_workspace_bytes(pb.make_dims(
+        batch=1, seq=128, hidden=256, heads=4, head_dim=64, ffn=1024, window=32))
+    assert out[2] == "PB_ERR_UNSUPPORTED"
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
