@@ -45,10 +45,14 @@ def test_gemm_matches_oracle(M, N, K):
     assert_parity(host(c), ref, f"gemm {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 12288, 1024), (4160, 2080, 512), (256 * 77, 256, 640)])
+@pytest.mark.parametrize("M,N,K", [(2048, 12288, 1024), (4160, 2080, 512),
+                                   (256 * 77, 256, 640), (4096, 5120, 16384),
+                                   (4160, 2560, 16384)])
 def test_gemm_stream_k_matches_oracle(M, N, K):
-    # Tile counts that leave a partial last wave on 76 CTA pairs, so the last waves are
-    # split along K (stream-K) when scratch is given; without scratch every tile is whole.
+    # Unit counts that leave a partial last wave on 76 CTA pairs, so the last units are
+    # split along K (stream-K) when scratch is given; without scratch every unit is whole.
+    # K >= 16384 with M > 256: units of two 256-row tiles, the leftover units split into
+    # their tiles (4160 rows: a ragged last unit whose second tile is empty).
     g = torch.Generator(device="cuda").manual_seed(M + N + K)
     a = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
     b = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
@@ -129,8 +133,8 @@ def test_stream_k_gemms_on_two_streams_at_once():
             assert torch.equal(outs[i][it], ref[i]), f"stream {i}, call {it}"
 
 
-@pytest.mark.parametrize("rows,H",[(37, 256), (7, 128), (9, 384), (5, 2048), (300, 4096), (3, 12288),
-                                    (64, 16384)])
+@pytest.mark.parametrize("rows,H", [(37, 256), (7, 128), (9, 384), (5, 2048), (300, 4096),
+                                    (3, 12288), (64, 16384)])
 def test_layernorm_matches_oracle(rows, H):
     g = torch.Generator(device="cuda").manual_seed(rows + H)
     x = (torch.randn(rows, H, generator=g, device="cuda") * 2 + 0.5).to(torch.bfloat16)

@@ -34,22 +34,32 @@ constexpr int BM = kGemmBM;       // output rows per CTA
 constexpr int PM = 2 * kGemmBM;   // output rows per CTA pair
 constexpr int BN = kGemmBN;       // output columns per pair tile
 constexpr int BK = kGemmBK;
-constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's rows of A
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's rows of A (one M tile)
 constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of B
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 2 * STAGES + 5;
 // Per epilogue warp, a 32 x 32 fp32 chunk (rows padded to 33 words: conflict-free both
 // ways) for the coalesced gradient stores.
 constexpr int STAGE_PITCH = 33;
-// 1024-byte aligned: the forward epilogues' TMA-store buffers (64-byte swizzle) live here
-constexpr size_t EPI_STAGE_OFF =
-    (size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16 + 1023) / 1024 * 1024;
-constexpr size_t SMEM_BYTES = 1024 + EPI_STAGE_OFF + 4 * 32 * STAGE_PITCH * 4;
 static_assert(4 * 32 * STAGE_PITCH * 4 >= 4 * 4096, "four warps' two 2 KB store buffers");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of the GEMM");
+
+// Shared-memory geometry for MT 256-row M tiles per CTA pair and work unit. MT = 1: a
+// 256 x 256 tile, six stages of A and B, the accumulator double-buffered in tensor memory
+// (2 x 256 columns). MT = 2: a 512 x 256 unit whose two M tiles share every B stage (a
+// quarter less operand traffic per FLOP), four stages of two A tiles and B, one 256-column
+// accumulator per M tile (not double-buffered).
+template <int MT>
+struct Geo {
+  static_assert(MT == 1 || MT == 2, "one or two M tiles per unit");
+  static constexpr int STAGES = MT == 2 ? 4 : 6;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  // 1024-byte aligned: the forward epilogues' TMA-store buffers (64-byte swizzle) live here
+  static constexpr size_t EPI_STAGE_OFF =
+      (size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16 + 1023) / 1024 * 1024;
+  static constexpr size_t SMEM_BYTES = 1024 + EPI_STAGE_OFF + 4 * 32 * STAGE_PITCH * 4;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of the GEMM");
+};
 
 __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
@@ -494,13 +504,15 @@ __device__ __forceinline__ void grad_store_warp(const EpiParams& ep, int row0, i
   __syncwarp();
 }
 
-// The work of one CTA pair: first whole tiles t = cluster, cluster + clusters, ... below
-// dp_tiles, then its contiguous share [cluster * W, (cluster + 1) * W) of the linearised
-// (tile, k-block) iterations of the sk_tiles stream-K tiles that follow them.
+// The work of one CTA pair: first whole units t = cluster, cluster + clusters, ... below
+// dp_tiles (a unit is mt M tiles of 256 rows by 256 columns), then its contiguous share
+// [cluster * W, (cluster + 1) * W) of the linearised (tile, k-block) iterations of the
+// sk_tiles stream-K tiles that follow them: the 256-row M tiles of the remaining units.
 struct Sched {
-  int num_m, num_n, num_kb;
+  int num_m, num_n, num_kb;  // num_m counts units of mt x 256 rows
   int cluster, clusters;
   int dp_tiles, sk_tiles, W;
+  int mt, group;             // M tiles per unit; units per rasterisation group
 };
 
 struct SkParams {
@@ -511,19 +523,23 @@ struct SkParams {
 };
 
 struct Unit {
-  int tile, kb0, kb1;
+  int row0, tn;  // first row (of the pair) and column block
+  int mt;        // M tiles in this unit (a stream-K tile has one)
+  int ts;        // stream-K tile index, -1 for a whole unit
+  int kb0, kb1;
 };
 
-// Tile index -> (pair-row block, column block). Tiles are ordered in groups of kGroupM
-// pair-rows, M fastest inside a group, so the CTA pairs running at the same time cover a
-// compact block of about kGroupM x (pairs / kGroupM) tiles and share both their A rows
-// and their B columns in L2.
+// Unit index -> (unit row block, column block). Units are ordered in groups of `group`
+// row blocks (kGroupM pair-rows of 256 in all), M fastest inside a group, so the CTA pairs
+// running at the same time cover a compact block of about 2048 rows x (pairs / group)
+// columns and share both their A rows and their B columns in L2.
 constexpr int kGroupM = 8;
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m, int& n) {
-  const int per_group = kGroupM * num_n;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group, int& m,
+                                            int& n) {
+  const int per_group = group * num_n;
   const int g = tile / per_group;
-  const int first_m = g * kGroupM;
-  const int gm = min(kGroupM, num_m - first_m);
+  const int first_m = g * group;
+  const int gm = min(group, num_m - first_m);
   const int r = tile - g * per_group;
   m = first_m + r % gm;
   n = r / gm;
@@ -537,8 +553,10 @@ struct UnitIter {
         it(int64_t(s.cluster) * s.W),
         it_end(min(int64_t(s.cluster + 1) * s.W, int64_t(s.sk_tiles) * s.num_kb)) {}
   __device__ bool next(const Sched& s, Unit& u) {
+    int tm, tn;
     if (t < s.dp_tiles) {
-      u = Unit{t, 0, s.num_kb};
+      tile_coords(t, s.num_m, s.num_n, s.group, tm, tn);
+      u = Unit{tm * s.mt * 2 * kGemmBM, tn, s.mt, -1, 0, s.num_kb};
       t += s.clusters;
       return true;
     }
@@ -546,7 +564,8 @@ struct UnitIter {
     const int ts = int(it / s.num_kb);
     const int kb0 = int(it - int64_t(ts) * s.num_kb);
     const int kb1 = int(min(int64_t(s.num_kb), int64_t(kb0) + (it_end - it)));
-    u = Unit{s.dp_tiles + ts, kb0, kb1};
+    tile_coords(s.dp_tiles + ts / s.mt, s.num_m, s.num_n, s.group, tm, tn);
+    u = Unit{(tm * s.mt + ts % s.mt) * 2 * kGemmBM, tn, 1, ts, kb0, kb1};
     it += kb1 - kb0;
     return true;
   }
@@ -561,11 +580,15 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-template <int KIND, int OP, int LAYOUT>
+template <int KIND, int OP, int LAYOUT, int MT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int K, const __grid_constant__ EpiParams ep, const SkParams sk, int* status,
                 uint64_t limit_ns) {
+  static_assert(MT == 1 || LAYOUT == kKK, "two M tiles per unit: K-major operands only");
+  constexpr int STAGES = Geo<MT>::STAGES, STAGE_BYTES = Geo<MT>::STAGE_BYTES;
+  constexpr int NUM_BARS = Geo<MT>::NUM_BARS;
+  constexpr size_t EPI_STAGE_OFF = Geo<MT>::EPI_STAGE_OFF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -615,8 +638,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint64_t drain_ns = limit_ns > kDrainFloorNs ? limit_ns : kDrainFloorNs;
 
   Sched sc;
-  sc.num_m = (ep.M + PM - 1) / PM;
+  sc.num_m = (ep.M + MT * PM - 1) / (MT * PM);
   sc.num_n = (ep.N + BN - 1) / BN;
+  sc.mt = MT;
+  sc.group = kGroupM / MT;
   constexpr int BKE = OP == kOpE4m3 ? kGemmBK8 : BK;  // K elements per stage (128 bytes)
   constexpr bool AMN = (LAYOUT & kMK) != 0, BMN = (LAYOUT & kKM) != 0;
   static_assert(!(AMN || BMN) || OP != kOpE4m3, "MN-major operands are 16-bit");
@@ -626,7 +651,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   sc.dp_tiles = sk.dp_tiles;
   sc.sk_tiles = sk.sk_tiles;
   sc.W = sk.W;
-  const int num_m = sc.num_m;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -641,10 +665,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       UnitIter ui(sc);
       Unit u;
       while (ok && ui.next(sc, u)) {
-        int tm, tn;
-        tile_coords(u.tile, num_m, sc.num_n, tm, tn);
-        const int m0 = tm * PM + int(rank) * BM;
-        const int n0 = tn * BN + int(rank) * (BN / 2);
+        const int m0 = u.row0 + int(rank) * BM;
+        const int n0 = u.tn * BN + int(rank) * (BN / 2);
+        const uint32_t stage_tx = 2u * uint32_t(u.mt * A_BYTES + B_BYTES);  // both CTAs
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, wc, 1)) {
             ok = false;
@@ -655,21 +678,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           // drive the transaction count below zero, and the phase cannot complete without
           // its arrival. The odd CTA reuses a stage only after the pair's MMAs read it, so
           // its copies always count toward the phase the MMA issuer waits for next.
-          if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, stage_tx);
           // K-major: one box of 128 rows x 64 K; MN-major: two boxes of 64 K-rows x 64
           // elements of M (or N), 8 KB apart
           if (AMN) {
             tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, m0, kb * BKE);
             tma_load_2d_pair(sa + A_BYTES / 2, &tmA, full_pair0 + 8 * stage, m0 + 64, kb * BKE);
           } else {
-            tma_load_2d_pair(sa, &tmA, full_pair0 + 8 * stage, kb * BKE, m0);
+            // MT = 2: the unit's second M tile 256 rows below, in the stage's second A slot
+            for (int g = 0; g < u.mt; ++g)
+              tma_load_2d_pair(sa + g * A_BYTES, &tmA, full_pair0 + 8 * stage, kb * BKE,
+                               m0 + g * PM);
           }
           if (BMN) {
             tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, n0, kb * BKE);
             tma_load_2d_pair(sa + A_BYTES + B_BYTES / 2, &tmB, full_pair0 + 8 * stage, n0 + 64,
                              kb * BKE);
           } else {
-            tma_load_2d_pair(sa + A_BYTES, &tmB, full_pair0 + 8 * stage, kb * BKE, n0);
+            tma_load_2d_pair(sa + MT * A_BYTES, &tmB, full_pair0 + 8 * stage, kb * BKE, n0);
           }
           last_par[stage] = phase;
           used |= 1u << stage;
@@ -703,6 +729,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       while (ok && ui.next(sc, u)) {
         if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1, wc, 2)) break;
         tc_fence_after();
+        // MT = 1: accumulator acc of two; MT = 2: M tile g in columns [g * BN, (g + 1) * BN)
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, wc, 3)) {
@@ -714,16 +741,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t da =
               AMN ? sdesc_mnmajor_sw128(sa, A_BYTES / 2) : sdesc_kmajor_sw128(sa);
           const uint64_t db = BMN ? sdesc_mnmajor_sw128(sa + A_BYTES, B_BYTES / 2)
-                                  : sdesc_kmajor_sw128(sa + A_BYTES);
-          // four products of 32 bytes of K each: K = 16 (16-bit) or 32 (FP8) elements
+                                  : sdesc_kmajor_sw128(sa + MT * A_BYTES);
+          // four products of 32 bytes of K each: K = 16 (16-bit) or 32 (FP8) elements; with
+          // MT = 2 each M tile's A slot against the shared B
+          for (int g = 0; g < u.mt; ++g) {
+            const uint32_t dt = MT == 2 ? tmem_base + uint32_t(g * BN) : d_tmem;
+            const uint64_t dag = da + uint64_t((g * A_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (OP == kOpE4m3)
-              mma_f8kind_ss_pair(d_tmem, da + kStepA * k, db + kStepB * k, idesc,
-                                 (kb > u.kb0) || k > 0);
-            else
-              mma_f16kind_ss_pair(d_tmem, da + kStepA * k, db + kStepB * k, idesc,
-                                  (kb > u.kb0) || k > 0);
+            for (int k = 0; k < 4; ++k) {
+              if (OP == kOpE4m3)
+                mma_f8kind_ss_pair(dt, dag + kStepA * k, db + kStepB * k, idesc,
+                                   (kb > u.kb0) || k > 0);
+              else
+                mma_f16kind_ss_pair(dt, dag + kStepA * k, db + kStepB * k, idesc,
+                                    (kb > u.kb0) || k > 0);
+            }
           }
           mma_commit_pair(empty0 + 8 * stage, 0x3);
           if (++stage == STAGES) {
@@ -733,8 +765,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) break;
         mma_commit_pair(tfull0 + 8 * acc, 0x3);
-        acc ^= 1;
-        if (acc == 0) acc_par ^= 1;
+        if (MT == 1) {
+          acc ^= 1;
+          if (acc == 0) acc_par ^= 1;
+        } else {
+          acc_par ^= 1;  // one accumulator set
+        }
       }
       // Every MMA this thread issued (into both CTAs' tensor memory) must finish before
       // either CTA releases it.
@@ -757,96 +793,94 @@ __global__ void __launch_bounds__(THREADS, 1)
     while (ok && ui.next(sc, u)) {
       if (!mbar_wait_warp(tfull0 + 8 * acc, acc_par, wc, 4)) break;
       tc_fence_after();
-      int tm, tn;
-      tile_coords(u.tile, num_m, sc.num_n, tm, tn);
-      const int m0 = tm * PM + int(rank) * BM, n0 = tn * BN;
-      const int row = m0 + int(quad * 32 + lane);
-      const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + uint32_t(acc * BN);
-      // This thread's row of a pair's partial tile ([2][128][256] fp32 per cluster).
-      const size_t part_off = (size_t(rank) * 128 + quad * 32 + lane) * BN;
-      if (u.kb0 > 0) {
-        // A K segment that does not start at 0: leave the partial sums for the pair that
-        // owns k-block 0 of this tile, then publish them (one flag per warp).
-        float* dst = sk.partials + size_t(sc.cluster) * (2 * 128 * BN) + part_off;
+      for (int g = 0; g < u.mt; ++g) {  // MT = 2: the unit's two M tiles, one after the other
+        const int m0 = u.row0 + g * PM + int(rank) * BM, n0 = u.tn * BN;
+        const int row = m0 + int(quad * 32 + lane);
+        const uint32_t taddr =
+            tmem_base + ((quad * 32u) << 16) + uint32_t((MT == 2 ? g : acc) * BN);
+        // This thread's row of a pair's partial tile ([2][128][256] fp32 per cluster).
+        const size_t part_off = (size_t(rank) * 128 + quad * 32 + lane) * BN;
+        if (u.kb0 > 0) {
+          // A K segment that does not start at 0: leave the partial sums for the pair that
+          // owns k-block 0 of this tile, then publish them (one flag per warp).
+          float* dst = sk.partials + size_t(sc.cluster) * (2 * 128 * BN) + part_off;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(taddr + uint32_t(c * 32), r);
-          tmem_ld_wait(r);
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + uint32_t(c * 32), r);
+            tmem_ld_wait(r);
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            __stcg(d4 + q, make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                       __uint_as_float(r[4 * q + 2]),
-                                       __uint_as_float(r[4 * q + 3])));
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0)
-          st_release_u64(sk.flags + (size_t(sc.cluster) * 2 + rank) * 4 + quad, sk.epoch);
-      } else {
-        // K segment from 0: this pair finishes the tile. For a stream-K tile, the pairs
-        // cluster+1 .. last computed its other K segments; wait for their partials.
-        int last = sc.cluster;
-        if (u.tile >= sc.dp_tiles) {
-          const int64_t ts = u.tile - sc.dp_tiles;
-          last = int(((ts + 1) * sc.num_kb - 1) / sc.W);
-        }
-        for (int c2 = sc.cluster + 1; ok && c2 <= last; ++c2) {
-          const uint64_t* f = sk.flags + (size_t(c2) * 2 + rank) * 4 + quad;
-          if (ld_acquire_u64(f) != sk.epoch) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_u64(f) != sk.epoch) {
-              __nanosleep(100);
-              if (*abort_flag) {
-                ok = false;
-                break;
-              }
-              if (globaltimer_ns() - t0 > limit_ns) {
-                wait_give_up(wc, 7);
-                ok = false;
-                break;
+            for (int q = 0; q < 8; ++q)
+              __stcg(d4 + q, make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                         __uint_as_float(r[4 * q + 2]),
+                                         __uint_as_float(r[4 * q + 3])));
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0)
+            st_release_u64(sk.flags + (size_t(sc.cluster) * 2 + rank) * 4 + quad, sk.epoch);
+        } else {
+          // K segment from 0: this pair finishes the tile. For a stream-K tile, the pairs
+          // cluster+1 .. last computed its other K segments; wait for their partials.
+          int last = sc.cluster;
+          if (u.ts >= 0) last = int(((int64_t(u.ts) + 1) * sc.num_kb - 1) / sc.W);
+          for (int c2 = sc.cluster + 1; ok && c2 <= last; ++c2) {
+            const uint64_t* f = sk.flags + (size_t(c2) * 2 + rank) * 4 + quad;
+            if (ld_acquire_u64(f) != sk.epoch) {
+              const uint64_t t0 = globaltimer_ns();
+              while (ld_acquire_u64(f) != sk.epoch) {
+                __nanosleep(100);
+                if (*abort_flag) {
+                  ok = false;
+                  break;
+                }
+                if (globaltimer_ns() - t0 > limit_ns) {
+                  wait_give_up(wc, 7);
+                  ok = false;
+                  break;
+                }
               }
             }
           }
-        }
-        ok = __all_sync(0xffffffffu, ok);
+          ok = __all_sync(0xffffffffu, ok);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col0 = n0 + c * 32;
-          if (col0 >= ep.N) break;
-          uint32_t r[32];
-          tmem_ld32(taddr + uint32_t(c * 32), r);
-          tmem_ld_wait(r);
-          if (!ok) continue;
-          float v[32];
+          for (int c = 0; c < BN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= ep.N) break;
+            uint32_t r[32];
+            tmem_ld32(taddr + uint32_t(c * 32), r);
+            tmem_ld_wait(r);
+            if (!ok) continue;
+            float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          for (int c2 = sc.cluster + 1; c2 <= last; ++c2) {
-            const float4* p4 = reinterpret_cast<const float4*>(
-                sk.partials + size_t(c2) * (2 * 128 * BN) + part_off + c * 32);
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            for (int c2 = sc.cluster + 1; c2 <= last; ++c2) {
+              const float4* p4 = reinterpret_cast<const float4*>(
+                  sk.partials + size_t(c2) * (2 * 128 * BN) + part_off + c * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 pv = __ldcg(p4 + q);
-              v[4 * q] += pv.x;
-              v[4 * q + 1] += pv.y;
-              v[4 * q + 2] += pv.z;
-              v[4 * q + 3] += pv.w;
+              for (int q = 0; q < 8; ++q) {
+                const float4 pv = __ldcg(p4 + q);
+                v[4 * q] += pv.x;
+                v[4 * q + 1] += pv.y;
+                v[4 * q + 2] += pv.z;
+                v[4 * q + 3] += pv.w;
+              }
             }
+            if (KIND == kEpiGrad)
+              grad_store_warp(ep, row - int(lane), col0, v, epi_stage);
+            else
+              epilogue32<KIND>(ep, row, col0, v, ss);
           }
-          if (KIND == kEpiGrad)
-            grad_store_warp(ep, row - int(lane), col0, v, epi_stage);
-          else
-            epilogue32<KIND>(ep, row, col0, v, ss);
+          // Each flag has exactly one reader, this warp: clear what it consumed, so the
+          // flags are zero again when the launch ends. A later launch that carries the same
+          // epoch value (a repeated launch of identical parameters) then cannot take them
+          // for its own. (After a wait that gave up the flags are left as they are; the
+          // status word reports that launch.)
+          if (ok && lane == 0)
+            for (int c2 = sc.cluster + 1; c2 <= last; ++c2)
+              sk.flags[(size_t(c2) * 2 + rank) * 4 + quad] = 0;
         }
-        // Each flag has exactly one reader, this warp: clear what it consumed, so the
-        // flags are zero again when the launch ends. A later launch that carries the same
-        // epoch value (a repeated launch of identical parameters) then cannot take them
-        // for its own. (After a wait that gave up the flags are left as they are; the
-        // status word reports that launch.)
-        if (ok && lane == 0)
-          for (int c2 = sc.cluster + 1; c2 <= last; ++c2)
-            sk.flags[(size_t(c2) * 2 + rank) * 4 + quad] = 0;
       }
       tc_fence_before();
       __syncwarp();
@@ -856,8 +890,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         else
           mbar_arrive_remote(mapa_shared(tempty0 + 8 * acc, 0));
       }
-      acc ^= 1;
-      if (acc == 0) acc_par ^= 1;
+      if (MT == 1) {
+        acc ^= 1;
+        if (acc == 0) acc_par ^= 1;
+      } else {
+        acc_par ^= 1;
+      }
     }
     // the warp's TMA stores must have read their buffers, and landed, before the CTA ends
     if (ss.n > 0 && lane == 0) bulk_wait_all();
@@ -884,10 +922,14 @@ uint64_t next_epoch() {
   return e == 0 ? ++counter : e;
 }
 
-template <int KIND, int OP, int LAYOUT = kKK>
+// Stream-K tiles of a two-M-tile launch: at most this many pairs share one tile along K.
+constexpr int kSkMaxSplit = 16;
+
+template <int KIND, int OP, int LAYOUT = kKK, int MT = 1>
 cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
                         const EpiParams& ep, int num_sms, int* status, uint64_t limit_ns,
                         void* sk_scratch, cudaStream_t stream) {
+  constexpr size_t SMEM_BYTES = Geo<MT>::SMEM_BYTES;
   static PerDeviceInit setup;  // per device: shared-memory opt-in and co-resident pairs
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -903,7 +945,7 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   const cudaError_t attr_err = per_device_init(
       setup,
       [&](int dev, int* out) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, OP, LAYOUT>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, OP, LAYOUT, MT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(SMEM_BYTES));
         if (e != cudaSuccess) return e;
@@ -913,28 +955,38 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
         cudaLaunchConfig_t occ = cfg;
         occ.gridDim = dim3(2 * (sms / 2), 1, 1);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, OP, LAYOUT>, &occ);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND, OP, LAYOUT, MT>, &occ);
         *out = (e == cudaSuccess && n > 0) ? n : 0;
         return e;
       },
       &max_clusters);
   if (attr_err != cudaSuccess) return attr_err;
   if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
-  const int tiles = ((M + PM - 1) / PM) * ((N + BN - 1) / BN);
-  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  const int units = ((M + MT * PM - 1) / (MT * PM)) * ((N + BN - 1) / BN);
+  const int clusters = units < max_clusters ? units : max_clusters;
   const int bke = OP == kOpE4m3 ? kGemmBK8 : BK;
   const int num_kb = (K + bke - 1) / bke;
-  // Stream-K for the last waves when they would leave pairs idle: every full wave but one
-  // runs whole tiles; the remaining (clusters + rem) tiles are split evenly along K.
+  // Stream-K for the last waves when they would leave pairs idle. MT = 1: every full wave
+  // but one runs whole tiles; the remaining (clusters + rem) tiles are split evenly along
+  // K. MT = 2: every full wave runs whole 512-row units (the traffic saving holds there);
+  // the rem units left over are split into their 256-row tiles, and those along K, over at
+  // most kSkMaxSplit pairs per tile.
   SkParams sk{};
-  sk.dp_tiles = tiles;
-  const int rem = tiles % clusters;
-  if (sk_scratch != nullptr && clusters <= kSkMaxClusters && tiles > clusters && rem != 0 &&
+  sk.dp_tiles = units;
+  const int rem = units % clusters;
+  if (sk_scratch != nullptr && clusters <= kSkMaxClusters && units > clusters && rem != 0 &&
       num_kb >= 8) {
-    sk.sk_tiles = clusters + rem;
-    sk.dp_tiles = tiles - sk.sk_tiles;
+    int sk_pairs = clusters;
+    if (MT == 1) {
+      sk.sk_tiles = clusters + rem;
+      sk.dp_tiles = units - sk.sk_tiles;
+    } else {
+      sk.sk_tiles = MT * rem;
+      sk.dp_tiles = units - rem;
+      if (sk.sk_tiles * kSkMaxSplit < sk_pairs) sk_pairs = sk.sk_tiles * kSkMaxSplit;
+    }
     const int64_t iters = int64_t(sk.sk_tiles) * num_kb;
-    sk.W = int((iters + clusters - 1) / clusters);
+    sk.W = int((iters + sk_pairs - 1) / sk_pairs);
     sk.partials = static_cast<float*>(sk_scratch);
     sk.flags = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(sk_scratch) +
                                            size_t(kSkMaxClusters) * kSkPartialBytes);
@@ -945,12 +997,19 @@ cudaError_t launch_kind(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, i
   e.N = N;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, OP, LAYOUT>, tmA, tmB, K, e, sk, status, limit_ns);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, OP, LAYOUT, MT>, tmA, tmB, K, e, sk, status,
+                            limit_ns);
 }
+
+// Two M tiles per unit for the K-major GEMMs whose M spans at least two 256-row tiles and
+// whose K is long: the shared B stage cuts operand traffic per FLOP by a quarter, and under
+// the power limit the lower traffic keeps the SM clock higher; the accumulator is not
+// double-buffered, so the epilogue must be small next to a unit's main loop.
+inline bool two_m_tiles(int M, int K) { return M > PM && K >= 16384; }
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return SMEM_BYTES; }
+size_t gemm_smem_bytes() { return Geo<1>::SMEM_BYTES; }
 
 namespace {
 // The bounded wait of the kernels above, on a barrier that never completes.
@@ -976,17 +1035,19 @@ cudaError_t launch_gemm(EpiKind kind, OpType op, const CUtensorMap& tmA, const C
                         uint64_t limit_ns, void* sk_scratch, cudaStream_t stream) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (K % (op == kOpE4m3 ? kGemmBK8 : kGemmBK) != 0) return cudaErrorInvalidValue;
+#define PB_GEMM_OP(KIND_, OP_)                                                                 \
+  return two_m_tiles(M, K) ? launch_kind<KIND_, OP_, kKK, 2>(tmA, tmB, M, N, K, ep, num_sms,     \
+                                                          status, limit_ns, sk_scratch, stream) \
+                        : launch_kind<KIND_, OP_, kKK, 1>(tmA, tmB, M, N, K, ep, num_sms,     \
+                                                          status, limit_ns, sk_scratch, stream)
 #define PB_GEMM_CASE(KIND_)                                                                    \
   switch (op) {                                                                                \
     case kOpF16:                                                                               \
-      return launch_kind<KIND_, kOpF16>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,      \
-                                        sk_scratch, stream);                                   \
+      PB_GEMM_OP(KIND_, kOpF16);                                                               \
     case kOpE4m3:                                                                              \
-      return launch_kind<KIND_, kOpE4m3>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,     \
-                                         sk_scratch, stream);                                  \
+      PB_GEMM_OP(KIND_, kOpE4m3);                                                              \
     default:                                                                                   \
-      return launch_kind<KIND_, kOpBf16>(tmA, tmB, M, N, K, ep, num_sms, status, limit_ns,     \
-                                         sk_scratch, stream);                                  \
+      PB_GEMM_OP(KIND_, kOpBf16);                                                              \
   }
   switch (kind) {
     case kEpiStore:
@@ -999,6 +1060,7 @@ cudaError_t launch_gemm(EpiKind kind, OpType op, const CUtensorMap& tmA, const C
       break;
   }
 #undef PB_GEMM_CASE
+#undef PB_GEMM_OP
   return cudaErrorInvalidValue;
 }
 
