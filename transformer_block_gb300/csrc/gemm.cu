@@ -73,7 +73,8 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // |error| <= 1.5e-7 (about 5e-7 in fp32; the GeLU error stays below 2e-4 of its value
 // where |GeLU| > 1e-3, a tenth of a bf16 step). With q = 1 - erf(|z| / sqrt 2),
 // GeLU(z) = z - z q / 2 for z >= 0 and z q / 2 below.
-__device__ __forceinline__ void gelu_pair(float& z0, float& z1) {
+// For a packed pair z: q = 1 - erf(|z| / sqrt 2) and e = exp(-z^2 / 2).
+__device__ __forceinline__ void erfc_terms(float z0, float z1, uint64_t& q, uint64_t& e) {
   constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f,
                   kA3 = 1.421413741f, kA4 = -1.453152027f, kA5 = 1.061405429f;
   constexpr float kRsqrt2 = 0.70710678118654752f, kLog2e = 1.4426950408889634f;
@@ -88,18 +89,36 @@ __device__ __forceinline__ void gelu_pair(float& z0, float& z1) {
   poly = f2_mul(poly, t);
   float g0, g1;
   f2_split(f2_mul(f2_mul(x, x), f2(-kLog2e, -kLog2e)), g0, g1);
-  const uint64_t q = f2_mul(poly, f2(ex2_approx(g0), ex2_approx(g1)));
+  e = f2(ex2_approx(g0), ex2_approx(g1));
+  q = f2_mul(poly, e);
+}
+
+__device__ __forceinline__ void gelu_pair(float& z0, float& z1) {
+  uint64_t q, e;
+  erfc_terms(z0, z1, q, e);
   float h0, h1;
   f2_split(f2_mul(f2_mul(f2(z0, z1), f2(0.5f, 0.5f)), q), h0, h1);
   z0 = z0 >= 0.f ? z0 - h0 : h0;
   z1 = z1 >= 0.f ? z1 - h1 : h1;
 }
 
-// d gelu / dz = Phi(z) + z phi(z), phi the standard normal density.
-__device__ __forceinline__ float gelu_erf_grad(float z) {
-  return 0.5f * (1.0f + erff(z * 0.70710678118654752f)) +
-         z * __expf(-0.5f * z * z) * 0.39894228040143268f;
+// d0, d1 times GeLU'(z) = Phi(z) + z phi(z), phi the standard normal density
+// exp(-z^2 / 2) / sqrt(2 pi), with Phi from the same erf terms.
+__device__ __forceinline__ void gelu_grad_pair(float& d0, float& d1, float z0, float z1) {
+  constexpr float kRsqrt2pi = 0.39894228040143268f;
+  uint64_t q, e;
+  erfc_terms(z0, z1, q, e);
+  float q0, q1, e0, e1;
+  f2_split(q, q0, q1);
+  f2_split(e, e0, e1);
+  const float p0 = z0 >= 0.f ? 1.f - 0.5f * q0 : 0.5f * q0;
+  const float p1 = z1 >= 0.f ? 1.f - 0.5f * q1 : 0.5f * q1;
+  float g0, g1;
+  f2_split(f2_fma(f2(z0 * kRsqrt2pi, z1 * kRsqrt2pi), e, f2(p0, p1)), g0, g1);
+  d0 *= g0;
+  d1 *= g1;
 }
+
 
 template <int N>
 __device__ __forceinline__ void load_bf16(const __nv_bfloat16* src, float (&v)[N]) {
@@ -365,7 +384,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
         // in the second GEMM's A operand
         float o[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = v[i] / (1.0f + __expf(-v[i])) * v[16 + i];
+        for (int i = 0; i < 16; ++i) o[i] = v[i] * rcp_approx(1.0f + __expf(-v[i])) * v[16 + i];
         const int64_t off = int64_t(row) * (H + ep.F) + H + (cc - 3 * H) / 2;
         if (ep.act_f16) {
           bool bad = false;
@@ -413,7 +432,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
       float h[32];
       load_bf16<32>(hp + f0, h);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= gelu_erf_grad(h[i]);
+      for (int i = 0; i < 32; i += 2) gelu_grad_pair(v[i], v[i + 1], h[i], h[i + 1]);
       store_row32<false>(dz + f0, v);
     } else {
       // features f0 .. f0 + 31 are the interleave groups f0 / 16 and f0 / 16 + 1: W1cat
@@ -427,7 +446,7 @@ __device__ __forceinline__ void epilogue32(const EpiParams& ep, int row, int col
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float d = v[16 * half + i];
-          const float sg = 1.0f / (1.0f + __expf(-g[i]));
+          const float sg = rcp_approx(1.0f + __expf(-g[i]));
           du[i] = d * g[i] * sg;
           dg[i] = d * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
         }
