@@ -21,7 +21,9 @@ from transformer_block_gb300 import pb
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 12288, 1024), (4160, 2080, 512)])
+# (4096, 5120, 16384): a long K, where the GEMM works in units of two 256-row M tiles and
+# splits the leftover units into their tiles for stream-K.
+@pytest.mark.parametrize("M,N,K", [(2048, 12288, 1024), (4160, 2080, 512), (4096, 5120, 16384)])
 def test_static_scratch_gemm_matches_caller_scratch_gemm(M, N, K):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
