@@ -178,7 +178,8 @@ class OracleSample:
             self.params.append({k: v.float().cpu().numpy() for k, v in p.items()})
             del p
         self.x = x.float().cpu().numpy().reshape(1, P, wl.hidden).astype(np.float64)
-        self.dims = O.Dims(1, P, wl.hidden, wl.heads, wl.head_dim, wl.ffn, wl.window, wl.ln_eps)
+        self.dims = O.Dims(1, P, wl.hidden, wl.heads, wl.head_dim, wl.ffn, wl.window, wl.ln_eps,
+                           getattr(wl, "variant", 0))
         self.rows = P
         self.work = wl.layers * (flops.gemm_flops(sub)
                                  + 4 * wl.hidden * flops.windowed_pairs(P, wl.window))

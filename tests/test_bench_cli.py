@@ -25,3 +25,13 @@ def test_reference_arm_json_line():
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"] == "tiny"
+
+
+def test_reference_arm_runs_the_swiglu_variant():
+    # The oracle sample takes the workload's block variant (RMSNorm + SwiGLU: w1 is [H, 2F]).
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny-swiglu", "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    d = json.loads([l for l in out.stdout.splitlines() if l.strip()][-1])
+    assert d["value"] > 0 and d["config"]["workload"] == "tiny-swiglu"
