@@ -67,13 +67,11 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-// GeLU(z) = z Phi(z) = z (1 + erf(z / sqrt 2)) / 2 on a packed pair, with erf from
-// Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.26: for x >= 0,
-// 1 - erf(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2), t = 1 / (1 + p x),
-// |error| <= 1.5e-7 (about 5e-7 in fp32; the GeLU error stays below 2e-4 of its value
-// where |GeLU| > 1e-3, a tenth of a bf16 step). With q = 1 - erf(|z| / sqrt 2),
-// GeLU(z) = z - z q / 2 for z >= 0 and z q / 2 below.
-// For a packed pair z: q = 1 - erf(|z| / sqrt 2) and e = exp(-z^2 / 2).
+// The GeLU epilogues take erf from Abramowitz & Stegun, Handbook of Mathematical
+// Functions, 7.1.26: for x >= 0, 1 - erf(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5)
+// exp(-x^2) with t = 1 / (1 + p x), |error| <= 1.5e-7 (about 5e-7 in fp32; GeLU then stays
+// within 2e-4 of its value where |GeLU| > 1e-3, a tenth of a bf16 step). For a packed pair
+// z: q = 1 - erf(|z| / sqrt 2) and e = exp(-z^2 / 2).
 __device__ __forceinline__ void erfc_terms(float z0, float z1, uint64_t& q, uint64_t& e) {
   constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f,
                   kA3 = 1.421413741f, kA4 = -1.453152027f, kA5 = 1.061405429f;
@@ -93,6 +91,8 @@ __device__ __forceinline__ void erfc_terms(float z0, float z1, uint64_t& q, uint
   q = f2_mul(poly, e);
 }
 
+// GeLU(z) = z Phi(z) = z (1 + erf(z / sqrt 2)) / 2 on a packed pair: with q as above,
+// z - z q / 2 for z >= 0 and z q / 2 below.
 __device__ __forceinline__ void gelu_pair(float& z0, float& z1) {
   uint64_t q, e;
   erfc_terms(z0, z1, q, e);
@@ -108,9 +108,8 @@ __device__ __forceinline__ void gelu_grad_pair(float& d0, float& d1, float z0, f
   constexpr float kRsqrt2pi = 0.39894228040143268f;
   uint64_t q, e;
   erfc_terms(z0, z1, q, e);
-  float q0, q1, e0, e1;
+  float q0, q1;
   f2_split(q, q0, q1);
-  f2_split(e, e0, e1);
   const float p0 = z0 >= 0.f ? 1.f - 0.5f * q0 : 0.5f * q0;
   const float p1 = z1 >= 0.f ? 1.f - 0.5f * q1 : 0.5f * q1;
   float g0, g1;
@@ -118,7 +117,6 @@ __device__ __forceinline__ void gelu_grad_pair(float& d0, float& d1, float z0, f
   d0 *= g0;
   d1 *= g1;
 }
-
 
 template <int N>
 __device__ __forceinline__ void load_bf16(const __nv_bfloat16* src, float (&v)[N]) {
