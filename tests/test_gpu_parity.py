@@ -47,12 +47,13 @@ def test_gemm_matches_oracle(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(2048, 12288, 1024), (4160, 2080, 512),
                                    (256 * 77, 256, 640), (4096, 5120, 16384),
-                                   (4160, 2560, 16384)])
+                                   (4160, 2560, 16384), (4160, 2080, 12288)])
 def test_gemm_stream_k_matches_oracle(M, N, K):
     # Unit counts that leave a partial last wave on 76 CTA pairs, so the last units are
     # split along K (stream-K) when scratch is given; without scratch every unit is whole.
-    # K >= 16384 with M > 256: units of two 256-row tiles, the leftover units split into
-    # their tiles (4160 rows: a ragged last unit whose second tile is empty).
+    # K >= 12288 with M > 256: units of two 256-row tiles, the leftover units split into
+    # their tiles (4160 rows: a ragged last unit whose second tile is empty; 2080 columns:
+    # a ragged last column block).
     g = torch.Generator(device="cuda").manual_seed(M + N + K)
     a = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
     b = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
