@@ -214,8 +214,11 @@ def test_backward_writes_stay_inside_their_regions(w):
     assert torch.isfinite(grads["dx"].float()).all()
 
 
-def test_stream_k_gemm_stays_inside_its_scratch():
-    M, N, K = 2048, 12288, 1024  # 384 tiles on 76 pairs: the last waves are split along K
+# 2048 x 12288 x 1024: 384 tiles on 76 pairs, the last waves split along K; 4160 x 2080 x
+# 12288: units of two M tiles (long K), a ragged last unit and column block, the leftover
+# units split into their tiles
+@pytest.mark.parametrize("M,N,K", [(2048, 12288, 1024), (4160, 2080, 12288)])
+def test_stream_k_gemm_stays_inside_its_scratch(M, N, K):
     g = torch.Generator(device="cuda").manual_seed(5)
     a = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
     b = torch.randn(N, K, generator=g, device="cuda").to(torch.bfloat16)
